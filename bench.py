@@ -1,0 +1,503 @@
+#!/usr/bin/env python3
+"""MoE-layer forward benchmark on GB300 (one process per GPU).
+
+A step is one pass of the whole layer -- Route, Dispatch, the tensor-core
+expert GEMMs (FC1, FC2, and the shared expert when the workload has one) and
+Combine -- over one batch of seeded synthetic tokens, issued through the C
+ABI (include/moe.h) one stage at a time so each stage is timed with CUDA
+events on the launching stream.  L2 is flushed (a 512 MB write) before every
+step, outside the timed events.
+
+Default workload: the Mixtral-8x7B-shaped layer (T=8192, h=4096, E=8, top-2,
+SwiGLU F=14336, bf16).  With N GPUs every rank runs its own replica on its own
+tokens (weak scaling, no collective on the data path); the per-step time is
+the max over ranks.
+
+Printed line (rank 0): value = tokens/s over all ranks with inputs resident;
+e2e = the same through moe_layer_fwd with the tokens copied in from pinned host
+memory and the output copied back every step; roofline of the dominant kernel
+(FC1 grouped GEMM); cpu_baseline = the float64 CPU oracle on a bounded sample.
+`--impl reference` times that oracle alone as the reference arm.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE-layer tokens/s on 1 GB300; grouped-GEMM % bf16 peak; permute/combine % HBM"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=50)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default=None, help="workload name (default: the Mixtral-shaped layer)")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--sample-tokens", type=int, default=0, help="oracle sample size (0: auto)")
+    return p.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    return ws, int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0"))
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.rows = []
+        self.proc = None
+        self.t_on = self.t_off = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50", "-i", str(self.gpu)], stdout=subprocess.PIPE,
+                stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append((time.time(), line.strip()))
+
+    def window(self, on: bool):
+        if on:
+            self.t_on = time.time()
+        else:
+            self.t_off = time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.12)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sel = [r for t, r in self.rows if self.t_on and self.t_on - 0.06 <= t <= (self.t_off or t) + 0.06]
+        if not sel:
+            sel = [r for _, r in self.rows]
+        mhz, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in sel:
+            f = [x.strip() for x in r.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                mhz.append(float(f[1]))
+                mx = max(mx, float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not mhz:
+            return None
+        return {"sm_mhz": statistics.median(mhz), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(mhz)}
+
+
+# ---------------------------------------------------------------------------
+# the oracle on a bounded sample (cpu_baseline and the reference arm)
+# ---------------------------------------------------------------------------
+class OracleSample:
+    """Host inputs for a sample of tokens that route to few experts, so the
+    oracle only needs those experts' weights (generated on the host by the
+    same seeded generator as the device inputs)."""
+
+    def __init__(self, w, want: int):
+        import numpy as np
+        from mixture_experts_layer_softmax_gb300 import inputs
+        from oracle import moe_oracle as O
+        self.w = w
+        self.x = w.host("x")
+        self.w_r = w.host("w_r")
+        self.sel_bias = w.host("sel_bias") if w.sel_bias_std > 0 else None
+        self.gate_bias = w.gate_bias()
+        logits = O.gating_logits(self.x, self.w_r, self.gate_bias)
+        idx, probs = O.route(logits, w.K, w.score, w.renorm, self.sel_bias, w.force_balance)
+        self.routing = (logits, idx, probs)
+        # Grow an expert set token by token (in token order) while the host
+        # weights it needs stay under a budget; the sample is the tokens whose
+        # experts all lie in the set.
+        per_expert = (w.w1_rows * w.h + w.h * w.F)
+        budget = 4.0e8  # elements generated on the host
+        chosen = set()
+        for t in range(w.T):
+            new = set(idx[t].tolist()) - chosen
+            if (len(chosen) + len(new)) * per_expert > budget:
+                continue
+            chosen |= new
+            if np.isin(idx, sorted(chosen)).all(axis=1).sum() >= want:
+                break
+        toks = np.nonzero(np.isin(idx, sorted(chosen)).all(axis=1))[0]
+        self.tokens = toks[:want]
+        need = sorted(set(idx[self.tokens].ravel().tolist()))
+        R1, h, F = w.w1_rows, w.h, w.F
+        st = w.std
+        self.w1 = {e: inputs.normal((R1, h), st("w1"), w.seed, inputs.TAG["w1"], w.dtype, start=e * R1 * h)
+                   for e in need}
+        self.w2 = {e: inputs.normal((h, F), st("w2"), w.seed, inputs.TAG["w2"], w.dtype, start=e * h * F)
+                   for e in need}
+        self.b1 = self.b2 = None
+        if w.has_bias:
+            b1, b2 = w.host("b1"), w.host("b2")
+            self.b1, self.b2 = b1, b2
+        self.w1s = w.host("w1_shared") if w.n_shared else None
+        self.w2s = w.host("w2_shared") if w.n_shared else None
+        self.experts = need
+
+    def run(self):
+        from oracle import moe_oracle as O
+        w = self.w
+        return O.layer_fwd(self.x, self.w_r, self.w1, self.w2, w.K, w.score, w.act, b1=self.b1,
+                           b2=self.b2, w1_shared=self.w1s, w2_shared=self.w2s,
+                           tokens=self.tokens, routing=self.routing)["y"]
+
+
+def blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 0) for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return max(n)
+    except Exception:
+        pass
+    return os.cpu_count()
+
+
+def auto_sample(w):
+    per_tok = 2.0 * (w.K + w.n_shared) * (3 if w.act == 1 else 2) * w.h * w.F
+    return int(max(16, min(1024, 1.5e11 / per_tok)))
+
+
+def run_reference(args, w):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    S = args.sample_tokens or auto_sample(w)
+    samp = OracleSample(w, S)
+    for _ in range(args.warmup):
+        samp.run()
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        samp.run()
+        times.append(time.perf_counter() - t0)
+    n = len(samp.tokens)
+    ms = 1000.0 * statistics.mean(times)
+    value = n / (ms / 1000.0)
+    cores = blas_threads()
+    sample = (f"{n} tokens of {w.name} routed only to experts {samp.experts}; float64 numpy "
+              f"oracle, one sample per step")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(w),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def workload_config(w):
+    return {"workload": w.name, "T": w.T, "h": w.h, "E": w.E, "K": w.K, "F": w.F,
+            "score": "sigmoid" if w.score == 1 else "softmax",
+            "act": "swiglu" if w.act == 1 else "gelu", "n_shared": w.n_shared,
+            "routing": "force-balanced" if w.force_balance else "router",
+            "l2": "flushed before every timed step (512 MB write, outside the events)",
+            "inputs": "seeded synthetic (SplitMix64 + Box-Muller), generated on the device"}
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+def kernel_hash():
+    h = hashlib.sha256()
+    for f in ("gemm_tc.cu", "tc_ptx.cuh", "common.cuh"):
+        h.update(open(os.path.join(ROOT, "mixture_experts_layer_softmax_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def traffic_record(w):
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    try:
+        rec = json.load(open(path)).get(w.name)
+    except Exception:
+        return None
+    if not rec or rec.get("kernel_hash") != kernel_hash():
+        return None
+    return rec.get("fc1_bytes_per_launch")
+
+
+def run_ours(args, w):
+    import numpy as np
+    import torch
+    from mixture_experts_layer_softmax_gb300 import _build, inputs
+    _build.build()
+    from mixture_experts_layer_softmax_gb300 import moe as M
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    bf = torch.bfloat16 if w.dtype == "bf16" else torch.float32
+    T, h, E, K, F = w.T, w.h, w.E, w.K, w.F
+    P = T * K
+    seed = w.seed + 1000 * rank  # each replica its own tokens
+
+    def gen(role, shape, dtype, s=None):
+        t = torch.empty(shape, dtype=dtype, device=dev)
+        M.synth_normal(t, w.seed if s is None else s, inputs.TAG[role], w.std(role))
+        return t
+
+    x = gen("x", (T, h), bf, seed)
+    w_r = torch.from_numpy(w.host("w_r")).to(dev)
+    w1 = gen("w1", (E, w.w1_rows, h), bf)
+    w2 = gen("w2", (E, h, F), bf)
+    b1 = gen("b1", (E, F), bf) if w.has_bias else None
+    b2 = gen("b2", (E, h), bf) if w.has_bias else None
+    w1s = gen("w1_shared", (w.w1_rows, h), bf) if w.n_shared else None
+    w2s = gen("w2_shared", (h, F), bf) if w.n_shared else None
+    sel_bias = torch.from_numpy(w.host("sel_bias")).to(dev) if w.sel_bias_std > 0 else None
+    gb = w.gate_bias()
+    gate_bias = torch.from_numpy(gb).to(dev) if gb is not None else None
+
+    cfg = M.config_for(w)
+    ws = torch.empty(M.moe_workspace_size(cfg), dtype=torch.uint8, device=dev)
+    i32 = dict(dtype=torch.int32, device=dev)
+    idx = torch.empty(T, K, **i32)
+    prob = torch.empty(T, K, dtype=torch.float32, device=dev)
+    counts, offsets = torch.empty(E, **i32), torch.empty(E + 1, **i32)
+    dst_row, src_token = torch.empty(T, K, **i32), torch.empty(P, **i32)
+    perm_prob = torch.empty(P, dtype=torch.float32, device=dev)
+    x_perm = torch.empty(P, h, dtype=bf, device=dev)
+    a = torch.empty(P, F, dtype=bf, device=dev)
+    y_perm = torch.empty(P, h, dtype=bf, device=dev)
+    y = torch.empty(T, h, dtype=bf, device=dev)
+    if w.n_shared:
+        cs = M.make_config(T, h, 1, 1, F, cfg.dtype, cfg.score, cfg.act, 0, 0, cfg.flags)
+        soff = torch.tensor([0, T], **i32)
+        a_s = torch.empty(T, F, dtype=bf, device=dev)
+        y_s = torch.empty(T, h, dtype=bf, device=dev)
+    flush_buf = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    stages = ["route", "dispatch", "fc1", "fc2", "shared", "combine"]
+
+    def step(ev=None):
+        def mark(i):
+            if ev is not None:
+                ev[i].record(stream)
+        mark(0)
+        M.moe_router_topk(cfg, x, w_r, gate_bias, sel_bias, None, idx, prob, None, ws)
+        mark(1)
+        M.moe_permute(cfg, x, idx, prob, x_perm, counts, offsets, dst_row, src_token, perm_prob, ws)
+        mark(2)
+        M.moe_expert_fc1(cfg, x_perm, offsets, perm_prob, w1, b1, None, a)
+        mark(3)
+        M.moe_expert_fc2(cfg, a, offsets, perm_prob, w2, b2, y_perm)
+        mark(4)
+        if w.n_shared:
+            M.moe_expert_fc1(cs, x, soff, None, w1s, None, None, a_s)
+            M.moe_expert_fc2(cs, a_s, soff, None, w2s, None, y_s)
+        mark(5)
+        M.moe_unpermute_combine(cfg, y_perm, dst_row, None, y_s if w.n_shared else None, y)
+        mark(6)
+
+    launches_per_step = (1 if E <= 32 else 2) + 4 + 2 + (2 if w.n_shared else 0) + 1
+
+    for _ in range(max(args.warmup, 3)):
+        flush_buf.fill_(1)
+        step()
+    torch.cuda.synchronize()
+    st = M.moe_get_error()
+    if st != M.MOE_OK:
+        raise RuntimeError(f"device status after warm-up: {M.moe_status_string(st)}")
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    sampler.window(True)
+    t_wall = time.perf_counter()
+    for i in range(args.steps):
+        flush_buf.fill_(1)
+        step(evs[i])
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall
+    sampler.window(False)
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop()
+    st = M.moe_get_error()
+    if st != M.MOE_OK:
+        raise RuntimeError(f"device status after the timed steps: {M.moe_status_string(st)}")
+
+    per_step = [e[0].elapsed_time(e[6]) for e in evs]
+    stage_ms = {s: statistics.mean(e[i].elapsed_time(e[i + 1]) for e in evs) for i, s in enumerate(stages)}
+    ms = statistics.mean(per_step)
+    if world > 1:
+        t = torch.tensor([ms], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    value = world * T / (ms / 1000.0)
+
+    # ---- end to end through moe_layer_fwd with host buffers ----
+    e2e = None
+    if not args.no_e2e:
+        x_host = x.cpu().pin_memory()
+        y_host = torch.empty(T, h, dtype=bf).pin_memory()
+        x_in = torch.empty_like(x)
+        y_out = torch.empty_like(y)
+        ws2 = ws
+
+        def e2e_step():
+            x_in.copy_(x_host, non_blocking=True)
+            M.moe_layer_fwd(cfg, x_in, w_r, gate_bias, sel_bias, w1, b1, w2, b2, w1s, w2s, y_out,
+                            None, None, ws2)
+            y_host.copy_(y_out, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize()
+        ee = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+        if world > 1:
+            torch.distributed.barrier()
+        for i in range(args.steps):
+            flush_buf.fill_(1)
+            ee[i][0].record(stream)
+            e2e_step()
+            ee[i][1].record(stream)
+        torch.cuda.synchronize()
+        ems = statistics.mean(s.elapsed_time(t) for s, t in ee)
+        if world > 1:
+            t = torch.tensor([ems], dtype=torch.float64, device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            ems = float(t.item())
+        esz = 2 if w.dtype == "bf16" else 4
+        e2e = {"value": world * T / (ems / 1000.0), "unit": "tokens/s",
+               "h2d_bytes_per_step": T * h * esz, "d2h_bytes_per_step": T * h * esz,
+               "ms_per_step": ems}
+
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
+
+    pk, pk_kind = peaks()
+    esz = 2 if w.dtype == "bf16" else 4
+    fc1_flops = 2.0 * P * h * w.w1_rows
+    fc2_flops = 2.0 * P * F * h
+    fc1_s = stage_ms["fc1"] / 1000.0
+    fc1_tf = fc1_flops / fc1_s / 1e12
+    gemm_tf = (fc1_flops + fc2_flops) / ((stage_ms["fc1"] + stage_ms["fc2"]) / 1000.0) / 1e12
+    perm_bytes = T * h * esz + P * h * esz
+    comb_bytes = P * h * esz + T * h * esz + (T * h * esz if w.n_shared else 0)
+    perm_gbs = perm_bytes / (stage_ms["dispatch"] / 1000.0) / 1e9
+    comb_gbs = comb_bytes / (stage_ms["combine"] / 1000.0) / 1e9
+    peak_tf = pk["bf16_tflops_sustained"]
+    rec = traffic_record(w)
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "f32",
+        "data": "synthetic", "config": workload_config(w),
+        "roofline": {"kernel": "grouped_gemm_tc_kernel<SwiGLU FC1>", "bound": "tensor",
+                     "achieved": fc1_tf, "peak": peak_tf, "unit": "TFLOP/s", "frac": fc1_tf / peak_tf,
+                     "peak_kind": f"{pk_kind} bf16 sustained", "traffic": rec,
+                     "flops_per_launch": fc1_flops, "ms_per_launch": stage_ms["fc1"]},
+        "grouped_gemm_pct_bf16_peak": 100.0 * gemm_tf / peak_tf,
+        "grouped_gemm_tflops": gemm_tf,
+        "permute_pct_hbm": 100.0 * perm_gbs / pk["hbm_gbs"],
+        "combine_pct_hbm": 100.0 * comb_gbs / pk["hbm_gbs"],
+        "stages_ms": stage_ms,
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+        "e2e": e2e,
+        "wall_s_timed": t_wall,
+    }
+    if not args.no_cpu_baseline:
+        S = args.sample_tokens or auto_sample(w)
+        samp = OracleSample(w, S)
+        t0 = time.perf_counter()
+        reps = 0
+        ref = None
+        while True:
+            ref = samp.run()
+            reps += 1
+            if time.perf_counter() - t0 > 10.0 or reps >= 50:
+                break
+        el = time.perf_counter() - t0
+        n = len(samp.tokens)
+        line["cpu_baseline"] = {
+            "value": reps * n / el, "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
+            "sample": f"{n} tokens of the timed workload routed only to experts {samp.experts}, "
+                      f"float64 oracle repeated {reps}x ({el:.1f} s)"}
+        # correctness column: the same tokens from the GPU output of the last step
+        gpu_rows = y[torch.from_numpy(samp.tokens).to(dev)].float().cpu().numpy().astype(np.float64)
+        err = float(np.abs(gpu_rows - ref).max())
+        bound = 2e-2 * float(np.abs(ref).max()) + 1e-3
+        line["check"] = {"tokens": n, "max_abs_err": err, "bound": bound, "ok": err <= bound}
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def main():
+    args = parse()
+    from mixture_experts_layer_softmax_gb300 import workloads
+    w = workloads.ALL[args.workload] if args.workload else workloads.MIXTRAL
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_ours(args, w)
+
+
+if __name__ == "__main__":
+    main()

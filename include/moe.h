@@ -1,0 +1,207 @@
+/*
+ * moe.h -- C ABI of the GB300 (sm_103a) single-GPU Mixture-of-Experts layer.
+ *
+ * The layer pass follows "Scalable Training of Mixture-of-Experts Models with
+ * Megatron Core" (paper review page), §2.1 "MoE layer architecture and forward
+ * pass": Route -> Dispatch -> Expert computation -> Combine, with the router of
+ * §2.2 and the grouped expert GEMM of §4.3.1.  The layer computes
+ *
+ *     p(x) = Score(W_r^T x + b_r)                        (review §1.1, §2.2)
+ *     MoE(x) = sum_{i in TopK} p_i(x) E_i(x)  [+ S(x)]   (review §1.1)
+ *
+ * Conventions shared by every entry point:
+ *  - Pointers named as device buffers are device pointers (cudaMalloc'd or
+ *    torch-allocated).  The caller owns every buffer; no call allocates device
+ *    memory.  Scratch lives in a caller-provided workspace of
+ *    moe_workspace_size(cfg) bytes (256-byte aligned).
+ *  - All calls are asynchronous on `stream` (a cudaStream_t, NULL = the legacy
+ *    default stream) and never synchronise or read device memory on the host,
+ *    except moe_get_error.  Per-expert counts and offsets stay on the device.
+ *  - Argument errors return MOE_ERR_INVALID_ARG / MOE_ERR_UNSUPPORTED /
+ *    MOE_ERR_WORKSPACE before anything is enqueued.  A failed launch returns
+ *    MOE_ERR_CUDA.  Conditions found on the device (a bounded wait that gave
+ *    up) are recorded in a per-device status word read by moe_get_error.
+ *  - Layouts are row-major.  "act" tensors (x, expert weights, biases,
+ *    x_perm, y_perm, y) have the config's dtype (fp32 or bf16); the router
+ *    weight, router biases, logits and probabilities are always fp32; index
+ *    tensors are int32.  Row strides are the dense widths stated per argument.
+ *  - Alignment: every buffer must be 16-byte aligned; bf16 configs need h and
+ *    F to be multiples of 8 and fp32 configs multiples of 4 (16-byte rows).
+ *  - Limits: 1 <= E <= 256, 1 <= K <= min(E, 16), T*K < 2^31, n_shared 0 or 1.
+ *    SwiGLU experts are bias-free.  Anything else: MOE_ERR_UNSUPPORTED.
+ *
+ * Shapes (P = T*K permuted rows; R1 = 2F for SwiGLU, F for GELU):
+ *   x [T,h]  w_r [E,h] (the review's W_r in R^{h x E}, stored transposed)
+ *   w1 [E][R1][h] (SwiGLU: rows 0..F-1 gate, F..2F-1 up)   b1 [E][F]
+ *   w2 [E][h][F]   b2 [E][h]   w1_shared [R1][h]   w2_shared [h][F]
+ */
+#ifndef MOE_GB300_H_
+#define MOE_GB300_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef void* moe_stream_t; /* cudaStream_t */
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,   /* null pointer, bad size, misaligned buffer   */
+  MOE_ERR_UNSUPPORTED = 2,   /* valid but outside this library's limits     */
+  MOE_ERR_WORKSPACE = 3,     /* workspace missing or smaller than required  */
+  MOE_ERR_CUDA = 4,          /* a CUDA runtime/driver call or launch failed */
+  MOE_ERR_TIMEOUT = 5,       /* a bounded device-side wait gave up          */
+  MOE_ERR_DEVICE_BOUNDS = 6  /* a device-side index check failed            */
+} moe_status_t;
+
+typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype_t;
+typedef enum { MOE_SCORE_SOFTMAX = 0, MOE_SCORE_SIGMOID = 1 } moe_score_t;
+typedef enum { MOE_ACT_GELU = 0, MOE_ACT_SWIGLU = 1 } moe_act_t;
+
+enum {
+  /* Divide the selected experts' scores by their sum (the skill page
+   * "emerging-techniques-moe-training", "Top-2 Routing (Mixtral)").  Without
+   * it: softmax is the full softmax over E at the selected experts, sigmoid is
+   * normalised over all E (review §2.2). */
+  MOE_FLAG_RENORM = 1u,
+  /* Force-balanced routing (review §2.2): slot k of token t goes to expert
+   * (t*K + k) mod E; probs are the scores at those experts. */
+  MOE_FLAG_FORCE_BALANCE = 2u,
+  /* Validate arguments and return without enqueuing anything. */
+  MOE_FLAG_VALIDATE_ONLY = 8u,
+  /* moe_layer_fwd keeps, in the workspace, what moe_layer_bwd needs. */
+  MOE_FLAG_SAVE_FOR_BWD = 16u,
+  /* Use the SIMT grouped GEMM for bf16 too (slow; a cross-check path). */
+  MOE_FLAG_GEMM_SIMT = 32u
+};
+
+typedef struct {
+  int32_t T;        /* tokens                                   */
+  int32_t h;        /* hidden size                              */
+  int32_t E;        /* routed experts                           */
+  int32_t K;        /* experts per token (top-k)                */
+  int32_t F;        /* expert FFN width (per SwiGLU branch)     */
+  int32_t dtype;    /* moe_dtype_t of activations and weights   */
+  int32_t score;    /* moe_score_t                              */
+  int32_t act;      /* moe_act_t                                */
+  int32_t has_bias; /* experts carry b1, b2 (GELU only)         */
+  int32_t n_shared; /* 0 or 1 always-on shared expert           */
+  uint32_t flags;   /* MOE_FLAG_*                               */
+} moe_config_t;
+
+/* Bytes of workspace every call below needs for `cfg` (the same figure for
+ * all of them; it grows with MOE_FLAG_SAVE_FOR_BWD).  0 if cfg is invalid. */
+size_t moe_workspace_size(const moe_config_t* cfg);
+
+/* Route (review §2.2 "Gating" and "Top-k selection"; §5.1 keeps the router
+ * in FP32).  Computes l = W_r^T x + b_r in fp32, selects the K experts with
+ * the largest key (softmax: l + sel_bias; sigmoid: fp32(sigma(l)) + sel_bias,
+ * sigma evaluated in double), ties to the lower expert index, listed in
+ * descending key order, and their probabilities.
+ *   x [T,h] dtype; w_r [E,h] f32; gate_bias [E] f32 or NULL (b_r);
+ *   sel_bias [E] f32 or NULL (selection only, never enters p);
+ *   logits [T,E] f32 out or NULL; topk_idx [T,K] i32 out; topk_prob [T,K] f32 out;
+ *   routing_map [T,E] u8 out or NULL (1 where selected). */
+moe_status_t moe_router_topk(const moe_config_t* cfg, const void* x, const float* w_r,
+                             const float* gate_bias, const float* sel_bias, float* logits,
+                             int32_t* topk_idx, float* topk_prob, uint8_t* routing_map,
+                             void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* The scoring / top-k / normalisation half of the router on given fp32
+ * logits [T,E]; same outputs and rules as moe_router_topk. */
+moe_status_t moe_router_topk_from_logits(const moe_config_t* cfg, const float* logits,
+                                         const float* sel_bias, int32_t* topk_idx,
+                                         float* topk_prob, uint8_t* routing_map,
+                                         moe_stream_t stream);
+
+/* Dispatch (review §2.1 "Dispatch"; permutation fusion, §4.3.1): the T*K
+ * (token, slot) pairs in expert-contiguous order, tokens ascending within an
+ * expert.  counts[e] = pairs routed to e; offsets = exclusive prefix sum
+ * (E+1 entries); dst_row[t,k] = offsets[e] + #{t' < t routed to e};
+ * src_token[r] / perm_prob[r] invert it; x_perm[dst_row[t,k]] = x[t].
+ *   x [T,h]; topk_idx [T,K]; topk_prob [T,K] or NULL (then perm_prob unused);
+ *   outputs x_perm [P,h] (NULL: maps only), counts [E], offsets [E+1],
+ *   dst_row [T,K], src_token [P], perm_prob [P] or NULL.
+ * Bit-exact and deterministic (no atomics decide a position). */
+moe_status_t moe_permute(const moe_config_t* cfg, const void* x, const int32_t* topk_idx,
+                         const float* topk_prob, void* x_perm, int32_t* counts, int32_t* offsets,
+                         int32_t* dst_row, int32_t* src_token, float* perm_prob, void* ws,
+                         size_t ws_bytes, moe_stream_t stream);
+
+/* Expert computation (review §2.1 "Expert computation": every expert in one
+ * grouped GEMM call; §4.1.1 memory-efficient permutation).  For every row r
+ * of expert e (offsets[e] <= r < offsets[e+1]):
+ *   bias-free:  a = p_r * phi(x_perm[r] W1_e^T),   y_perm[r] = a W2_e^T
+ *   biased:     a = GELU(x_perm[r] W1_e^T + b1_e), y_perm[r] = p_r (a W2_e^T + b2_e)
+ * phi = silu(gate) * up (SwiGLU) or GELU (exact erf); p_r = perm_prob[r]
+ * (NULL: 1).  bf16 runs on the tensor cores (tcgen05, fp32 accumulate),
+ * fp32 on the SIMT FMA units.
+ *   x_perm [P,h]; offsets [E+1] device; w1, b1, w2, b2 as above;
+ *   act_save [P,R1] out or NULL: the pre-activation x_perm W1^T (+ b1);
+ *   y_perm [P,h] out. */
+moe_status_t moe_grouped_mlp_fwd(const moe_config_t* cfg, const void* x_perm,
+                                 const int32_t* offsets, const float* perm_prob, const void* w1,
+                                 const void* b1, const void* w2, const void* b2, void* act_save,
+                                 void* y_perm, void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* The two halves of moe_grouped_mlp_fwd, one grouped GEMM launch each.
+ * FC1: a[r] = p_r * phi(x_perm[r] W1_e^T) (bias-free experts) or
+ *      a[r] = GELU(x_perm[r] W1_e^T + b1_e) (biased experts);
+ *      act_save [P,R1] out or NULL (pre-activation); a [P,F] out.
+ * FC2: y_perm[r] = a[r] W2_e^T (bias-free) or p_r (a[r] W2_e^T + b2_e). */
+moe_status_t moe_expert_fc1(const moe_config_t* cfg, const void* x_perm, const int32_t* offsets,
+                            const float* perm_prob, const void* w1, const void* b1,
+                            void* act_save, void* a, moe_stream_t stream);
+moe_status_t moe_expert_fc2(const moe_config_t* cfg, const void* a, const int32_t* offsets,
+                            const float* perm_prob, const void* w2, const void* b2,
+                            void* y_perm, moe_stream_t stream);
+
+/* Combine (review §2.1 "Combine"; the skill page's index_add_):
+ *   y[t] = sum_{k=0}^{K-1} w[t,k] * y_perm[dst_row[t,k]]  (+ shared_y[t])
+ * with w = topk_prob, or 1 when topk_prob is NULL (probabilities already
+ * applied in the expert GEMM).  fp32 accumulation in fixed k order, rounded
+ * once: bitwise deterministic.
+ *   y_perm [P,h]; dst_row [T,K]; topk_prob [T,K] or NULL; shared_y [T,h] or NULL;
+ *   y [T,h] out. */
+moe_status_t moe_unpermute_combine(const moe_config_t* cfg, const void* y_perm,
+                                   const int32_t* dst_row, const float* topk_prob,
+                                   const void* shared_y, void* y, moe_stream_t stream);
+
+/* The whole forward layer pass: Route, Dispatch, grouped expert GEMMs (plus
+ * the shared expert when n_shared = 1, weight 1, not routed), Combine.
+ *   y [T,h] out; topk_idx_out [T,K] and topk_prob_out [T,K] optional copies of
+ *   the routing.  With MOE_FLAG_SAVE_FOR_BWD the workspace keeps the routing,
+ *   maps and activations for moe_layer_bwd. */
+moe_status_t moe_layer_fwd(const moe_config_t* cfg, const void* x, const float* w_r,
+                           const float* gate_bias, const float* sel_bias, const void* w1,
+                           const void* b1, const void* w2, const void* b2,
+                           const void* w1_shared, const void* w2_shared, void* y,
+                           int32_t* topk_idx_out, float* topk_prob_out, void* ws,
+                           size_t ws_bytes, moe_stream_t stream);
+
+/* Bytes of host-visible state: none.  Reports (and clears) the per-device
+ * status word written by device-side checks, after synchronising `stream`.
+ * Returns MOE_OK, MOE_ERR_TIMEOUT, MOE_ERR_DEVICE_BOUNDS or MOE_ERR_CUDA. */
+moe_status_t moe_get_error(moe_stream_t stream);
+
+/* A static string naming a status code. */
+const char* moe_status_string(moe_status_t status);
+
+/* Library version, "major.minor.patch". */
+const char* moe_version(void);
+
+/* Test hook for the bounded-wait machinery: launches one block that waits on
+ * an mbarrier nothing will ever complete, with the same bounded wait the
+ * tensor-core GEMM uses, capped at `max_polls` polls.  The kernel gives up,
+ * records MOE_ERR_TIMEOUT in the status word and returns; read it with
+ * moe_get_error.  Never faults or hangs the device. */
+moe_status_t moe_test_bounded_wait(int64_t max_polls, moe_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_GB300_H_ */

@@ -1,0 +1,373 @@
+// The C ABI (include/moe.h): argument validation, workspace carving and the
+// order of the layer's steps.  Host code here only validates and enqueues; it
+// never reads device memory or synchronises (except moe_get_error).
+#include <mutex>
+
+#include "common.cuh"
+
+namespace moe {
+cudaError_t launch_router(const moe_config_t&, const void*, const float*, const float*,
+                          const float*, float*, int32_t*, float*, uint8_t*, cudaStream_t);
+cudaError_t launch_router_select(const moe_config_t&, const float*, const float*, int32_t*,
+                                 float*, uint8_t*, cudaStream_t);
+cudaError_t launch_permute_maps(const moe_config_t&, const int32_t*, const float*, int32_t*,
+                                int32_t*, int32_t*, int32_t*, int32_t*, int32_t*, float*, int*,
+                                cudaStream_t);
+cudaError_t launch_scatter_rows(const moe_config_t&, const void*, const int32_t*, void*, int,
+                                int*, cudaStream_t);
+cudaError_t launch_combine(const moe_config_t&, const void*, const int32_t*, const float*,
+                           const void*, void*, int, int*, cudaStream_t);
+cudaError_t launch_expert_gemm_simt(const moe_config_t&, int, int, const void*, const int32_t*,
+                                    const float*, const void*, const void*, void*, void*,
+                                    cudaStream_t);
+cudaError_t launch_expert_gemm_tc(const moe_config_t&, int, int, const void*, const int32_t*,
+                                  const float*, const void*, const void*, void*, void*, int, int*,
+                                  cudaStream_t);
+cudaError_t launch_bounded_wait_probe(int64_t, int*, cudaStream_t);
+}  // namespace moe
+
+using namespace moe;
+
+// Per-device status word: device-side checks record the first error here.
+__device__ int g_moe_status = 0;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+  int* status = nullptr;
+  int sms = 0;
+  bool ready = false;
+};
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+// Status-word address and SM count of the current device (looked up once per
+// device, with that device current).
+const DeviceInfo* device_info() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(g_dev_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.ready) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_moe_status) != cudaSuccess) return nullptr;
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return nullptr;
+    d.status = static_cast<int*>(p);
+    d.sms = sms;
+    d.ready = true;
+  }
+  return &d;
+}
+
+bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+moe_status_t check_config(const moe_config_t* c) {
+  if (!c) return MOE_ERR_INVALID_ARG;
+  if (c->T < 0 || c->h < 1 || c->E < 1 || c->K < 1 || c->F < 1) return MOE_ERR_INVALID_ARG;
+  if (c->K > c->E) return MOE_ERR_INVALID_ARG;
+  if (c->dtype != MOE_F32 && c->dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
+  if (c->score != MOE_SCORE_SOFTMAX && c->score != MOE_SCORE_SIGMOID) return MOE_ERR_INVALID_ARG;
+  if (c->act != MOE_ACT_GELU && c->act != MOE_ACT_SWIGLU) return MOE_ERR_INVALID_ARG;
+  if ((c->has_bias != 0 && c->has_bias != 1) || (c->n_shared != 0 && c->n_shared != 1))
+    return MOE_ERR_INVALID_ARG;
+  const uint32_t known = MOE_FLAG_RENORM | MOE_FLAG_FORCE_BALANCE | MOE_FLAG_VALIDATE_ONLY |
+                         MOE_FLAG_SAVE_FOR_BWD | MOE_FLAG_GEMM_SIMT;
+  if (c->flags & ~known) return MOE_ERR_INVALID_ARG;
+  if (c->E > 256 || c->K > 16) return MOE_ERR_UNSUPPORTED;
+  if (c->act == MOE_ACT_SWIGLU && c->has_bias) return MOE_ERR_UNSUPPORTED;
+  const int vec = c->dtype == MOE_BF16 ? 8 : 4;
+  if (c->h % vec || c->F % vec) return MOE_ERR_UNSUPPORTED;
+  const int64_t R1 = c->act == MOE_ACT_SWIGLU ? 2LL * c->F : c->F;
+  if ((int64_t)c->T * c->K >= (1LL << 31) || (int64_t)c->E * R1 >= (1LL << 31) ||
+      (int64_t)c->E * c->h >= (1LL << 31))
+    return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+moe_status_t check_ws(const moe_config_t* c, const void* ws, size_t ws_bytes) {
+  const size_t need = workspace_layout(*c).total;
+  if (need == 0) return MOE_OK;
+  if (!ws || ws_bytes < need) return MOE_ERR_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(ws) & 255u) return MOE_ERR_INVALID_ARG;
+  return MOE_OK;
+}
+
+template <typename T> T* at(void* ws, size_t off) {
+  return reinterpret_cast<T*>(static_cast<char*>(ws) + off);
+}
+
+moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+__global__ void fill_shared_offsets(int32_t* off, int T) {
+  off[0] = 0;
+  off[1] = T;
+}
+
+bool use_tensor_cores(const moe_config_t& c) {
+  return c.dtype == MOE_BF16 && !(c.flags & MOE_FLAG_GEMM_SIMT);
+}
+
+cudaError_t run_expert_gemm(const moe_config_t& c, int fc, int rows, const void* A,
+                            const int32_t* offsets, const float* prob, const void* w,
+                            const void* bias, void* act_save, void* out, const DeviceInfo* d,
+                            cudaStream_t s) {
+  if (use_tensor_cores(c))
+    return launch_expert_gemm_tc(c, fc, rows, A, offsets, prob, w, bias, act_save, out, d->sms,
+                                 d->status, s);
+  return launch_expert_gemm_simt(c, fc, rows, A, offsets, prob, w, bias, act_save, out, s);
+}
+
+cudaError_t run_grouped_mlp(const moe_config_t& c, int rows, const void* x_perm,
+                            const int32_t* offsets, const float* prob, const void* w1,
+                            const void* b1, const void* w2, const void* b2, void* act_save,
+                            void* a, void* y_perm, const DeviceInfo* d, cudaStream_t s) {
+  cudaError_t e = run_expert_gemm(c, 1, rows, x_perm, offsets, prob, w1, b1, act_save, a, d, s);
+  if (e != cudaSuccess) return e;
+  return run_expert_gemm(c, 2, rows, a, offsets, prob, w2, b2, nullptr, y_perm, d, s);
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t moe_workspace_size(const moe_config_t* cfg) {
+  if (check_config(cfg) != MOE_OK) return 0;
+  return workspace_layout(*cfg).total;
+}
+
+moe_status_t moe_router_topk(const moe_config_t* cfg, const void* x, const float* w_r,
+                             const float* gate_bias, const float* sel_bias, float* logits,
+                             int32_t* topk_idx, float* topk_prob, uint8_t* routing_map, void* ws,
+                             size_t ws_bytes, moe_stream_t stream) {
+  moe_status_t st = check_config(cfg);
+  if (st != MOE_OK) return st;
+  if (cfg->T > 0 && (!x || !w_r || !topk_idx || !topk_prob)) return MOE_ERR_INVALID_ARG;
+  if (!al16(x) || !al16(w_r)) return MOE_ERR_INVALID_ARG;
+  const bool need_ws_logits = !logits && cfg->E > 32;
+  if (need_ws_logits && (st = check_ws(cfg, ws, ws_bytes)) != MOE_OK) return st;
+  if (cfg->flags & MOE_FLAG_VALIDATE_ONLY) return MOE_OK;
+  if (cfg->T == 0) return MOE_OK;
+  float* lg = logits ? logits : (need_ws_logits ? at<float>(ws, workspace_layout(*cfg).logits)
+                                                : nullptr);
+  return cuda_status(launch_router(*cfg, x, w_r, gate_bias, sel_bias, lg, topk_idx, topk_prob,
+                                   routing_map, static_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_router_topk_from_logits(const moe_config_t* cfg, const float* logits,
+                                         const float* sel_bias, int32_t* topk_idx,
+                                         float* topk_prob, uint8_t* routing_map,
+                                         moe_stream_t stream) {
+  moe_status_t st = check_config(cfg);
+  if (st != MOE_OK) return st;
+  if (cfg->T > 0 && (!logits || !topk_idx || !topk_prob)) return MOE_ERR_INVALID_ARG;
+  if (cfg->flags & MOE_FLAG_VALIDATE_ONLY) return MOE_OK;
+  if (cfg->T == 0) return MOE_OK;
+  return cuda_status(launch_router_select(*cfg, logits, sel_bias, topk_idx, topk_prob,
+                                          routing_map, static_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_permute(const moe_config_t* cfg, const void* x, const int32_t* topk_idx,
+                         const float* topk_prob, void* x_perm, int32_t* counts, int32_t* offsets,
+                         int32_t* dst_row, int32_t* src_token, float* perm_prob, void* ws,
+                         size_t ws_bytes, moe_stream_t stream) {
+  moe_status_t st = check_config(cfg);
+  if (st != MOE_OK) return st;
+  if (!counts || !offsets) return MOE_ERR_INVALID_ARG;
+  if (cfg->T > 0 && (!topk_idx || !dst_row || !src_token)) return MOE_ERR_INVALID_ARG;
+  if ((x == nullptr) != (x_perm == nullptr)) return MOE_ERR_INVALID_ARG;
+  if (!al16(x) || !al16(x_perm)) return MOE_ERR_INVALID_ARG;
+  if ((st = check_ws(cfg, ws, ws_bytes)) != MOE_OK) return st;
+  if (cfg->flags & MOE_FLAG_VALIDATE_ONLY) return MOE_OK;
+  const DeviceInfo* d = device_info();
+  if (!d) return MOE_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const Workspace w = workspace_layout(*cfg);
+  cudaError_t e = launch_permute_maps(*cfg, topk_idx, topk_prob, at<int32_t>(ws, w.hist),
+                                      at<int32_t>(ws, w.chunk_base), counts, offsets, dst_row,
+                                      src_token, perm_prob, d->status, s);
+  if (e == cudaSuccess && x) e = launch_scatter_rows(*cfg, x, dst_row, x_perm, d->sms, d->status, s);
+  return cuda_status(e);
+}
+
+moe_status_t moe_grouped_mlp_fwd(const moe_config_t* cfg, const void* x_perm,
+                                 const int32_t* offsets, const float* perm_prob, const void* w1,
+                                 const void* b1, const void* w2, const void* b2, void* act_save,
+                                 void* y_perm, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  moe_status_t st = check_config(cfg);
+  if (st != MOE_OK) return st;
+  if (!x_perm || !offsets || !w1 || !w2 || !y_perm) return MOE_ERR_INVALID_ARG;
+  if (cfg->has_bias && (!b1 || !b2)) return MOE_ERR_INVALID_ARG;
+  if (!al16(x_perm) || !al16(w1) || !al16(w2) || !al16(y_perm) || !al16(act_save))
+    return MOE_ERR_INVALID_ARG;
+  if ((st = check_ws(cfg, ws, ws_bytes)) != MOE_OK) return st;
+  if (cfg->flags & MOE_FLAG_VALIDATE_ONLY) return MOE_OK;
+  const DeviceInfo* d = device_info();
+  if (!d) return MOE_ERR_CUDA;
+  const Workspace w = workspace_layout(*cfg);
+  const int P = cfg->T * cfg->K;
+  return cuda_status(run_grouped_mlp(*cfg, P, x_perm, offsets, perm_prob, w1,
+                                     cfg->has_bias ? b1 : nullptr, w2,
+                                     cfg->has_bias ? b2 : nullptr, act_save,
+                                     at<void>(ws, w.a), y_perm, d,
+                                     static_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_expert_fc1(const moe_config_t* cfg, const void* x_perm, const int32_t* offsets,
+                            const float* perm_prob, const void* w1, const void* b1,
+                            void* act_save, void* a, moe_stream_t stream) {
+  moe_status_t st = check_config(cfg);
+  if (st != MOE_OK) return st;
+  if (!x_perm || !offsets || !w1 || !a) return MOE_ERR_INVALID_ARG;
+  if (cfg->has_bias && !b1) return MOE_ERR_INVALID_ARG;
+  if (!al16(x_perm) || !al16(w1) || !al16(a) || !al16(act_save)) return MOE_ERR_INVALID_ARG;
+  if (cfg->flags & MOE_FLAG_VALIDATE_ONLY) return MOE_OK;
+  const DeviceInfo* d = device_info();
+  if (!d) return MOE_ERR_CUDA;
+  return cuda_status(run_expert_gemm(*cfg, 1, cfg->T * cfg->K, x_perm, offsets, perm_prob, w1,
+                                     cfg->has_bias ? b1 : nullptr, act_save, a, d,
+                                     static_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_expert_fc2(const moe_config_t* cfg, const void* a, const int32_t* offsets,
+                            const float* perm_prob, const void* w2, const void* b2,
+                            void* y_perm, moe_stream_t stream) {
+  moe_status_t st = check_config(cfg);
+  if (st != MOE_OK) return st;
+  if (!a || !offsets || !w2 || !y_perm) return MOE_ERR_INVALID_ARG;
+  if (cfg->has_bias && !b2) return MOE_ERR_INVALID_ARG;
+  if (!al16(a) || !al16(w2) || !al16(y_perm)) return MOE_ERR_INVALID_ARG;
+  if (cfg->flags & MOE_FLAG_VALIDATE_ONLY) return MOE_OK;
+  const DeviceInfo* d = device_info();
+  if (!d) return MOE_ERR_CUDA;
+  return cuda_status(run_expert_gemm(*cfg, 2, cfg->T * cfg->K, a, offsets, perm_prob, w2,
+                                     cfg->has_bias ? b2 : nullptr, nullptr, y_perm, d,
+                                     static_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_unpermute_combine(const moe_config_t* cfg, const void* y_perm,
+                                   const int32_t* dst_row, const float* topk_prob,
+                                   const void* shared_y, void* y, moe_stream_t stream) {
+  moe_status_t st = check_config(cfg);
+  if (st != MOE_OK) return st;
+  if (cfg->T > 0 && (!y_perm || !dst_row || !y)) return MOE_ERR_INVALID_ARG;
+  if (!al16(y_perm) || !al16(shared_y) || !al16(y)) return MOE_ERR_INVALID_ARG;
+  if (cfg->flags & MOE_FLAG_VALIDATE_ONLY) return MOE_OK;
+  const DeviceInfo* d = device_info();
+  if (!d) return MOE_ERR_CUDA;
+  return cuda_status(launch_combine(*cfg, y_perm, dst_row, topk_prob, shared_y, y, d->sms,
+                                    d->status, static_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_layer_fwd(const moe_config_t* cfg, const void* x, const float* w_r,
+                           const float* gate_bias, const float* sel_bias, const void* w1,
+                           const void* b1, const void* w2, const void* b2,
+                           const void* w1_shared, const void* w2_shared, void* y,
+                           int32_t* topk_idx_out, float* topk_prob_out, void* ws,
+                           size_t ws_bytes, moe_stream_t stream) {
+  moe_status_t st = check_config(cfg);
+  if (st != MOE_OK) return st;
+  const moe_config_t& c = *cfg;
+  if (c.T > 0 && (!x || !w_r || !w1 || !w2 || !y)) return MOE_ERR_INVALID_ARG;
+  if (c.has_bias && (!b1 || !b2)) return MOE_ERR_INVALID_ARG;
+  if (c.n_shared && (!w1_shared || !w2_shared)) return MOE_ERR_INVALID_ARG;
+  if (!al16(x) || !al16(w_r) || !al16(w1) || !al16(w2) || !al16(y) || !al16(w1_shared) ||
+      !al16(w2_shared))
+    return MOE_ERR_INVALID_ARG;
+  if ((st = check_ws(cfg, ws, ws_bytes)) != MOE_OK) return st;
+  if (c.flags & MOE_FLAG_VALIDATE_ONLY) return MOE_OK;
+  if (c.T == 0) return MOE_OK;
+  const DeviceInfo* d = device_info();
+  if (!d) return MOE_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const Workspace w = workspace_layout(c);
+  const bool save = (c.flags & MOE_FLAG_SAVE_FOR_BWD) != 0;
+  int32_t* idx = at<int32_t>(ws, w.topk_idx);
+  float* prob = at<float>(ws, w.topk_prob);
+  int32_t* offsets = at<int32_t>(ws, w.offsets);
+  int32_t* dst_row = at<int32_t>(ws, w.dst_row);
+  float* perm_prob = at<float>(ws, w.perm_prob);
+  // Route
+  cudaError_t e = launch_router(c, x, w_r, gate_bias, sel_bias, at<float>(ws, w.logits), idx,
+                                prob, nullptr, s);
+  // Dispatch
+  if (e == cudaSuccess)
+    e = launch_permute_maps(c, idx, prob, at<int32_t>(ws, w.hist), at<int32_t>(ws, w.chunk_base),
+                            at<int32_t>(ws, w.counts), offsets, dst_row,
+                            at<int32_t>(ws, w.src_token), perm_prob, d->status, s);
+  if (e == cudaSuccess)
+    e = launch_scatter_rows(c, x, dst_row, at<void>(ws, w.x_perm), d->sms, d->status, s);
+  // Expert computation
+  if (e == cudaSuccess)
+    e = run_grouped_mlp(c, c.T * c.K, at<void>(ws, w.x_perm), offsets, perm_prob, w1, b1, w2, b2,
+                        save ? at<void>(ws, w.act_save) : nullptr, at<void>(ws, w.a),
+                        at<void>(ws, w.y_perm), d, s);
+  const void* shared_y = nullptr;
+  if (e == cudaSuccess && c.n_shared) {
+    moe_config_t cs = c;  // one always-on expert over all T tokens, weight 1
+    cs.E = 1;
+    cs.K = 1;
+    cs.has_bias = 0;
+    int32_t* soff = at<int32_t>(ws, w.shared_off);
+    fill_shared_offsets<<<1, 1, 0, s>>>(soff, c.T);
+    e = cudaGetLastError();
+    if (e == cudaSuccess)
+      e = run_grouped_mlp(cs, c.T, x, soff, nullptr, w1_shared, nullptr, w2_shared, nullptr,
+                          save ? at<void>(ws, w.shared_h) : nullptr, at<void>(ws, w.shared_a),
+                          at<void>(ws, w.shared_y), d, s);
+    shared_y = at<void>(ws, w.shared_y);
+  }
+  // Combine (probabilities were applied inside the expert GEMMs)
+  if (e == cudaSuccess)
+    e = launch_combine(c, at<void>(ws, w.y_perm), dst_row, nullptr, shared_y, y, d->sms,
+                       d->status, s);
+  if (e == cudaSuccess && topk_idx_out)
+    e = cudaMemcpyAsync(topk_idx_out, idx, sizeof(int32_t) * c.T * c.K, cudaMemcpyDeviceToDevice, s);
+  if (e == cudaSuccess && topk_prob_out)
+    e = cudaMemcpyAsync(topk_prob_out, prob, sizeof(float) * c.T * c.K, cudaMemcpyDeviceToDevice, s);
+  return cuda_status(e);
+}
+
+moe_status_t moe_get_error(moe_stream_t stream) {
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+  const DeviceInfo* d = device_info();
+  if (!d) return MOE_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpy(&v, d->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (v != 0) {
+    const int zero = 0;
+    if (cudaMemcpy(d->status, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
+      return MOE_ERR_CUDA;
+  }
+  return static_cast<moe_status_t>(v);
+}
+
+const char* moe_status_string(moe_status_t s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported configuration";
+    case MOE_ERR_WORKSPACE: return "workspace missing or too small";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_TIMEOUT: return "device-side wait timed out";
+    case MOE_ERR_DEVICE_BOUNDS: return "device-side index out of range";
+  }
+  return "unknown status";
+}
+
+const char* moe_version(void) { return "0.1.0"; }
+
+moe_status_t moe_test_bounded_wait(int64_t max_polls, moe_stream_t stream) {
+  if (max_polls < 1) return MOE_ERR_INVALID_ARG;
+  const DeviceInfo* d = device_info();
+  if (!d) return MOE_ERR_CUDA;
+  return cuda_status(
+      launch_bounded_wait_probe(max_polls, d->status, static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

@@ -1,0 +1,435 @@
+// Grouped expert GEMMs on the 5th-generation tensor cores (tcgen05 + TMEM),
+// operands staged by TMA.  bf16 in, fp32 accumulate, bf16 out.
+//
+// "Scalable Training of Mixture-of-Experts Models with Megatron Core" (review),
+// §2.1 "Expert computation" (every local expert in one grouped GEMM call) and
+// §4.3.1 (grouped GEMM); §4.1.1 memory-efficient permutation: for bias-free
+// experts the routing weight p scales the activation in the FC1 epilogue, so
+// FC2 is a plain GEMM; with expert biases p scales the FC2 output instead.
+//
+// One persistent CTA per SM walks a device-side tile list (no host sync: the
+// per-expert row offsets are read on the device, review §4.3.3).  Tiles are
+// 128 rows x 256 accumulator columns; an expert's rows start a new tile, so a
+// tile never mixes experts (rows past the expert's end are computed and
+// dropped).  Tiles are ordered expert by expert, m fastest, so the CTAs that
+// run at the same time share one weight panel and one activation panel in L2.
+//
+// Warp roles (192 threads):
+//   warp 0      TMA producer: 4-stage ring of {A 128x64, B 256x64} bf16 tiles
+//               (128-byte swizzle), completion on mbarriers (expect_tx).
+//   warp 1      TMEM owner and MMA issuer: tcgen05.mma M128 N256 K16, fp32
+//               accumulators in TMEM, double buffered (2 x 256 columns), so the
+//               epilogue of tile i overlaps the main loop of tile i+1.
+//   warps 2-5   epilogue: tcgen05.ld 32 lanes x 32 columns, activation / bias /
+//               probability, bf16 stores.
+// SwiGLU FC1 tiles load 128 gate rows and the matching 128 up rows of W1, so
+// silu(gate) * up is formed from two columns of the same thread's TMEM lane.
+//
+// Every wait is bounded (time limit); a wait that gives up records
+// MOE_ERR_TIMEOUT, every role leaves its loop, the producer waits (bounded) for
+// its copies in flight, the MMA issuer for its MMAs, and TMEM is freed.
+#include <mutex>
+
+#include "tc_ptx.cuh"
+
+namespace moe {
+
+namespace {
+
+constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;  // 16 KB
+constexpr int B_BYTES = BN * BK * 2;  // 32 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr int kThreads = 192;
+
+enum TcMode { kTcSwiGLU = 0, kTcGelu = 1, kTcFc2 = 2 };
+
+struct TcParams {
+  const int32_t* offsets;        // [E+1]
+  const float* prob;             // [P] or null
+  const __nv_bfloat16* bias;     // GELU FC1: b1 [E][N]; FC2: b2 [E][N]; or null
+  __nv_bfloat16* out;            // [P, N]
+  __nv_bfloat16* act_save;       // [P, Nb] or null (FC1 only)
+  int E, Kd, N, Nb;              // output columns N; B rows per expert Nb
+  int prob_here;                 // apply p in this epilogue
+  int* status;
+  uint64_t wait_limit_ns;
+};
+
+struct SmemCtl {
+  uint64_t full[STAGES], empty[STAGES], tmem_full[2], tmem_empty[2], drain;
+  uint32_t tmem_base;
+  int abort;
+  int tile_start[257];
+  int off[257];
+};
+
+constexpr size_t kSmemBytes = 1024 + (size_t)STAGES * STAGE_BYTES + sizeof(SmemCtl);
+
+MOE_D void decode_tile(const SmemCtl& c, int E, int nblk, int tile, int& e, int& mb, int& nb) {
+  int lo = 0, hi = E - 1;  // largest e with tile_start[e] <= tile
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (c.tile_start[mid] <= tile) lo = mid; else hi = mid - 1;
+  }
+  e = lo;
+  const int local = tile - c.tile_start[e];
+  const int mblk = (c.off[e + 1] - c.off[e] + BM - 1) / BM;
+  nb = local / mblk;
+  mb = local - nb * mblk;
+}
+
+MOE_D uint32_t pack_bf16x2(float a, float b) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+MOE_D void store8(__nv_bfloat16* dst, const float* v) {
+  uint4 u;
+  u.x = pack_bf16x2(v[0], v[1]);
+  u.y = pack_bf16x2(v[2], v[3]);
+  u.z = pack_bf16x2(v[4], v[5]);
+  u.w = pack_bf16x2(v[6], v[7]);
+  *reinterpret_cast<uint4*>(dst) = u;
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(kThreads, 1)
+    grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
+                           const __grid_constant__ CUtensorMap tmB, const TcParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + STAGES * A_BYTES;
+  SmemCtl& ctl = *reinterpret_cast<SmemCtl*>(smem + STAGES * STAGE_BYTES);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int E = p.E;
+  const int nblk = MODE == kTcSwiGLU ? (p.N + BN / 2 - 1) / (BN / 2) : (p.N + BN - 1) / BN;
+  const int KB = (p.Kd + BK - 1) / BK;
+
+  // ---- prologue: barriers, TMEM, tile list ----
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      tc::mbar_init(tc::smem_u32(&ctl.full[s]), 1);
+      tc::mbar_init(tc::smem_u32(&ctl.empty[s]), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      tc::mbar_init(tc::smem_u32(&ctl.tmem_full[a]), 1);
+      tc::mbar_init(tc::smem_u32(&ctl.tmem_empty[a]), 4);
+    }
+    tc::mbar_init(tc::smem_u32(&ctl.drain), 1);
+    ctl.abort = 0;
+    tc::fence_barrier_init();
+    tc::fence_proxy_async_smem();
+    tc::prefetch_tensormap(&tmA);
+    tc::prefetch_tensormap(&tmB);
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(tc::smem_u32(&ctl.tmem_base), TMEM_COLS);
+    tc::tmem_relinquish();
+  }
+  for (int e = threadIdx.x; e <= E; e += kThreads) ctl.off[e] = __ldg(p.offsets + e);
+  __syncthreads();
+  if (warp == 2) {  // tile_start = exclusive scan of m-blocks x n-blocks
+    int running = 0;
+    for (int e0 = 0; e0 < E; e0 += 32) {
+      const int e = e0 + lane;
+      const int v = e < E ? ((ctl.off[e + 1] - ctl.off[e] + BM - 1) / BM) * nblk : 0;
+      int incl = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+      }
+      if (e < E) ctl.tile_start[e] = running + incl - v;
+      running += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) ctl.tile_start[E] = running;
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem_base = ctl.tmem_base;
+  const int total = ctl.tile_start[E];
+  tc::WaitCtl wc{p.status, &ctl.abort, p.wait_limit_ns, 0};
+  tc::WaitCtl wdrain{p.status, nullptr, 1000000000ull, 0};
+
+  if (warp == 0) {
+    // ================= TMA producer =================
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0, issued = 0, issued_par = 0;
+      for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+        int e, mb, nb;
+        decode_tile(ctl, E, nblk, tile, e, mb, nb);
+        const int a_row = ctl.off[e] + mb * BM;
+        int b_row0, b_row1 = 0;
+        if (MODE == kTcSwiGLU) {
+          b_row0 = e * p.Nb + nb * (BN / 2);
+          b_row1 = e * p.Nb + p.N + nb * (BN / 2);
+        } else {
+          b_row0 = e * p.Nb + nb * BN;
+        }
+        bool ok = true;
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!tc::mbar_wait(tc::smem_u32(&ctl.empty[stage]), phase ^ 1, wc)) { ok = false; break; }
+          const uint32_t fb = tc::smem_u32(&ctl.full[stage]);
+          tc::mbar_arrive_expect_tx(fb, STAGE_BYTES);
+          const uint32_t a_dst = tc::smem_u32(sA + stage * A_BYTES);
+          const uint32_t b_dst = tc::smem_u32(sB + stage * B_BYTES);
+          tc::tma_load_2d(a_dst, &tmA, kb * BK, a_row, fb);
+          if (MODE == kTcSwiGLU) {
+            tc::tma_load_2d(b_dst, &tmB, kb * BK, b_row0, fb);
+            tc::tma_load_2d(b_dst + B_BYTES / 2, &tmB, kb * BK, b_row1, fb);
+          } else {
+            tc::tma_load_2d(b_dst, &tmB, kb * BK, b_row0, fb);
+          }
+          issued |= 1u << stage;
+          issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
+          if (++stage == STAGES) { stage = 0; phase ^= 1; }
+        }
+        if (!ok) break;
+      }
+      // copies still in flight must land before the block exits
+      for (int s = 0; s < STAGES; ++s)
+        if ((issued >> s) & 1u)
+          tc::mbar_wait(tc::smem_u32(&ctl.full[s]), (issued_par >> s) & 1u, wdrain);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ================= MMA issuer =================
+    if (lane == 0) {
+      constexpr uint32_t idesc = tc::idesc_bf16_f32(BM, BN);
+      int stage = 0, acc = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+        if (!tc::mbar_wait(tc::smem_u32(&ctl.tmem_empty[acc]), acc_phase ^ 1, wc)) break;
+        tc::fence_after_sync();
+        const uint32_t d = tmem_base + (uint32_t)(acc * BN);
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!tc::mbar_wait(tc::smem_u32(&ctl.full[stage]), phase, wc)) { ok = false; break; }
+          tc::fence_after_sync();
+          const uint32_t a0 = tc::smem_u32(sA + stage * A_BYTES);
+          const uint32_t b0 = tc::smem_u32(sB + stage * B_BYTES);
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k)
+            tc::mma_bf16(d, tc::desc_kmajor_sw128(a0 + k * 32), tc::desc_kmajor_sw128(b0 + k * 32),
+                         idesc, (kb | k) != 0);
+          tc::mma_commit(tc::smem_u32(&ctl.empty[stage]));
+          if (++stage == STAGES) { stage = 0; phase ^= 1; }
+        }
+        if (!ok) break;
+        tc::mma_commit(tc::smem_u32(&ctl.tmem_full[acc]));
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1;
+      }
+      if (ctl.abort) {  // let every issued MMA finish before TMEM is freed
+        tc::mma_commit(tc::smem_u32(&ctl.drain));
+        tc::mbar_wait(tc::smem_u32(&ctl.drain), 0, wdrain);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ================= epilogue (warps 2..5) =================
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+      int e, mb, nb;
+      decode_tile(ctl, E, nblk, tile, e, mb, nb);
+      if (!tc::mbar_wait(tc::smem_u32(&ctl.tmem_full[acc]), acc_phase, wc)) break;
+      tc::fence_after_sync();
+      const int m_e = ctl.off[e + 1] - ctl.off[e];
+      const int local_row = mb * BM + q * 32 + lane;
+      const bool valid = local_row < m_e;
+      const int64_t row = (int64_t)ctl.off[e] + local_row;
+      const float pr = (p.prob && p.prob_here && valid) ? __ldg(p.prob + row) : 1.f;
+      const uint32_t tbase = tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(q * 32) << 16);
+      if (MODE == kTcSwiGLU) {
+#pragma unroll 1
+        for (int c = 0; c < BN / 2 / 32; ++c) {
+          uint32_t g[32], u[32];
+          tc::tmem_ld_32x32b_x32(tbase + c * 32, g);
+          tc::tmem_ld_32x32b_x32(tbase + BN / 2 + c * 32, u);
+          const int n = nb * (BN / 2) + c * 32;
+          if (valid) {
+#pragma unroll
+            for (int gq = 0; gq < 4; ++gq) {
+              if (n + gq * 8 >= p.N) break;
+              float o[8], gv[8], uv[8];
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                gv[i] = __uint_as_float(g[gq * 8 + i]);
+                uv[i] = __uint_as_float(u[gq * 8 + i]);
+                o[i] = pr * (silu_f(gv[i]) * uv[i]);
+              }
+              store8(p.out + row * p.N + n + gq * 8, o);
+              if (p.act_save) {
+                store8(p.act_save + row * p.Nb + n + gq * 8, gv);
+                store8(p.act_save + row * p.Nb + p.N + n + gq * 8, uv);
+              }
+            }
+          }
+        }
+      } else {
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t r[32];
+          tc::tmem_ld_32x32b_x32(tbase + c * 32, r);
+          const int n = nb * BN + c * 32;
+          if (valid) {
+#pragma unroll
+            for (int gq = 0; gq < 4; ++gq) {
+              const int n8 = n + gq * 8;
+              if (n8 >= p.N) break;
+              float v[8], o[8];
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                v[i] = __uint_as_float(r[gq * 8 + i]);
+                if (p.bias) v[i] += __bfloat162float(p.bias[(int64_t)e * p.N + n8 + i]);
+              }
+              if (MODE == kTcGelu) {
+                if (p.act_save) store8(p.act_save + row * p.Nb + n8, v);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) o[i] = pr * gelu_f(v[i]);
+              } else {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) o[i] = pr * v[i];
+              }
+              store8(p.out + row * p.N + n8, o);
+            }
+          }
+        }
+      }
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(tc::smem_u32(&ctl.tmem_empty[acc]));
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1;
+    }
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+// ---- host side ----------------------------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  });
+  return fn;
+}
+
+// 2-D bf16 row-major [rows, cols] map with a {64, box_rows} box, 128-B swizzle.
+bool encode_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  EncodeTiledFn fn = get_encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * 2};
+  const cuuint32_t box[2] = {(cuuint32_t)BK, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int MODE>
+cudaError_t launch_mode(const CUtensorMap& a, const CUtensorMap& b, const TcParams& p, int grid,
+                        cudaStream_t s) {
+  cudaError_t e = cudaFuncSetAttribute(grouped_gemm_tc_kernel<MODE>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)kSmemBytes);
+  if (e != cudaSuccess) return e;
+  grouped_gemm_tc_kernel<MODE><<<grid, kThreads, kSmemBytes, s>>>(a, b, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+// One grouped GEMM: out[r, :] = epilogue(A[r, :] B_e^T) for the rows r of each
+// expert e.  A [P, Kd]; B [E * Nb, Kd] (bf16, row-major).
+cudaError_t launch_grouped_gemm_tc(int mode, int P, const void* A, int Kd, const void* B, int Nb,
+                                   int E, int N, const int32_t* offsets, const float* prob,
+                                   int prob_here, const void* bias, void* out, void* act_save,
+                                   int sms, int* status, cudaStream_t s) {
+  if (P == 0) return cudaSuccess;
+  CUtensorMap ma, mb;
+  if (!encode_2d(&ma, A, (uint64_t)P, (uint64_t)Kd, BM)) return cudaErrorInvalidValue;
+  const uint32_t brows = mode == kTcSwiGLU ? BN / 2 : BN;
+  if (!encode_2d(&mb, B, (uint64_t)E * Nb, (uint64_t)Kd, brows)) return cudaErrorInvalidValue;
+  TcParams p;
+  p.offsets = offsets; p.prob = prob;
+  p.bias = static_cast<const __nv_bfloat16*>(bias);
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.act_save = static_cast<__nv_bfloat16*>(act_save);
+  p.E = E; p.Kd = Kd; p.N = N; p.Nb = Nb; p.prob_here = prob_here;
+  p.status = status;
+  p.wait_limit_ns = 2000000000ull;  // 2 s: far above any real wait
+  const int nblk = mode == kTcSwiGLU ? (N + BN / 2 - 1) / (BN / 2) : (N + BN - 1) / BN;
+  const int64_t tiles_max = (ceil_div(P, BM) + E) * (int64_t)nblk;
+  const int grid = (int)(tiles_max < sms ? tiles_max : sms);
+  switch (mode) {
+    case kTcSwiGLU: return launch_mode<kTcSwiGLU>(ma, mb, p, grid, s);
+    case kTcGelu: return launch_mode<kTcGelu>(ma, mb, p, grid, s);
+    default: return launch_mode<kTcFc2>(ma, mb, p, grid, s);
+  }
+}
+
+// One of the two expert GEMMs (fc = 1: x_perm -> a, fc = 2: a -> y_perm).
+cudaError_t launch_expert_gemm_tc(const moe_config_t& c, int fc, int P, const void* A,
+                                  const int32_t* offsets, const float* prob, const void* w,
+                                  const void* bias, void* act_save, void* out, int sms,
+                                  int* status, cudaStream_t s) {
+  const bool swiglu = c.act == MOE_ACT_SWIGLU;
+  const bool prob_after = c.has_bias != 0;
+  if (fc == 1)
+    return launch_grouped_gemm_tc(swiglu ? kTcSwiGLU : kTcGelu, P, A, c.h, w,
+                                  swiglu ? 2 * c.F : c.F, c.E, c.F, offsets, prob, !prob_after,
+                                  bias, out, act_save, sms, status, s);
+  return launch_grouped_gemm_tc(kTcFc2, P, A, c.F, w, c.h, c.E, c.h, offsets, prob, prob_after,
+                                bias, out, nullptr, sms, status, s);
+}
+
+// ---- test hook: a wait nothing will complete ---------------------------------
+__global__ void bounded_wait_probe_kernel(int* status, int64_t max_polls) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    tc::mbar_init(tc::smem_u32(&bar), 1);
+    abort_flag = 0;
+    tc::fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    tc::WaitCtl w{status, &abort_flag, 1000000000ull, max_polls};
+    tc::mbar_wait(tc::smem_u32(&bar), 0, w);  // phase 0 never completes
+  }
+}
+
+cudaError_t launch_bounded_wait_probe(int64_t max_polls, int* status, cudaStream_t s) {
+  bounded_wait_probe_kernel<<<1, 32, 0, s>>>(status, max_polls);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

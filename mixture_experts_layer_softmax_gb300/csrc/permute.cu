@@ -1,0 +1,234 @@
+// Dispatch: expert-contiguous permutation of the T*K (token, slot) pairs.
+//
+// "Scalable Training of Mixture-of-Experts Models with Megatron Core" (review),
+// §2.1 "Dispatch" (tokens are permuted so each expert's rows are contiguous,
+// with per-expert counts and offsets) and §4.3.1 (permutation fusion);
+// §4.3.3 asks for sync-free kernels: counts and offsets never leave the device.
+//
+// Positions are decided without atomics, so the permutation is unique and
+// bit-reproducible: inside an expert's segment rows are in ascending token
+// order.  Tokens are cut into chunks of 32 (one warp each):
+//   1. chunk_hist:   hist[c][e] = pairs of chunk c routed to e
+//   2. chunk_scan:   base[c][e] = sum_{c' < c} hist[c'][e]; counts[e] (warp per expert)
+//   3. chunk_ranks:  offsets = exclusive scan of counts; for every pair
+//                    dst_row = offsets[e] + base[c][e] + rank inside the chunk
+//                    (ranks from ballots over the lanes' expert ids);
+//                    src_token, perm_prob are the inverse maps.
+//   4. scatter_rows: each token's row is read once and written to its K
+//                    destinations with 16-byte vectors.
+#include "common.cuh"
+
+namespace moe {
+
+constexpr int kChunk = 32;
+
+// One warp per chunk of 32 tokens; 8 warps per block.
+__global__ void __launch_bounds__(256) chunk_hist_kernel(const int32_t* __restrict__ idx, int T,
+                                                         int K, int E, int NC,
+                                                         int32_t* __restrict__ hist, int* status) {
+  extern __shared__ int32_t sh[];  // [8][E]
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int c = blockIdx.x * 8 + warp;
+  int32_t* my = sh + warp * E;
+  for (int e = lane; e < E; e += 32) my[e] = 0;
+  __syncwarp();
+  if (c < NC) {
+    const int64_t t = (int64_t)c * kChunk + lane;
+    if (t < T)
+      for (int k = 0; k < K; ++k) {
+        const int e = __ldg(idx + t * K + k);
+        if (e >= 0 && e < E)
+          atomicAdd(&my[e], 1);
+        else
+          report(status, MOE_ERR_DEVICE_BOUNDS);
+      }
+  }
+  __syncwarp();
+  if (c < NC)
+    for (int e = lane; e < E; e += 32) hist[(int64_t)c * E + e] = my[e];
+}
+
+// Warp per expert: exclusive scan of hist[:, e] over the chunks.
+__global__ void __launch_bounds__(256) chunk_scan_kernel(const int32_t* __restrict__ hist, int NC,
+                                                         int E, int32_t* __restrict__ base,
+                                                         int32_t* __restrict__ counts) {
+  const int lane = threadIdx.x & 31;
+  const int e = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (e >= E) return;
+  int running = 0;
+  for (int c0 = 0; c0 < NC; c0 += 32) {
+    const int c = c0 + lane;
+    const int v = c < NC ? __ldg(hist + (int64_t)c * E + e) : 0;
+    int incl = v;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int o = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += o;
+    }
+    if (c < NC) base[(int64_t)c * E + e] = running + incl - v;
+    running += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  if (lane == 0) counts[e] = running;
+}
+
+// Block: exclusive scan of counts into shared offsets (E <= 256), then one
+// warp per chunk computes every pair's destination row.
+__global__ void __launch_bounds__(256) chunk_ranks_kernel(
+    const int32_t* __restrict__ idx, const float* __restrict__ prob, int T, int K, int E, int NC,
+    const int32_t* __restrict__ base, const int32_t* __restrict__ counts,
+    int32_t* __restrict__ offsets_out, int32_t* __restrict__ dst_row,
+    int32_t* __restrict__ src_token, float* __restrict__ perm_prob) {
+  // expert ids outside [0, E) were reported by chunk_hist; they get no row
+  // (dst_row = -1) here.
+  __shared__ int32_t s_off[257];
+  __shared__ int32_t s_warp[8];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  {
+    // exclusive scan of counts[0..E) by the 256 threads (zero past E), so
+    // s_off[E] is the total
+    const int e = threadIdx.x;
+    const int v = e < E ? __ldg(counts + e) : 0;
+    int incl = v;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int o = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += o;
+    }
+    if (lane == 31) s_warp[warp] = incl;
+    __syncthreads();
+    int wbase = 0;
+    for (int w = 0; w < warp; ++w) wbase += s_warp[w];
+    s_off[e] = wbase + incl - v;
+    if (e == 255) s_off[256] = wbase + incl;
+    __syncthreads();
+    if (blockIdx.x == 0 && offsets_out && e <= E) offsets_out[e] = s_off[e];
+    if (blockIdx.x == 0 && offsets_out && E == 256 && e == 0) offsets_out[256] = s_off[256];
+  }
+  const int c = blockIdx.x * 8 + warp;
+  if (c >= NC) return;
+  const int64_t t = (int64_t)c * kChunk + lane;
+  const bool valid = t < T;
+  const unsigned lt_mask = (1u << lane) - 1u;
+  // rank of pair (t, k) among the chunk's earlier tokens routed to the same
+  // expert: for every slot k2, 8 ballots give the lanes' expert-id bits, and
+  // the lanes whose id equals e are the AND of matching bit masks (E <= 256).
+  int my_e[16], rank[16];
+  for (int k = 0; k < K; ++k) {
+    const int e = valid ? __ldg(idx + t * K + k) : -1;
+    my_e[k] = (e >= 0 && e < E) ? e : -1;
+    rank[k] = 0;
+  }
+  for (int k2 = 0; k2 < K; ++k2) {
+    const int v = my_e[k2];
+    const unsigned present = __ballot_sync(0xffffffffu, v >= 0);
+    unsigned bits[8];
+#pragma unroll
+    for (int b = 0; b < 8; ++b) bits[b] = __ballot_sync(0xffffffffu, (v >> b) & 1);
+    for (int k = 0; k < K; ++k) {
+      const int e = my_e[k];
+      unsigned m = present & lt_mask;
+#pragma unroll
+      for (int b = 0; b < 8; ++b) m &= ((e >> b) & 1) ? bits[b] : ~bits[b];
+      rank[k] += __popc(m);
+    }
+  }
+  if (valid) {
+    for (int k = 0; k < K; ++k) {
+      const int e = my_e[k];
+      if (e < 0) {
+        dst_row[t * K + k] = -1;
+        continue;
+      }
+      const int r = s_off[e] + __ldg(base + (int64_t)c * E + e) + rank[k];
+      dst_row[t * K + k] = r;
+      src_token[r] = (int32_t)t;
+      if (perm_prob) perm_prob[r] = prob ? __ldg(prob + t * K + k) : 1.f;
+    }
+  }
+}
+
+// One warp per token: read the row once, write it to its K destinations.
+template <typename T>
+__global__ void __launch_bounds__(256) scatter_rows_kernel(const T* __restrict__ x,
+                                                           const int32_t* __restrict__ dst_row,
+                                                           int ntok, int K, int h,
+                                                           T* __restrict__ x_perm, int* status) {
+  constexpr int V = Vec<T>::N;
+  constexpr int kMaxVec = 8;  // per lane per pass: 32 lanes x 8 x 16 B = 4 KB
+  const int lane = threadIdx.x & 31;
+  const int nvec = h / V;
+  for (int64_t t = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5); t < ntok;
+       t += (int64_t)gridDim.x * 8) {
+    int dst[16];
+    const int64_t P = (int64_t)ntok * K;
+    for (int k = 0; k < K; ++k) {
+      dst[k] = __ldg(dst_row + t * K + k);
+      if (dst[k] < 0 || dst[k] >= P) {
+        if (dst[k] >= P) report(status, MOE_ERR_DEVICE_BOUNDS);
+        dst[k] = -1;
+      }
+    }
+    const T* src = x + t * h;
+    for (int v0 = 0; v0 < nvec; v0 += 32 * kMaxVec) {
+      Vec<T> buf[kMaxVec];
+#pragma unroll
+      for (int i = 0; i < kMaxVec; ++i) {
+        const int v = v0 + i * 32 + lane;
+        if (v < nvec) buf[i] = ld16_stream(src + (int64_t)v * V);
+      }
+      for (int k = 0; k < K; ++k) {
+        if (dst[k] < 0) continue;
+        T* d = x_perm + (int64_t)dst[k] * h;
+#pragma unroll
+        for (int i = 0; i < kMaxVec; ++i) {
+          const int v = v0 + i * 32 + lane;
+          if (v < nvec) st16(d + (int64_t)v * V, buf[i]);
+        }
+      }
+    }
+  }
+}
+
+int num_chunks(int T) { return (int)ceil_div(T, kChunk); }
+
+cudaError_t launch_permute_maps(const moe_config_t& c, const int32_t* idx, const float* prob,
+                                int32_t* hist, int32_t* base, int32_t* counts, int32_t* offsets,
+                                int32_t* dst_row, int32_t* src_token, float* perm_prob,
+                                int* status, cudaStream_t s) {
+  const int NC = num_chunks(c.T);
+  if (c.T == 0) {
+    // no rows: counts and offsets are all zero
+    cudaError_t e = cudaMemsetAsync(counts, 0, sizeof(int32_t) * c.E, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(offsets, 0, sizeof(int32_t) * (c.E + 1), s);
+    return e;
+  }
+  const int blocks = (int)ceil_div(NC, 8);
+  chunk_hist_kernel<<<blocks, 256, 8 * c.E * sizeof(int32_t), s>>>(idx, c.T, c.K, c.E, NC, hist,
+                                                                  status);
+  chunk_scan_kernel<<<(unsigned)ceil_div(c.E, 8), 256, 0, s>>>(hist, NC, c.E, base, counts);
+  chunk_ranks_kernel<<<blocks, 256, 0, s>>>(idx, prob, c.T, c.K, c.E, NC, base, counts, offsets,
+                                            dst_row, src_token, perm_prob);
+  return cudaGetLastError();
+}
+
+int scatter_grid(int ntok, int sms) {
+  const int64_t need = ceil_div(ntok, 8);
+  const int64_t cap = (int64_t)sms * 8;
+  return (int)(need < cap ? (need > 0 ? need : 1) : cap);
+}
+
+cudaError_t launch_scatter_rows(const moe_config_t& c, const void* x, const int32_t* dst_row,
+                                void* x_perm, int sms, int* status, cudaStream_t s) {
+  if (c.T == 0) return cudaSuccess;
+  const int grid = scatter_grid(c.T, sms);
+  if (c.dtype == MOE_BF16)
+    scatter_rows_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(
+        static_cast<const __nv_bfloat16*>(x), dst_row, c.T, c.K, c.h,
+        static_cast<__nv_bfloat16*>(x_perm), status);
+  else
+    scatter_rows_kernel<float><<<grid, 256, 0, s>>>(static_cast<const float*>(x), dst_row, c.T,
+                                                    c.K, c.h, static_cast<float*>(x_perm), status);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,414 @@
+// Route: gating projection, scoring, top-k selection and normalisation.
+//
+// "Scalable Training of Mixture-of-Experts Models with Megatron Core" (review),
+// §2.2 "Router architecture": gating l = W_r^T x, softmax or sigmoid scoring,
+// top-k selection; balancing by a selection-only bias (aux-loss-free) or by
+// force-balanced routing; §5.1 keeps the router in FP32.  The skill page
+// "emerging-techniques-moe-training" ("Top-2 Routing (Mixtral)") divides the
+// selected scores by their sum (MOE_FLAG_RENORM).
+//
+// Kernels:
+//  * router_fused_small: E <= 32.  One block stages W_r chunks in shared
+//    memory; each warp accumulates the gating dot products of a few tokens,
+//    reduces them across the warp (31 shuffles for 32 sums), then selects
+//    top-k with warp shuffles.  One pass over x, no logits round trip.
+//  * router_gemm: E > 32.  SIMT fp32 tiled GEMM logits = x W_r^T (+ b_r).
+//  * router_select: warp per token top-k + probabilities on fp32 logits.
+#include <float.h>
+
+#include "common.cuh"
+
+namespace moe {
+
+struct RouterArgs {
+  int T, E, K, h;
+  int score;
+  bool renorm, force_balance;
+  const float* sel_bias;
+  int32_t* topk_idx;
+  float* topk_prob;
+  uint8_t* routing_map;
+};
+
+// Selection key of one (token, expert): softmax uses the logit, sigmoid uses
+// fp32(sigma(l)) with sigma evaluated in double; then + sel_bias in fp32.
+MOE_D float selection_key(float l, int e, const RouterArgs& a) {
+  float key = l;
+  if (a.score == MOE_SCORE_SIGMOID) key = (float)(1.0 / (1.0 + exp(-(double)l)));
+  if (a.sel_bias) key = __fadd_rn(key, __ldg(a.sel_bias + e));
+  return key;
+}
+
+MOE_D bool better(float ka, int ia, float kb, int ib) { return ka > kb || (ka == kb && ia < ib); }
+
+// Selects K experts for one token whose logits are spread over the warp
+// (slot j of lane l is expert l + 32 j) and writes idx/prob/routing_map.
+template <int J>
+MOE_D void select_and_write(const float (&logit)[J], int t, const RouterArgs& a, int lane) {
+  const unsigned FULL = 0xffffffffu;
+  bool taken[J];
+  float key[J];
+#pragma unroll
+  for (int j = 0; j < J; ++j) {
+    const int e = lane + 32 * j;
+    taken[j] = false;
+    key[j] = e < a.E ? selection_key(logit[j], e, a) : -FLT_MAX;
+  }
+  int my_idx = -1;      // lane k < K ends up holding the k-th selected expert
+  float my_logit = 0.f; // and its logit
+  if (a.force_balance) {
+    if (lane < a.K) my_idx = (int)(((int64_t)t * a.K + lane) % a.E);
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+      const int e = lane + 32 * j;
+      // expert e is selected iff (e - t*K) mod E < K
+      const int64_t d = (((int64_t)e - (int64_t)t * a.K) % a.E + a.E) % a.E;
+      taken[j] = e < a.E && d < a.K;
+    }
+  } else {
+    for (int k = 0; k < a.K; ++k) {
+      float bk = -INFINITY;
+      int bi = 0x7fffffff;
+#pragma unroll
+      for (int j = 0; j < J; ++j) {
+        const int e = lane + 32 * j;
+        if (e < a.E && !taken[j] && better(key[j], e, bk, bi)) {
+          bk = key[j];
+          bi = e;
+        }
+      }
+#pragma unroll
+      for (int off = 16; off >= 1; off >>= 1) {
+        const float ok = __shfl_xor_sync(FULL, bk, off);
+        const int oi = __shfl_xor_sync(FULL, bi, off);
+        if (better(ok, oi, bk, bi)) {
+          bk = ok;
+          bi = oi;
+        }
+      }
+      if ((bi & 31) == lane) taken[bi >> 5] = true;
+      if (lane == k) my_idx = bi;
+    }
+  }
+  // logit of this lane's selected expert
+  {
+    float sel_l = 0.f;
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+      // fetch logit of expert my_idx from lane my_idx & 31, slot my_idx >> 5
+      const int src = my_idx & 31;
+      const float v = __shfl_sync(FULL, logit[j], src);
+      if (my_idx >= 0 && (my_idx >> 5) == j) sel_l = v;
+    }
+    my_logit = sel_l;
+  }
+  const bool active = lane < a.K;
+  float p = 0.f;
+  if (a.score == MOE_SCORE_SOFTMAX) {
+    if (a.renorm) {
+      float m = active ? my_logit : -INFINITY;
+#pragma unroll
+      for (int off = 16; off >= 1; off >>= 1) m = fmaxf(m, __shfl_xor_sync(FULL, m, off));
+      const float ex = active ? expf(my_logit - m) : 0.f;
+      float s = ex;
+#pragma unroll
+      for (int off = 16; off >= 1; off >>= 1) s += __shfl_xor_sync(FULL, s, off);
+      p = ex / s;
+    } else {
+      float m = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < J; ++j)
+        if (lane + 32 * j < a.E) m = fmaxf(m, logit[j]);
+#pragma unroll
+      for (int off = 16; off >= 1; off >>= 1) m = fmaxf(m, __shfl_xor_sync(FULL, m, off));
+      float s = 0.f;
+#pragma unroll
+      for (int j = 0; j < J; ++j)
+        if (lane + 32 * j < a.E) s += expf(logit[j] - m);
+#pragma unroll
+      for (int off = 16; off >= 1; off >>= 1) s += __shfl_xor_sync(FULL, s, off);
+      p = expf(my_logit - m) / s;
+    }
+  } else {
+    const float sg = active ? sigmoid_f(my_logit) : 0.f;
+    float s = 0.f;
+    if (a.renorm) {
+      s = sg;
+    } else {
+#pragma unroll
+      for (int j = 0; j < J; ++j)
+        if (lane + 32 * j < a.E) s += sigmoid_f(logit[j]);
+    }
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) s += __shfl_xor_sync(FULL, s, off);
+    p = sg / s;
+  }
+  if (active) {
+    a.topk_idx[(int64_t)t * a.K + lane] = my_idx;
+    a.topk_prob[(int64_t)t * a.K + lane] = p;
+  }
+  if (a.routing_map) {
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+      const int e = lane + 32 * j;
+      if (e < a.E) a.routing_map[(int64_t)t * a.E + e] = taken[j] ? 1 : 0;
+    }
+  }
+}
+
+// ---- top-k on given logits: one warp per token --------------------------
+template <int J>
+__global__ void __launch_bounds__(256) router_select_kernel(const float* __restrict__ logits,
+                                                             RouterArgs a) {
+  const int lane = threadIdx.x & 31;
+  const int64_t t = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (t >= a.T) return;
+  float l[J];
+#pragma unroll
+  for (int j = 0; j < J; ++j) {
+    const int e = lane + 32 * j;
+    l[j] = e < a.E ? __ldg(logits + t * a.E + e) : 0.f;
+  }
+  select_and_write<J>(l, (int)t, a, lane);
+}
+
+// ---- fused gating + top-k for E <= 32 ------------------------------------
+// EP: padded expert count (8, 16 or 32); TPW = 32 / EP tokens per warp, so a
+// warp reduces exactly 32 partial sums.
+template <typename Tin, int EP>
+__global__ void __launch_bounds__(256) router_fused_small_kernel(
+    const Tin* __restrict__ x, const float* __restrict__ w_r, const float* __restrict__ gate_bias,
+    float* __restrict__ logits_out, RouterArgs a, int hc) {
+  constexpr int TPW = 32 / EP;
+  constexpr int kWarps = 8;
+  extern __shared__ float sw[];  // [EP][hc] chunk of W_r
+  __shared__ float s_logit[kWarps][TPW][EP];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int64_t t0 = ((int64_t)blockIdx.x * kWarps + warp) * TPW;
+  float acc[TPW * EP];
+#pragma unroll
+  for (int i = 0; i < TPW * EP; ++i) acc[i] = 0.f;
+
+  for (int c0 = 0; c0 < a.h; c0 += hc) {
+    const int cw = min(hc, a.h - c0);
+    __syncthreads();
+    for (int i = threadIdx.x * 4; i < EP * hc; i += blockDim.x * 4) {
+      const int e = i / hc, c = i % hc;
+      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (e < a.E && c < cw) v = __ldg(reinterpret_cast<const float4*>(w_r + (int64_t)e * a.h + c0 + c));
+      *reinterpret_cast<float4*>(sw + e * hc + c) = v;
+    }
+    __syncthreads();
+    // each lane takes 4 consecutive columns, the warp strides by 128
+    for (int c = lane * 4; c < cw; c += 128) {
+      float wv[EP][4];
+#pragma unroll
+      for (int e = 0; e < EP; ++e) {
+        const float4 q = *reinterpret_cast<const float4*>(sw + e * hc + c);
+        wv[e][0] = q.x; wv[e][1] = q.y; wv[e][2] = q.z; wv[e][3] = q.w;
+      }
+#pragma unroll
+      for (int u = 0; u < TPW; ++u) {
+        const int64_t t = t0 + u;
+        if (t >= a.T) continue;
+        float xv[4];
+        const Tin* px = x + t * a.h + c0 + c;
+        if constexpr (sizeof(Tin) == 2) {
+          const uint2 r = __ldg(reinterpret_cast<const uint2*>(px));
+          const __nv_bfloat162 p0 = *reinterpret_cast<const __nv_bfloat162*>(&r.x);
+          const __nv_bfloat162 p1 = *reinterpret_cast<const __nv_bfloat162*>(&r.y);
+          xv[0] = __low2float(p0); xv[1] = __high2float(p0);
+          xv[2] = __low2float(p1); xv[3] = __high2float(p1);
+        } else {
+          const float4 r = __ldg(reinterpret_cast<const float4*>(px));
+          xv[0] = r.x; xv[1] = r.y; xv[2] = r.z; xv[3] = r.w;
+        }
+#pragma unroll
+        for (int e = 0; e < EP; ++e)
+#pragma unroll
+          for (int q = 0; q < 4; ++q) acc[u * EP + e] = fmaf(xv[q], wv[e][q], acc[u * EP + e]);
+      }
+    }
+  }
+  // 32 sums across 32 lanes in 31 shuffles: lane l ends with sum #l.
+  const unsigned FULL = 0xffffffffu;
+#pragma unroll
+  for (int off = 16, n = 32; off >= 1; off >>= 1, n >>= 1) {
+    const bool upper = (lane & off) != 0;
+#pragma unroll
+    for (int i = 0; i < n / 2; ++i) {
+      const float send = upper ? acc[i] : acc[i + n / 2];
+      const float keep = upper ? acc[i + n / 2] : acc[i];
+      acc[i] = keep + __shfl_xor_sync(FULL, send, off);
+    }
+  }
+  {
+    const int u = lane / EP, e = lane % EP;
+    float v = acc[0];
+    if (gate_bias && e < a.E) v += __ldg(gate_bias + e);
+    s_logit[warp][u][e] = v;
+    const int64_t t = t0 + u;
+    if (logits_out && t < a.T && e < a.E) logits_out[t * a.E + e] = v;
+  }
+  __syncwarp();
+#pragma unroll 1
+  for (int u = 0; u < TPW; ++u) {
+    const int64_t t = t0 + u;
+    if (t >= a.T) break;
+    float l[1] = {lane < EP ? s_logit[warp][u][lane] : 0.f};
+    select_and_write<1>(l, (int)t, a, lane);
+  }
+}
+
+// ---- SIMT fp32 gating GEMM for E > 32 -----------------------------------
+// logits[T,E] = x[T,h] W_r[E,h]^T + b_r.  64x64 tile, BK = 32, 256 threads,
+// 4x4 outputs per thread, operands transposed into shared memory.
+template <typename Tin>
+__global__ void __launch_bounds__(256) router_gemm_kernel(const Tin* __restrict__ x,
+                                                          const float* __restrict__ w_r,
+                                                          const float* __restrict__ gate_bias,
+                                                          float* __restrict__ logits, int T, int E,
+                                                          int h) {
+  constexpr int BT = 64, BE = 64, BK = 32;
+  __shared__ float xs[BK][BT + 4];
+  __shared__ float ws[BK][BE + 4];
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+  const int64_t tb = (int64_t)blockIdx.y * BT;
+  const int eb = blockIdx.x * BE;
+  float acc[4][4] = {};
+  for (int k0 = 0; k0 < h; k0 += BK) {
+    // x tile: 64 rows x 32 cols, 8 consecutive elements per thread
+    {
+      const int r = threadIdx.x >> 2, c = (threadIdx.x & 3) * 8;
+      const int64_t t = tb + r;
+      float v[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) v[q] = 0.f;
+      if (t < T) {
+        const Tin* p = x + t * h + k0 + c;
+        if constexpr (sizeof(Tin) == 2) {
+          if (k0 + c + 8 <= h) {
+            const Vec<__nv_bfloat16> u = ldg16(reinterpret_cast<const __nv_bfloat16*>(p));
+#pragma unroll
+            for (int q = 0; q < 8; ++q) v[q] = __bfloat162float(u.v[q]);
+          }
+        } else {
+#pragma unroll
+          for (int hq = 0; hq < 2; ++hq)
+            if (k0 + c + 4 * hq + 4 <= h) {
+              const float4 u = __ldg(reinterpret_cast<const float4*>(p + 4 * hq));
+              v[4 * hq] = u.x; v[4 * hq + 1] = u.y; v[4 * hq + 2] = u.z; v[4 * hq + 3] = u.w;
+            }
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < 8; ++q) xs[c + q][r] = v[q];
+    }
+    // W tile: 64 experts x 32 cols
+    {
+      const int r = threadIdx.x >> 2, c = (threadIdx.x & 3) * 8;
+      const int e = eb + r;
+#pragma unroll
+      for (int hq = 0; hq < 2; ++hq) {
+        float4 u = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (e < E && k0 + c + 4 * hq + 4 <= h)
+          u = __ldg(reinterpret_cast<const float4*>(w_r + (int64_t)e * h + k0 + c + 4 * hq));
+        ws[c + 4 * hq][r] = u.x; ws[c + 4 * hq + 1][r] = u.y;
+        ws[c + 4 * hq + 2][r] = u.z; ws[c + 4 * hq + 3][r] = u.w;
+      }
+    }
+    __syncthreads();
+#pragma unroll 8
+    for (int kk = 0; kk < BK; ++kk) {
+      const float4 av = *reinterpret_cast<const float4*>(&xs[kk][ty * 4]);
+      const float4 bv = *reinterpret_cast<const float4*>(&ws[kk][tx * 4]);
+      const float a4[4] = {av.x, av.y, av.z, av.w}, b4[4] = {bv.x, bv.y, bv.z, bv.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a4[i], b4[j], acc[i][j]);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int64_t t = tb + ty * 4 + i;
+    if (t >= T) continue;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int e = eb + tx * 4 + j;
+      if (e < E) logits[t * E + e] = acc[i][j] + (gate_bias ? __ldg(gate_bias + e) : 0.f);
+    }
+  }
+}
+
+// ---- host launchers -------------------------------------------------------
+static RouterArgs make_args(const moe_config_t& c, const float* sel_bias, int32_t* idx,
+                            float* prob, uint8_t* map) {
+  RouterArgs a;
+  a.T = c.T; a.E = c.E; a.K = c.K; a.h = c.h; a.score = c.score;
+  a.renorm = (c.flags & MOE_FLAG_RENORM) != 0;
+  a.force_balance = (c.flags & MOE_FLAG_FORCE_BALANCE) != 0;
+  a.sel_bias = sel_bias; a.topk_idx = idx; a.topk_prob = prob; a.routing_map = map;
+  return a;
+}
+
+cudaError_t launch_router_select(const moe_config_t& c, const float* logits, const float* sel_bias,
+                                 int32_t* idx, float* prob, uint8_t* map, cudaStream_t s) {
+  if (c.T == 0) return cudaSuccess;
+  RouterArgs a = make_args(c, sel_bias, idx, prob, map);
+  const int blocks = (int)ceil_div(c.T, 8);
+  const int J = (int)ceil_div(c.E, 32);
+  switch (J) {
+    case 1: router_select_kernel<1><<<blocks, 256, 0, s>>>(logits, a); break;
+    case 2: router_select_kernel<2><<<blocks, 256, 0, s>>>(logits, a); break;
+    case 3: case 4: router_select_kernel<4><<<blocks, 256, 0, s>>>(logits, a); break;
+    default: router_select_kernel<8><<<blocks, 256, 0, s>>>(logits, a); break;
+  }
+  return cudaGetLastError();
+}
+
+template <typename Tin, int EP>
+static cudaError_t launch_fused(const moe_config_t& c, const Tin* x, const float* w_r,
+                                const float* gate_bias, float* logits, RouterArgs a,
+                                cudaStream_t s) {
+  constexpr int TPW = 32 / EP;
+  const int hc = (8192 / EP) / 128 * 128;  // 32 KB of W_r per chunk
+  const size_t smem = (size_t)EP * hc * sizeof(float);
+  const int blocks = (int)ceil_div(c.T, 8 * TPW);
+  router_fused_small_kernel<Tin, EP><<<blocks, 256, smem, s>>>(x, w_r, gate_bias, logits, a, hc);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_router(const moe_config_t& c, const void* x, const float* w_r,
+                          const float* gate_bias, const float* sel_bias, float* logits,
+                          int32_t* idx, float* prob, uint8_t* map, cudaStream_t s) {
+  if (c.T == 0) return cudaSuccess;
+  RouterArgs a = make_args(c, sel_bias, idx, prob, map);
+  const bool bf = c.dtype == MOE_BF16;
+  if (c.E <= 32) {
+    const int EP = c.E <= 8 ? 8 : (c.E <= 16 ? 16 : 32);
+    if (bf) {
+      const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
+      if (EP == 8) return launch_fused<__nv_bfloat16, 8>(c, xb, w_r, gate_bias, logits, a, s);
+      if (EP == 16) return launch_fused<__nv_bfloat16, 16>(c, xb, w_r, gate_bias, logits, a, s);
+      return launch_fused<__nv_bfloat16, 32>(c, xb, w_r, gate_bias, logits, a, s);
+    }
+    const float* xf = static_cast<const float*>(x);
+    if (EP == 8) return launch_fused<float, 8>(c, xf, w_r, gate_bias, logits, a, s);
+    if (EP == 16) return launch_fused<float, 16>(c, xf, w_r, gate_bias, logits, a, s);
+    return launch_fused<float, 32>(c, xf, w_r, gate_bias, logits, a, s);
+  }
+  dim3 grid((unsigned)ceil_div(c.E, 64), (unsigned)ceil_div(c.T, 64));
+  if (bf)
+    router_gemm_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(
+        static_cast<const __nv_bfloat16*>(x), w_r, gate_bias, logits, c.T, c.E, c.h);
+  else
+    router_gemm_kernel<float><<<grid, 256, 0, s>>>(static_cast<const float*>(x), w_r, gate_bias,
+                                                   logits, c.T, c.E, c.h);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  return launch_router_select(c, logits, sel_bias, idx, prob, map, s);
+}
+
+}  // namespace moe

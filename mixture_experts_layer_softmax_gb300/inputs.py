@@ -18,6 +18,9 @@ own, on the host here or on the device by ``moe_synth_normal``):
 
 from __future__ import annotations
 
+import concurrent.futures as _cf
+import os
+
 import numpy as np
 
 GAMMA = 0x9E3779B97F4A7C15
@@ -30,7 +33,15 @@ TWO_PI = 6.283185307179586  # the float64 nearest to 2*pi
 TAG = dict(x=1, w_r=2, gate_bias=3, sel_bias=4, w1=5, b1=6, w2=7, b2=8,
            w1_shared=9, w2_shared=10, dy=11, zipf_rank=12)
 
-_CHUNK = 1 << 22
+_CHUNK = 1 << 16          # elements per work item (fits in L2)
+_POOL = None
+
+
+def _pool():
+    global _POOL
+    if _POOL is None:
+        _POOL = _cf.ThreadPoolExecutor(max_workers=max(1, min(32, os.cpu_count() or 1)))
+    return _POOL
 
 
 def mix64_int(z: int) -> int:
@@ -86,12 +97,19 @@ def normal(shape, std: float, seed: int, tag: int, dtype: str = "f32", start: in
     counter, so a slice of a larger tensor can be generated on its own."""
     n = int(np.prod(shape))
     out = np.empty(n, np.float32)
-    for s in range(0, n, _CHUNK):
+
+    def work(s):
         m = min(_CHUNK, n - s)
         v = (np.float64(std) * normal_f64(seed, tag, start + s, m)).astype(np.float32)
         if dtype == "bf16":
             v = bf16_bits_to_f32(f32_to_bf16_bits(v))
         out[s:s + m] = v
+
+    if n <= 4 * _CHUNK:
+        for s in range(0, n, _CHUNK):
+            work(s)
+    else:  # numpy releases the GIL in these ufuncs: chunks run in parallel
+        list(_pool().map(work, range(0, n, _CHUNK)))
     return out.reshape(shape)
 
 

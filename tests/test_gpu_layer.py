@@ -1,0 +1,143 @@
+"""GPU parity of the expert GEMMs and of the whole forward layer against the
+oracle, at sizes the oracle finishes in seconds that still span several
+tiles and ragged tails, plus determinism."""
+
+import numpy as np
+import pytest
+import torch
+
+from gpu_util import Layer, lib, needs_gpu, to_dev, to_np, tol_ok
+from mixture_experts_layer_softmax_gb300 import inputs, workloads as W
+from oracle import moe_oracle as O
+
+pytestmark = [pytest.mark.gpu, needs_gpu]
+
+
+def _grouped_case(P_tokens, h, E, K, F, act, bias, dtype, skew=False, seed=0):
+    rng = np.random.default_rng(seed)
+    logits = rng.normal(size=(P_tokens, E)).astype(np.float32)
+    if skew:
+        logits[:, 0] += 3.0
+        logits[:, E - 1] -= 100.0  # the last expert gets nothing
+    idx, _ = O.route(logits, K, O.SCORE_SOFTMAX)
+    counts, offsets, _, src_token, _ = O.dispatch_maps(idx, E)
+    P = P_tokens * K
+    R1 = 2 * F if act == O.ACT_SWIGLU else F
+    x_perm = inputs.normal((P, h), 1.0, seed, 1, dtype)
+    w1 = inputs.normal((E, R1, h), h ** -0.5, seed, 2, dtype)
+    w2 = inputs.normal((E, h, F), F ** -0.5, seed, 3, dtype)
+    b1 = inputs.normal((E, F), h ** -0.5, seed, 4, dtype) if bias else None
+    b2 = inputs.normal((E, h), F ** -0.5, seed, 5, dtype) if bias else None
+    prob = rng.uniform(0.05, 1.0, size=P).astype(np.float32)
+    return dict(x_perm=x_perm, w1=w1, w2=w2, b1=b1, b2=b2, prob=prob, offsets=offsets,
+                counts=counts, P=P, R1=R1)
+
+
+GROUPED = [
+    # tokens, h, E, K, F, act, bias, dtype, skew, simt
+    (600, 512, 8, 2, 768, O.ACT_SWIGLU, False, "bf16", False, False),
+    (300, 200, 5, 2, 136, O.ACT_SWIGLU, False, "bf16", True, False),
+    (700, 256, 1, 1, 384, O.ACT_SWIGLU, False, "bf16", False, False),
+    (150, 128, 16, 4, 264, O.ACT_GELU, False, "bf16", True, False),
+    (150, 128, 16, 4, 264, O.ACT_GELU, True, "bf16", False, False),
+    (600, 512, 8, 2, 768, O.ACT_SWIGLU, False, "bf16", False, True),
+    (256, 128, 8, 2, 512, O.ACT_GELU, True, "f32", False, False),
+    (100, 96, 3, 2, 52, O.ACT_SWIGLU, False, "f32", True, False),
+]
+
+
+@pytest.mark.parametrize("T,h,E,K,F,act,bias,dtype,skew,simt", GROUPED)
+def test_grouped_mlp_matches_oracle(T, h, E, K, F, act, bias, dtype, skew, simt):
+    M = lib()
+    c = _grouped_case(T, h, E, K, F, act, bias, dtype, skew, seed=T + F)
+    flags = M.MOE_FLAG_RENORM | (M.MOE_FLAG_GEMM_SIMT if simt else 0)
+    cfg = M.make_config(T, h, E, K, F, M.MOE_BF16 if dtype == "bf16" else M.MOE_F32,
+                        M.MOE_SCORE_SOFTMAX, act, int(bias), 0, flags)
+    ws = torch.empty(M.moe_workspace_size(cfg), dtype=torch.uint8, device="cuda")
+    tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
+    P = c["P"]
+    y_perm = torch.full((P, h), float("nan"), dtype=tdt, device="cuda")
+    act_save = torch.full((P, c["R1"]), float("nan"), dtype=tdt, device="cuda")
+    dv = lambda a: None if a is None else to_dev(a, dtype)
+    M.moe_grouped_mlp_fwd(cfg, dv(c["x_perm"]), torch.from_numpy(c["offsets"].astype(np.int32)).cuda(),
+                          to_dev(c["prob"], "f32"), dv(c["w1"]), dv(c["b1"]), dv(c["w2"]), dv(c["b2"]),
+                          act_save, y_perm, ws)
+    torch.cuda.synchronize()
+    assert M.moe_get_error() == M.MOE_OK
+    ref = np.zeros((P, h))
+    ref_h = np.zeros((P, c["R1"]))
+    off = c["offsets"]
+    for e in range(E):
+        r = slice(off[e], off[e + 1])
+        if off[e + 1] == off[e]:
+            continue
+        b1e = None if c["b1"] is None else c["b1"][e]
+        b2e = None if c["b2"] is None else c["b2"][e]
+        ref[r] = c["prob"][r, None] * O.expert_ffn(c["x_perm"][r], c["w1"][e], c["w2"][e], act, b1e, b2e)
+        ref_h[r] = O.expert_hidden(c["x_perm"][r], c["w1"][e], b1e, act)[0]
+    ok, err, bound = tol_ok(to_np(y_perm), ref, dtype)
+    assert ok, (err, bound)
+    ok, err, bound = tol_ok(to_np(act_save), ref_h, dtype)
+    assert ok, ("act_save", err, bound)
+
+
+def small_workloads():
+    return [
+        W.TINY,
+        W.MIXTRAL.replace(name="mixtral_small", T=600, h=512, F=768),
+        W.QWEN3.replace(name="qwen3_small", T=1000, h=256, F=192),
+        W.DSV3.replace(name="dsv3_small", T=300, h=256, F=128),
+        W.Workload("sweep_small_random", T=512, h=256, E=64, K=8, F=128, seed=5),
+        W.Workload("sweep_small_balanced", T=512, h=256, E=64, K=8, F=128, force_balance=True, seed=5),
+        W.Workload("edge_one_token", T=1, h=64, E=4, K=2, F=64, seed=9),
+        W.Workload("edge_three_tokens_K_eq_E", T=3, h=64, E=3, K=3, F=40, seed=9),
+        W.Workload("edge_single_expert", T=130, h=128, E=1, K=1, F=136, seed=9),
+        W.Workload("edge_gelu_bf16_bias", T=200, h=128, E=8, K=2, F=256, act=W.GELU, has_bias=True,
+                   seed=9),
+    ]
+
+
+@pytest.mark.parametrize("w", small_workloads(), ids=lambda w: w.name)
+def test_layer_forward_matches_oracle(w):
+    M = lib()
+    L = Layer(w)
+    y, idx, prob, _ = L.run_fwd(M)
+    ref = L.oracle_fwd()
+    ok_tok = L.margins(ref["logits"]) >= 1e-5
+    assert ok_tok.mean() > 0.98
+    np.testing.assert_array_equal(to_np(idx)[ok_tok], ref["idx"][ok_tok])
+    np.testing.assert_allclose(to_np(prob)[ok_tok], ref["probs"][ok_tok], rtol=1e-5, atol=1e-6)
+    good, err, bound = tol_ok(to_np(y)[ok_tok], ref["y"][ok_tok], w.dtype)
+    assert good, (err, bound)
+
+
+@pytest.mark.parametrize("w", small_workloads()[1:4], ids=lambda w: w.name)
+def test_layer_forward_is_deterministic(w):
+    M = lib()
+    L = Layer(w)
+    y1, i1, p1, ws = L.run_fwd(M)
+    y2, i2, p2, _ = L.run_fwd(M, ws=ws)
+    assert torch.equal(y1.view(torch.int16) if y1.dtype == torch.bfloat16 else y1,
+                       y2.view(torch.int16) if y2.dtype == torch.bfloat16 else y2)
+    assert torch.equal(i1, i2) and torch.equal(p1, p2)
+
+
+def test_layer_simt_and_tensor_core_paths_agree():
+    M = lib()
+    w = W.MIXTRAL.replace(name="mixtral_small", T=300, h=256, F=384)
+    L = Layer(w)
+    y_tc, *_ = L.run_fwd(M)
+    y_simt, *_ = L.run_fwd(M, flags_extra=M.MOE_FLAG_GEMM_SIMT)
+    ok, err, bound = tol_ok(to_np(y_tc), to_np(y_simt), "bf16")
+    assert ok, (err, bound)
+
+
+def test_empty_batch_is_a_no_op():
+    M = lib()
+    cfg = M.make_config(0, 64, 4, 2, 64)
+    ws = torch.empty(max(M.moe_workspace_size(cfg), 256), dtype=torch.uint8, device="cuda")
+    e = torch.empty(0, device="cuda")
+    z = torch.zeros(8, 64, dtype=torch.bfloat16, device="cuda")
+    M.moe_layer_fwd(cfg, z, torch.zeros(4, 64, device="cuda"), None, None, z, None, z, None, None,
+                    None, z, None, None, ws)
+    assert M.moe_get_error() == M.MOE_OK

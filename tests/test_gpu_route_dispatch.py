@@ -1,0 +1,174 @@
+"""GPU parity of Route, Dispatch and Combine against the oracle: routing,
+counts, offsets and the permutation are bit-exact given the same fp32 logits;
+permuted rows are exact copies; the combine matches to fp32 rounding."""
+
+import numpy as np
+import pytest
+import torch
+
+from gpu_util import lib, needs_gpu, to_dev, to_np, tol_ok
+from mixture_experts_layer_softmax_gb300 import inputs
+from oracle import moe_oracle as O
+
+pytestmark = [pytest.mark.gpu, needs_gpu]
+
+ROUTER_CASES = [
+    # T, E, K, score, renorm, bias, force
+    (1, 1, 1, 0, True, False, False),
+    (3, 2, 2, 0, True, False, False),
+    (127, 8, 2, 0, True, False, False),
+    (1000, 8, 2, 0, False, False, False),
+    (513, 3, 3, 0, True, False, False),
+    (700, 64, 8, 0, True, False, False),
+    (700, 128, 8, 0, True, True, False),
+    (300, 256, 8, 1, True, True, False),
+    (300, 256, 8, 1, False, True, False),
+    (256, 256, 16, 1, True, False, False),
+    (512, 64, 8, 0, True, False, True),
+    (96, 256, 8, 1, True, True, True),
+    (200, 33, 5, 1, True, False, False),
+]
+
+
+@pytest.mark.parametrize("T,E,K,score,renorm,bias,force", ROUTER_CASES)
+def test_router_from_logits_bit_exact(T, E, K, score, renorm, bias, force):
+    M = lib()
+    logits = inputs.normal((T, E), 1.0, 100 + E, 1)
+    if E > 4:  # plant exact ties: the lower index must win
+        logits[::7, 1] = logits[::7, 0]
+        logits[::11, E - 1] = logits[::11, 2]
+    b = inputs.normal((E,), 0.1, 101, 2) if bias else None
+    flags = (M.MOE_FLAG_RENORM if renorm else 0) | (M.MOE_FLAG_FORCE_BALANCE if force else 0)
+    cfg = M.make_config(T, 8, E, K, 8, M.MOE_F32, score, M.MOE_ACT_SWIGLU, 0, 0, flags)
+    idx = torch.empty(T, K, dtype=torch.int32, device="cuda")
+    prob = torch.empty(T, K, dtype=torch.float32, device="cuda")
+    rmap = torch.empty(T, E, dtype=torch.uint8, device="cuda")
+    M.moe_router_topk_from_logits(cfg, to_dev(logits, "f32"), None if b is None else to_dev(b, "f32"),
+                                  idx, prob, rmap)
+    torch.cuda.synchronize()
+    oi, op = O.route(logits, K, score, renorm, b, force)
+    np.testing.assert_array_equal(to_np(idx), oi)
+    np.testing.assert_allclose(to_np(prob), op, rtol=2e-6, atol=1e-7)
+    np.testing.assert_array_equal(to_np(rmap).astype(bool), O.routing_map(oi, E))
+
+
+@pytest.mark.parametrize("T,h,E,K,score,dtype,gate_bias", [
+    (300, 128, 8, 2, 0, "bf16", False), (257, 4096, 8, 2, 0, "bf16", False),
+    (256, 128, 8, 2, 0, "f32", False), (100, 256, 16, 4, 0, "bf16", True),
+    (100, 64, 32, 8, 1, "f32", False), (300, 512, 128, 8, 0, "bf16", True),
+    (200, 7168, 256, 8, 1, "bf16", False), (64, 200, 5, 2, 0, "bf16", False),
+])
+def test_router_gating_matches_oracle(T, h, E, K, score, dtype, gate_bias):
+    M = lib()
+    x = inputs.normal((T, h), 1.0, 7, 1, dtype)
+    w_r = inputs.normal((E, h), 0.02 if h > 256 else 0.1, 7, 2)
+    gb = inputs.normal((E,), 0.5, 7, 3) if gate_bias else None
+    cfg = M.make_config(T, h, E, K, 16, M.MOE_BF16 if dtype == "bf16" else M.MOE_F32, score,
+                        M.MOE_ACT_SWIGLU, 0, 0, M.MOE_FLAG_RENORM)
+    logits = torch.empty(T, E, dtype=torch.float32, device="cuda")
+    idx = torch.empty(T, K, dtype=torch.int32, device="cuda")
+    prob = torch.empty(T, K, dtype=torch.float32, device="cuda")
+    M.moe_router_topk(cfg, to_dev(x, dtype), to_dev(w_r, "f32"), None if gb is None else to_dev(gb, "f32"),
+                      None, logits, idx, prob)
+    torch.cuda.synchronize()
+    ol = O.gating_logits(x, w_r, gb)
+    gl = to_np(logits)
+    scale = np.abs(x).astype(np.float64) @ np.abs(w_r).astype(np.float64).T
+    assert np.all(np.abs(gl - ol) <= 1e-6 * scale + 1e-30)
+    # selection: identical except where the top-K margin is below 1e-5
+    oi, _ = O.route(ol, K, score, True)
+    margin = O.selection_margin(ol, K, score)
+    ok = margin >= 1e-5
+    np.testing.assert_array_equal(to_np(idx)[ok], oi[ok])
+
+
+@pytest.mark.parametrize("T,E,K,skew", [
+    (1, 1, 1, False), (3, 2, 2, False), (127, 8, 2, False), (1000, 8, 2, True),
+    (1000, 128, 8, True), (2049, 256, 8, False), (4096, 64, 8, False), (33, 4, 4, False),
+])
+def test_permute_maps_bit_exact(T, E, K, skew):
+    M = lib()
+    h = 64
+    rng = np.random.default_rng(T + E)
+    logits = rng.normal(size=(T, E)).astype(np.float32)
+    if skew:
+        logits[:, 0] += 100.0  # everyone picks expert 0; several experts get nothing
+    oi, op = O.route(logits, K, O.SCORE_SOFTMAX)
+    counts, offsets, dst_row, src_token, src_slot = O.dispatch_maps(oi, E)
+    x = inputs.normal((T, h), 1.0, 3, 1, "bf16")
+    cfg = M.make_config(T, h, E, K, 8, M.MOE_BF16, 0, M.MOE_ACT_SWIGLU, 0, 0, M.MOE_FLAG_RENORM)
+    ws = torch.empty(M.moe_workspace_size(cfg), dtype=torch.uint8, device="cuda")
+    P = T * K
+    d = dict(x_perm=torch.empty(P, h, dtype=torch.bfloat16, device="cuda"),
+             counts=torch.empty(E, dtype=torch.int32, device="cuda"),
+             offsets=torch.empty(E + 1, dtype=torch.int32, device="cuda"),
+             dst_row=torch.empty(T, K, dtype=torch.int32, device="cuda"),
+             src_token=torch.empty(P, dtype=torch.int32, device="cuda"),
+             perm_prob=torch.empty(P, dtype=torch.float32, device="cuda"))
+    M.moe_permute(cfg, to_dev(x, "bf16"), torch.from_numpy(oi).cuda(), to_dev(op, "f32"),
+                  d["x_perm"], d["counts"], d["offsets"], d["dst_row"], d["src_token"],
+                  d["perm_prob"], ws)
+    torch.cuda.synchronize()
+    assert M.moe_get_error() == M.MOE_OK
+    np.testing.assert_array_equal(to_np(d["counts"]), counts)
+    np.testing.assert_array_equal(to_np(d["offsets"]), offsets)
+    np.testing.assert_array_equal(to_np(d["dst_row"]), dst_row)
+    np.testing.assert_array_equal(to_np(d["src_token"]), src_token)
+    np.testing.assert_array_equal(to_np(d["perm_prob"]), op.astype(np.float32)[src_token, src_slot])
+    np.testing.assert_array_equal(to_np(d["x_perm"]), O.permute_rows(x, src_token))
+
+
+def test_permute_rejects_bad_expert_ids_without_faulting():
+    M = lib()
+    T, E, K, h = 64, 8, 2, 32
+    idx = np.tile(np.array([[0, 1]], np.int32), (T, 1))
+    idx[5, 1] = 99  # out of range: reported, row skipped
+    cfg = M.make_config(T, h, E, K, 8, M.MOE_BF16, 0, M.MOE_ACT_SWIGLU, 0, 0, M.MOE_FLAG_RENORM)
+    ws = torch.empty(M.moe_workspace_size(cfg), dtype=torch.uint8, device="cuda")
+    P = T * K
+    x_perm = torch.zeros(P, h, dtype=torch.bfloat16, device="cuda")
+    out = [torch.zeros(n, dtype=torch.int32, device="cuda") for n in (E, E + 1, P, P)]
+    M.moe_permute(cfg, torch.zeros(T, h, dtype=torch.bfloat16, device="cuda"),
+                  torch.from_numpy(idx).cuda(), None, x_perm, out[0], out[1], out[2], out[3],
+                  None, ws)
+    assert M.moe_get_error() == M.MOE_ERR_DEVICE_BOUNDS
+    assert M.moe_get_error() == M.MOE_OK  # cleared
+    assert int(out[1][-1]) == P - 1
+
+
+@pytest.mark.parametrize("T,E,K,h,dtype,weighted,shared", [
+    (1, 1, 1, 8, "bf16", False, False), (300, 8, 2, 4096, "bf16", False, True),
+    (257, 16, 4, 136, "bf16", True, False), (100, 8, 2, 128, "f32", True, True),
+    (2000, 64, 8, 512, "bf16", False, False),
+])
+def test_combine_matches_oracle(T, E, K, h, dtype, weighted, shared):
+    M = lib()
+    rng = np.random.default_rng(T)
+    oi, op = O.route(rng.normal(size=(T, E)).astype(np.float32), K, O.SCORE_SOFTMAX)
+    _, _, dst_row, _, _ = O.dispatch_maps(oi, E)
+    y_perm = inputs.normal((T * K, h), 1.0, 9, 1, dtype)
+    sy = inputs.normal((T, h), 1.0, 9, 2, dtype) if shared else None
+    cfg = M.make_config(T, h, E, K, 8, M.MOE_BF16 if dtype == "bf16" else M.MOE_F32, 0,
+                        M.MOE_ACT_SWIGLU, 0, 0, M.MOE_FLAG_RENORM)
+    y = torch.empty(T, h, dtype=torch.bfloat16 if dtype == "bf16" else torch.float32, device="cuda")
+    M.moe_unpermute_combine(cfg, to_dev(y_perm, dtype), torch.from_numpy(dst_row.astype(np.int32)).cuda(),
+                            to_dev(op, "f32") if weighted else None,
+                            None if sy is None else to_dev(sy, dtype), y)
+    torch.cuda.synchronize()
+    ref = O.unpermute_combine(y_perm, dst_row, op.astype(np.float32) if weighted else None)
+    if shared:
+        ref = ref + sy
+    g = to_np(y)
+    if dtype == "bf16":  # one rounding of the fp32 sum
+        assert np.all(np.abs(g - ref) <= np.abs(ref) * 2.0 ** -8 + 1e-6 * K)
+    else:
+        np.testing.assert_allclose(g, ref, rtol=1e-6, atol=1e-5)
+
+
+def test_bounded_wait_times_out_and_context_survives():
+    M = lib()
+    M.moe_test_bounded_wait(2000)
+    assert M.moe_get_error() == M.MOE_ERR_TIMEOUT
+    assert M.moe_get_error() == M.MOE_OK
+    t = torch.ones(8, device="cuda")
+    assert float(t.sum()) == 8.0
