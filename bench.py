@@ -49,6 +49,8 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--sample-tokens", type=int, default=0, help="oracle sample size (0: auto)")
+    p.add_argument("--tokens", type=int, default=0,
+                   help="override T (smaller cases for profiler captures; not a bench line)")
     return p.parse_args()
 
 
@@ -493,6 +495,8 @@ def main():
     args = parse()
     from mixture_experts_layer_softmax_gb300 import workloads
     w = workloads.ALL[args.workload] if args.workload else workloads.MIXTRAL
+    if args.tokens:
+        w = w.replace(name=f"{w.name}_T{args.tokens}", T=args.tokens)
     if args.impl == "reference":
         run_reference(args, w)
     else:

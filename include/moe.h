@@ -131,6 +131,27 @@ moe_status_t moe_permute(const moe_config_t* cfg, const void* x, const int32_t* 
                          int32_t* dst_row, int32_t* src_token, float* perm_prob, void* ws,
                          size_t ws_bytes, moe_stream_t stream);
 
+/* moe_permute without a workspace, for callers that cannot allocate device
+ * memory: plugins hosted by a framework that owns all device memory and
+ * offers them no allocator, and serving loops that must not allocate after
+ * start-up.  The pages have no counterpart of this entry point; it is a
+ * deployment convenience.  Same arguments (minus ws), rules and results as
+ * moe_permute.
+ *  - Scratch: a fixed 2 MiB array inside the library (two tables of
+ *    ceil(T/32) * E int32), held by every GPU that loads the library until the
+ *    process exits.  Configurations with ceil(T/32) * E > 262144 return
+ *    MOE_ERR_UNSUPPORTED.  Nothing in it needs clearing between calls.
+ *  - The first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress, with that device current); make that first call
+ *    before capturing any stream.
+ *  - Every call on a device shares the one array: calls whose kernels can
+ *    overlap on the GPU (different streams without ordering) race.
+ *  - Allocates nothing: no cudaMalloc, cudaFree or allocating library call. */
+moe_status_t moe_permute_noalloc(const moe_config_t* cfg, const void* x, const int32_t* topk_idx,
+                                 const float* topk_prob, void* x_perm, int32_t* counts,
+                                 int32_t* offsets, int32_t* dst_row, int32_t* src_token,
+                                 float* perm_prob, moe_stream_t stream);
+
 /* Expert computation (review §2.1 "Expert computation": every expert in one
  * grouped GEMM call; §4.1.1 memory-efficient permutation).  For every row r
  * of expert e (offsets[e] <= r < offsets[e+1]):

@@ -132,6 +132,15 @@ cudaError_t run_grouped_mlp(const moe_config_t& c, int rows, const void* x_perm,
 
 }  // namespace
 
+namespace moe {
+// Internal accessors for other translation units of the library.
+moe_status_t validate_config(const moe_config_t* c) { return check_config(c); }
+int* device_status_word() {
+  const DeviceInfo* d = device_info();
+  return d ? d->status : nullptr;
+}
+}  // namespace moe
+
 extern "C" {
 
 size_t moe_workspace_size(const moe_config_t* cfg) {

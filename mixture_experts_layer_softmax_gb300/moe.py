@@ -51,6 +51,7 @@ _SIG = {
     "moe_router_topk": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "moe_router_topk_from_logits": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P]),
     "moe_permute": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
+    "moe_permute_noalloc": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "moe_grouped_mlp_fwd": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                            ctypes.c_size_t, _P]),
     "moe_expert_fc1": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P, _P, _P]),
@@ -152,6 +153,15 @@ def moe_permute(cfg, x, topk_idx, topk_prob, x_perm, counts, offsets, dst_row, s
     _check("moe_permute", _lib.moe_permute(
         ctypes.byref(cfg), _ptr(x), _ptr(topk_idx), _ptr(topk_prob), _ptr(x_perm), _ptr(counts),
         _ptr(offsets), _ptr(dst_row), _ptr(src_token), _ptr(perm_prob), wp, wb, _stream(stream)))
+
+
+def moe_permute_noalloc(cfg, x, topk_idx, topk_prob, x_perm, counts, offsets, dst_row, src_token,
+                        perm_prob, stream=None):
+    """moe_permute for callers that cannot allocate device memory: no
+    workspace; the library's fixed scratch array is used (see moe.h)."""
+    _check("moe_permute_noalloc", _lib.moe_permute_noalloc(
+        ctypes.byref(cfg), _ptr(x), _ptr(topk_idx), _ptr(topk_prob), _ptr(x_perm), _ptr(counts),
+        _ptr(offsets), _ptr(dst_row), _ptr(src_token), _ptr(perm_prob), _stream(stream)))
 
 
 def moe_grouped_mlp_fwd(cfg, x_perm, offsets, perm_prob, w1, b1, w2, b2, act_save, y_perm, ws,
