@@ -203,6 +203,56 @@ moe_status_t moe_layer_fwd(const moe_config_t* cfg, const void* x, const float* 
                            int32_t* topk_idx_out, float* topk_prob_out, void* ws,
                            size_t ws_bytes, moe_stream_t stream);
 
+/* ---- Backward (the training configuration: bf16, SwiGLU experts, a
+ * renormalised softmax or sigmoid router; others return MOE_ERR_UNSUPPORTED).
+ * The pages give no backward formulas ("Scalable Training of Mixture-of-Experts
+ * Models with Megatron Core", review §4.1.2, only names the recomputed
+ * activations); these calls compute the reverse-mode derivatives of the
+ * forward above with the expert selection held fixed.  The selection bias
+ * receives no gradient.  Weight gradients are written (not accumulated). */
+
+/* Expert FFNs over permuted rows, from the forward's saved pre-activation
+ * (act_save [P,2F]) and FC2 input (a [P,F] = p * silu(gate) * up):
+ *   G = dy_perm W2_e;  dprob_perm[r] = <G_r, silu(g_r) * u_r> = <dy_perm_r, E_e(x_r)>;
+ *   dH = [p G u silu'(g), p G silu(g)];  dW2_e = dy_perm_e^T a_e;
+ *   dx_perm = dH W1_e;  dW1_e = dH_e^T x_perm_e.
+ *   dy_perm, x_perm [P,h]; offsets [E+1]; perm_prob [P]; w1 [E][2F][h]; w2 [E][h][F];
+ *   outputs dx_perm [P,h], dw1 [E][2F][h], dw2 [E][h][F] (bf16, fp32 accumulate;
+ *   experts without rows get zeros), dprob_perm [P] f32 or NULL.
+ *   ws: moe_workspace_size of cfg with MOE_FLAG_SAVE_FOR_BWD. */
+moe_status_t moe_grouped_mlp_bwd(const moe_config_t* cfg, const void* dy_perm, const void* x_perm,
+                                 const void* act_save, const void* a, const int32_t* offsets,
+                                 const float* perm_prob, const void* w1, const void* w2,
+                                 void* dx_perm, void* dw1, void* dw2, float* dprob_perm, void* ws,
+                                 size_t ws_bytes, moe_stream_t stream);
+
+/* Route backward from dprob_perm (permuted order, as moe_grouped_mlp_bwd
+ * gives it): for each token's selected experts
+ *   softmax: dl_k = p_k (dp_k - sum_j p_j dp_j)
+ *   sigmoid: dl_k = s_k (1 - s_k) (dp_k - sum_j p_j dp_j) / sum_sel s
+ * then dW_r[e] = sum over e's tokens of dl x_t (fp32), db_r[e] = sum dl, and
+ * optionally dx_router[t] = sum_k dl_k W_r[e_k] (fp32 [T,h]).
+ *   x [T,h]; logits [T,E]; topk_idx/topk_prob [T,K]; offsets, dst_row, src_token
+ *   from moe_permute; outputs dl_topk [T,K], dw_r [E,h], db_r [E] or NULL,
+ *   dx_router or NULL (then w_r may be NULL). */
+moe_status_t moe_router_bwd(const moe_config_t* cfg, const void* x, const float* logits,
+                            const int32_t* topk_idx, const float* topk_prob,
+                            const int32_t* offsets, const int32_t* dst_row,
+                            const int32_t* src_token, const float* dprob_perm, const float* w_r,
+                            float* dl_topk, float* dw_r, float* db_r, float* dx_router, void* ws,
+                            size_t ws_bytes, moe_stream_t stream);
+
+/* The whole backward layer pass after moe_layer_fwd with MOE_FLAG_SAVE_FOR_BWD
+ * on the same workspace and inputs: dy [T,h] -> dx [T,h] (routed experts +
+ * shared expert + router), dw_r [E,h] f32, db_r [E] f32 or NULL (gradient of
+ * the gate bias), dw1, dw2 and, with a shared expert, dw1_shared [2F][h],
+ * dw2_shared [h][F]. */
+moe_status_t moe_layer_bwd(const moe_config_t* cfg, const void* x, const float* w_r,
+                           const void* w1, const void* w2, const void* w1_shared,
+                           const void* w2_shared, const void* dy, void* dx, float* dw_r,
+                           float* db_r, void* dw1, void* dw2, void* dw1_shared, void* dw2_shared,
+                           void* ws, size_t ws_bytes, moe_stream_t stream);
+
 /* Bytes of host-visible state: none.  Reports (and clears) the per-device
  * status word written by device-side checks, after synchronising `stream`.
  * Returns MOE_OK, MOE_ERR_TIMEOUT, MOE_ERR_DEVICE_BOUNDS or MOE_ERR_CUDA. */

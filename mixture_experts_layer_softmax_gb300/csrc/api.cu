@@ -24,6 +24,18 @@ cudaError_t launch_expert_gemm_tc(const moe_config_t&, int, int, const void*, co
                                   const float*, const void*, const void*, void*, void*, int, int*,
                                   cudaStream_t);
 cudaError_t launch_bounded_wait_probe(int64_t, int*, cudaStream_t);
+cudaError_t launch_tc_dgrad(bool, int, const void*, int, const void*, int, int, const int32_t*,
+                            const float*, const void*, void*, float*, int, int*, cudaStream_t);
+cudaError_t launch_tc_wgrad(int, const void*, int, const void*, int, int, const int32_t*, void*,
+                            int, int*, cudaStream_t);
+cudaError_t launch_dprob_reduce(const float*, int, int, float*, cudaStream_t);
+cudaError_t launch_router_bwd(const moe_config_t&, const float*, const int32_t*, const float*,
+                              const int32_t*, const float*, float*, float*, int*, cudaStream_t);
+cudaError_t launch_router_wgrad(const moe_config_t&, const void*, const int32_t*, const int32_t*,
+                                const float*, float*, float*, cudaStream_t);
+cudaError_t launch_bwd_combine(const moe_config_t&, const void*, const int32_t*, const void*,
+                               const float*, const int32_t*, const float*, void*, float*, int,
+                               int*, cudaStream_t);
 }  // namespace moe
 
 using namespace moe;
@@ -128,6 +140,39 @@ cudaError_t run_grouped_mlp(const moe_config_t& c, int rows, const void* x_perm,
   cudaError_t e = run_expert_gemm(c, 1, rows, x_perm, offsets, prob, w1, b1, act_save, a, d, s);
   if (e != cudaSuccess) return e;
   return run_expert_gemm(c, 2, rows, a, offsets, prob, w2, b2, nullptr, y_perm, d, s);
+}
+
+// The backward covers the training configuration: bf16 SwiGLU experts with a
+// renormalised router (softmax or sigmoid).
+moe_status_t check_bwd_support(const moe_config_t& c) {
+  if (c.dtype != MOE_BF16 || c.act != MOE_ACT_SWIGLU || !(c.flags & MOE_FLAG_RENORM))
+    return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+// Expert-FFN backward over permuted rows: dH and dprob partials (FC2 dgrad with
+// the dSwiGLU epilogue), dW2, dx_perm (FC1 dgrad), dW1.
+cudaError_t run_mlp_bwd(const moe_config_t& c, int rows, int E, const void* dy_rows,
+                        const void* x_rows, const void* H, const void* a, const int32_t* offsets,
+                        const float* prob, const void* w1, const void* w2, void* dH,
+                        float* dprob_part, void* dx_rows, void* dw1, void* dw2,
+                        const DeviceInfo* d, cudaStream_t s) {
+  const int F = c.F, h = c.h;
+  if (rows == 0) {  // no rows: every weight gradient is zero
+    cudaError_t e = cudaMemsetAsync(dw1, 0, (size_t)E * 2 * F * h * 2, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(dw2, 0, (size_t)E * h * F * 2, s);
+    return e;
+  }
+  cudaError_t e = launch_tc_dgrad(true, rows, dy_rows, h, w2, E, F, offsets, prob, H, dH,
+                                  dprob_part, d->sms, d->status, s);
+  if (e == cudaSuccess)
+    e = launch_tc_wgrad(rows, dy_rows, h, a, F, E, offsets, dw2, d->sms, d->status, s);
+  if (e == cudaSuccess)
+    e = launch_tc_dgrad(false, rows, dH, 2 * F, w1, E, h, offsets, nullptr, nullptr, dx_rows,
+                        nullptr, d->sms, d->status, s);
+  if (e == cudaSuccess)
+    e = launch_tc_wgrad(rows, dH, 2 * F, x_rows, h, E, offsets, dw1, d->sms, d->status, s);
+  return e;
 }
 
 }  // namespace
@@ -337,6 +382,138 @@ moe_status_t moe_layer_fwd(const moe_config_t* cfg, const void* x, const float* 
     e = cudaMemcpyAsync(topk_idx_out, idx, sizeof(int32_t) * c.T * c.K, cudaMemcpyDeviceToDevice, s);
   if (e == cudaSuccess && topk_prob_out)
     e = cudaMemcpyAsync(topk_prob_out, prob, sizeof(float) * c.T * c.K, cudaMemcpyDeviceToDevice, s);
+  return cuda_status(e);
+}
+
+moe_status_t moe_grouped_mlp_bwd(const moe_config_t* cfg, const void* dy_perm, const void* x_perm,
+                                 const void* act_save, const void* a, const int32_t* offsets,
+                                 const float* perm_prob, const void* w1, const void* w2,
+                                 void* dx_perm, void* dw1, void* dw2, float* dprob_perm, void* ws,
+                                 size_t ws_bytes, moe_stream_t stream) {
+  moe_status_t st = check_config(cfg);
+  if (st != MOE_OK) return st;
+  if ((st = check_bwd_support(*cfg)) != MOE_OK) return st;
+  if (!dy_perm || !x_perm || !act_save || !a || !offsets || !w1 || !w2 || !dx_perm || !dw1 || !dw2)
+    return MOE_ERR_INVALID_ARG;
+  if (!al16(dy_perm) || !al16(x_perm) || !al16(act_save) || !al16(a) || !al16(w1) || !al16(w2) ||
+      !al16(dx_perm) || !al16(dw1) || !al16(dw2))
+    return MOE_ERR_INVALID_ARG;
+  moe_config_t cs = *cfg;
+  cs.flags |= MOE_FLAG_SAVE_FOR_BWD;
+  if ((st = check_ws(&cs, ws, ws_bytes)) != MOE_OK) return st;
+  if (cfg->flags & MOE_FLAG_VALIDATE_ONLY) return MOE_OK;
+  const DeviceInfo* d = device_info();
+  if (!d) return MOE_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const Workspace w = workspace_layout(cs);
+  const int P = cfg->T * cfg->K;
+  float* part = at<float>(ws, w.dprob_part);
+  cudaError_t e = run_mlp_bwd(*cfg, P, cfg->E, dy_perm, x_perm, act_save, a, offsets, perm_prob,
+                              w1, w2, at<void>(ws, w.dh), part, dx_perm, dw1, dw2, d, s);
+  if (e == cudaSuccess && dprob_perm)
+    e = launch_dprob_reduce(part, P, (cfg->F + 255) / 256, dprob_perm, s);
+  return cuda_status(e);
+}
+
+moe_status_t moe_router_bwd(const moe_config_t* cfg, const void* x, const float* logits,
+                            const int32_t* topk_idx, const float* topk_prob,
+                            const int32_t* offsets, const int32_t* dst_row,
+                            const int32_t* src_token, const float* dprob_perm, const float* w_r,
+                            float* dl_topk, float* dw_r, float* db_r, float* dx_router, void* ws,
+                            size_t ws_bytes, moe_stream_t stream) {
+  moe_status_t st = check_config(cfg);
+  if (st != MOE_OK) return st;
+  if ((st = check_bwd_support(*cfg)) != MOE_OK) return st;
+  if (cfg->T > 0 && (!x || !logits || !topk_idx || !topk_prob || !offsets || !dst_row ||
+                     !src_token || !dprob_perm || !dl_topk || !dw_r))
+    return MOE_ERR_INVALID_ARG;
+  if (dx_router && !w_r) return MOE_ERR_INVALID_ARG;
+  if (!al16(x) || !al16(dw_r) || !al16(w_r) || !al16(dx_router)) return MOE_ERR_INVALID_ARG;
+  moe_config_t cs = *cfg;
+  cs.flags |= MOE_FLAG_SAVE_FOR_BWD;
+  if ((st = check_ws(&cs, ws, ws_bytes)) != MOE_OK) return st;
+  if (cfg->flags & MOE_FLAG_VALIDATE_ONLY) return MOE_OK;
+  const DeviceInfo* d = device_info();
+  if (!d) return MOE_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const Workspace w = workspace_layout(cs);
+  float* dl_perm = at<float>(ws, w.dl_perm);
+  cudaError_t e = launch_router_bwd(*cfg, logits, topk_idx, topk_prob, dst_row, dprob_perm,
+                                    dl_topk, dl_perm, d->status, s);
+  if (e == cudaSuccess)
+    e = launch_router_wgrad(*cfg, x, src_token, offsets, dl_perm, dw_r, db_r, s);
+  if (e == cudaSuccess && dx_router)
+    e = launch_bwd_combine(*cfg, nullptr, nullptr, nullptr, dl_topk, topk_idx, w_r, nullptr,
+                           dx_router, d->sms, d->status, s);
+  return cuda_status(e);
+}
+
+moe_status_t moe_layer_bwd(const moe_config_t* cfg, const void* x, const float* w_r,
+                           const void* w1, const void* w2, const void* w1_shared,
+                           const void* w2_shared, const void* dy, void* dx, float* dw_r,
+                           float* db_r, void* dw1, void* dw2, void* dw1_shared, void* dw2_shared,
+                           void* ws, size_t ws_bytes, moe_stream_t stream) {
+  moe_status_t st = check_config(cfg);
+  if (st != MOE_OK) return st;
+  const moe_config_t& c = *cfg;
+  if ((st = check_bwd_support(c)) != MOE_OK) return st;
+  if (!(c.flags & MOE_FLAG_SAVE_FOR_BWD)) return MOE_ERR_INVALID_ARG;
+  if (!x || !w_r || !w1 || !w2 || !dy || !dx || !dw_r || !dw1 || !dw2) return MOE_ERR_INVALID_ARG;
+  if (c.n_shared && (!w1_shared || !w2_shared || !dw1_shared || !dw2_shared))
+    return MOE_ERR_INVALID_ARG;
+  if (!al16(x) || !al16(w_r) || !al16(w1) || !al16(w2) || !al16(dy) || !al16(dx) ||
+      !al16(dw_r) || !al16(dw1) || !al16(dw2) || !al16(w1_shared) || !al16(w2_shared) ||
+      !al16(dw1_shared) || !al16(dw2_shared))
+    return MOE_ERR_INVALID_ARG;
+  if ((st = check_ws(cfg, ws, ws_bytes)) != MOE_OK) return st;
+  if (c.flags & MOE_FLAG_VALIDATE_ONLY) return MOE_OK;
+  const DeviceInfo* d = device_info();
+  if (!d) return MOE_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const Workspace w = workspace_layout(c);
+  const int P = c.T * c.K;
+  if (c.T == 0) {
+    cudaError_t e = cudaMemsetAsync(dw_r, 0, (size_t)c.E * c.h * 4, s);
+    if (e == cudaSuccess && db_r) e = cudaMemsetAsync(db_r, 0, (size_t)c.E * 4, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(dw1, 0, (size_t)c.E * 2 * c.F * c.h * 2, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(dw2, 0, (size_t)c.E * c.h * c.F * 2, s);
+    if (e == cudaSuccess && c.n_shared) e = cudaMemsetAsync(dw1_shared, 0, (size_t)2 * c.F * c.h * 2, s);
+    if (e == cudaSuccess && c.n_shared) e = cudaMemsetAsync(dw2_shared, 0, (size_t)c.h * c.F * 2, s);
+    return cuda_status(e);
+  }
+  const int32_t* offsets = at<int32_t>(ws, w.offsets);
+  const int32_t* dst_row = at<int32_t>(ws, w.dst_row);
+  const int32_t* idx = at<int32_t>(ws, w.topk_idx);
+  float* dl_topk = at<float>(ws, w.dl_topk);
+  // dy in expert order, then the routed experts' backward
+  cudaError_t e = launch_scatter_rows(c, dy, dst_row, at<void>(ws, w.dy_perm), d->sms, d->status, s);
+  if (e == cudaSuccess)
+    e = run_mlp_bwd(c, P, c.E, at<void>(ws, w.dy_perm), at<void>(ws, w.x_perm),
+                    at<void>(ws, w.act_save), at<void>(ws, w.a), offsets,
+                    at<float>(ws, w.perm_prob), w1, w2, at<void>(ws, w.dh),
+                    at<float>(ws, w.dprob_part), at<void>(ws, w.dx_perm), dw1, dw2, d, s);
+  // the shared expert: one group of all T tokens, weight 1
+  if (e == cudaSuccess && c.n_shared)
+    e = run_mlp_bwd(c, c.T, 1, dy, x, at<void>(ws, w.shared_h), at<void>(ws, w.shared_a),
+                    at<int32_t>(ws, w.shared_off), nullptr, w1_shared, w2_shared,
+                    at<void>(ws, w.shared_dh), nullptr, at<void>(ws, w.shared_dx), dw1_shared,
+                    dw2_shared, d, s);
+  // Route backward: dprob -> dl -> dW_r, db_r
+  if (e == cudaSuccess)
+    e = launch_dprob_reduce(at<float>(ws, w.dprob_part), P, (c.F + 255) / 256,
+                            at<float>(ws, w.dprob_perm), s);
+  if (e == cudaSuccess)
+    e = launch_router_bwd(c, at<float>(ws, w.logits), idx, at<float>(ws, w.topk_prob), dst_row,
+                          at<float>(ws, w.dprob_perm), dl_topk, at<float>(ws, w.dl_perm),
+                          d->status, s);
+  if (e == cudaSuccess)
+    e = launch_router_wgrad(c, x, at<int32_t>(ws, w.src_token), offsets, at<float>(ws, w.dl_perm),
+                            dw_r, db_r, s);
+  // dx = routed + shared + router contributions
+  if (e == cudaSuccess)
+    e = launch_bwd_combine(c, at<void>(ws, w.dx_perm), dst_row,
+                           c.n_shared ? at<void>(ws, w.shared_dx) : nullptr, dl_topk, idx, w_r, dx,
+                           nullptr, d->sms, d->status, s);
   return cuda_status(e);
 }
 

@@ -69,7 +69,10 @@ MOE_D float silu_f(float z) { return z * sigmoid_f(z); }
 // what a SAVE_FOR_BWD forward left behind.
 struct Workspace {
   size_t logits, topk_idx, topk_prob, hist, chunk_base, counts, offsets, dst_row, src_token,
-      perm_prob, x_perm, act_save, a, y_perm, shared_off, shared_h, shared_a, shared_y, total;
+      perm_prob, x_perm, act_save, a, y_perm, shared_off, shared_h, shared_a, shared_y,
+      // backward (MOE_FLAG_SAVE_FOR_BWD only)
+      dy_perm, dh, dx_perm, dprob_part, dprob_perm, dl_topk, dl_perm, shared_dh, shared_dx,
+      total;
 };
 
 inline size_t elem_bytes(int dtype) { return dtype == MOE_BF16 ? 2 : 4; }
@@ -106,6 +109,16 @@ inline Workspace workspace_layout(const moe_config_t& c) {
   w.shared_h = take(c.n_shared && save ? T * R1 * eb : 0);
   w.shared_a = take(c.n_shared ? T * F * eb : 0);
   w.shared_y = take(c.n_shared ? T * h * eb : 0);
+  const size_t NT = (F + 255) / 256;  // N tiles of the FC2 data-gradient GEMM
+  w.dy_perm = take(save ? P * h * eb : 0);
+  w.dh = take(save ? P * R1 * eb : 0);
+  w.dx_perm = take(save ? P * h * eb : 0);
+  w.dprob_part = take(save ? P * NT * 4 : 0);
+  w.dprob_perm = take(save ? P * 4 : 0);
+  w.dl_topk = take(save ? P * 4 : 0);
+  w.dl_perm = take(save ? P * 4 : 0);
+  w.shared_dh = take(save && c.n_shared ? T * R1 * eb : 0);
+  w.shared_dx = take(save && c.n_shared ? T * h * eb : 0);
   w.total = off;
   return w;
 }

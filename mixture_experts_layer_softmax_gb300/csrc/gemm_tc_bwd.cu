@@ -1,0 +1,465 @@
+// Backward grouped GEMMs of the expert FFNs on the tensor cores (tcgen05 +
+// TMEM, TMA-fed), bf16 operands, fp32 accumulation.
+//
+// The pages give no backward formulas ("Scalable Training of Mixture-of-
+// Experts Models with Megatron Core", review, §4.1.2 only says which
+// activations are recomputed for it); these are the plain reverse-mode
+// derivatives of the forward expert FFN with the routing held fixed:
+//   G      = dy_perm W2_e                       (FC2 dgrad, [rows, F])
+//   dprob  = <G, silu(g) * u>  per row          (fused, partial sums per N tile)
+//   dH     = [p G u silu'(g), p G silu(g)]      (fused dSwiGLU, [rows, 2F])
+//   dW2_e  = dy_perm_e^T a_e                    (FC2 wgrad, [h, F])
+//   dx_perm= dH W1_e                            (FC1 dgrad, [rows, h])
+//   dW1_e  = dH_e^T x_perm_e                    (FC1 wgrad, [2F, h])
+//
+// Operand layouts come straight from the forward buffers and the weights, no
+// transposes: the dgrad B operand (W2_e read as [F x h], W1_e as [h x 2F]) is
+// MN-major, fetched by a 3-D TMA map [E][K][N] so K never runs into the next
+// expert; the wgrad operands are MN-major slices of the permuted activations,
+// and the reduction runs over the expert's own rows: in the last 64-row block
+// only ceil(v/16) MMA K-steps are issued and the < 16 rows past the expert's
+// end are zeroed in shared memory first.
+//
+// Kernel structure as the forward kernel: persistent, 1 CTA per SM, TMA warp,
+// MMA warp, 4 epilogue warps, 4-stage ring of 48 KB, TMEM 2 x 256 columns,
+// bounded waits.  MN-major tiles are {64 elements, 64 K-rows} TMA boxes with
+// 128-byte swizzle (8 KB each): LBO = 8 KB between 64-element atoms, SBO =
+// 1 KB between 8-row groups.
+#include "tc_ptx.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;  // 16 KB
+constexpr int B_BYTES = BN * BK * 2;  // 32 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int ATOM = 64 * 64 * 2;     // one MN-major {64, 64} box
+constexpr uint32_t TMEM_COLS = 512;
+constexpr int kThreads = 192;
+
+enum BwdKind { kDgradSwiGLU = 0, kDgradPlain = 1, kWgrad = 2 };
+
+struct BwdParams {
+  const int32_t* offsets;      // [E+1]
+  const float* prob;           // dSwiGLU: [rows] or null (weight 1)
+  const __nv_bfloat16* H;      // dSwiGLU: pre-activation [rows, 2N] (gate | up)
+  __nv_bfloat16* out;          // dSwiGLU: dH [rows, 2N]; plain: [rows, N]; wgrad: [E][M][N]
+  float* dprob_part;           // dSwiGLU: [rows, nblk] or null
+  int E, Kd, M, N;
+  int* status;
+  uint64_t wait_limit_ns;
+};
+
+struct SmemCtl {
+  uint64_t full[STAGES], empty[STAGES], tmem_full[2], tmem_empty[2], drain;
+  uint32_t tmem_base;
+  int abort;
+  int tile_start[257];
+  int off[257];
+};
+
+constexpr size_t kSmemBytes = 1024 + (size_t)STAGES * STAGE_BYTES + sizeof(SmemCtl);
+
+MOE_D void tma_load_3d(uint32_t dst, const CUtensorMap* map, int32_t c0, int32_t c1, int32_t c2,
+                       uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+      : "memory");
+}
+
+MOE_D uint32_t pack2(float a, float b) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+MOE_D void store8(__nv_bfloat16* dst, const float* v) {
+  uint4 u;
+  u.x = pack2(v[0], v[1]); u.y = pack2(v[2], v[3]); u.z = pack2(v[4], v[5]); u.w = pack2(v[6], v[7]);
+  *reinterpret_cast<uint4*>(dst) = u;
+}
+MOE_D void load8(const __nv_bfloat16* src, float* v) {
+  const uint4 u = *reinterpret_cast<const uint4*>(src);
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    v[2 * i] = __low2float(h[i]);
+    v[2 * i + 1] = __high2float(h[i]);
+  }
+}
+
+template <int KIND>
+struct Tiles {
+  // dgrad: row tiles of each expert x N tiles; wgrad: M tiles x N tiles per expert
+  MOE_D static void decode(const SmemCtl& c, int E, int mt, int nt, int tile, int& e, int& mb,
+                           int& nb) {
+    if (KIND == kWgrad) {
+      const int tpe = mt * nt;
+      e = tile / tpe;
+      const int local = tile - e * tpe;
+      nb = local / mt;
+      mb = local - nb * mt;
+      return;
+    }
+    int lo = 0, hi = E - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (c.tile_start[mid] <= tile) lo = mid; else hi = mid - 1;
+    }
+    e = lo;
+    const int local = tile - c.tile_start[e];
+    const int mblk = (c.off[e + 1] - c.off[e] + BM - 1) / BM;
+    nb = local / mblk;
+    mb = local - nb * mblk;
+  }
+};
+
+template <int KIND>
+__global__ void __launch_bounds__(kThreads, 1)
+    grouped_gemm_tc_bwd_kernel(const __grid_constant__ CUtensorMap tmA,
+                               const __grid_constant__ CUtensorMap tmB, const BwdParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + STAGES * A_BYTES;
+  SmemCtl& ctl = *reinterpret_cast<SmemCtl*>(smem + STAGES * STAGE_BYTES);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int E = p.E;
+  const int nt = (p.N + BN - 1) / BN;
+  const int mt = (p.M + BM - 1) / BM;  // wgrad only
+  const int KBfix = (p.Kd + BK - 1) / BK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      tc::mbar_init(tc::smem_u32(&ctl.full[s]), 1);
+      tc::mbar_init(tc::smem_u32(&ctl.empty[s]), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      tc::mbar_init(tc::smem_u32(&ctl.tmem_full[a]), 1);
+      tc::mbar_init(tc::smem_u32(&ctl.tmem_empty[a]), 4);
+    }
+    tc::mbar_init(tc::smem_u32(&ctl.drain), 1);
+    ctl.abort = 0;
+    tc::fence_barrier_init();
+    tc::fence_proxy_async_smem();
+    tc::prefetch_tensormap(&tmA);
+    tc::prefetch_tensormap(&tmB);
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(tc::smem_u32(&ctl.tmem_base), TMEM_COLS);
+    tc::tmem_relinquish();
+  }
+  for (int e = threadIdx.x; e <= E; e += kThreads) ctl.off[e] = __ldg(p.offsets + e);
+  __syncthreads();
+  if (warp == 2) {
+    if (KIND == kWgrad) {
+      if (lane == 0) ctl.tile_start[E] = E * mt * nt;
+    } else {
+      int running = 0;
+      for (int e0 = 0; e0 < E; e0 += 32) {
+        const int e = e0 + lane;
+        const int v = e < E ? ((ctl.off[e + 1] - ctl.off[e] + BM - 1) / BM) * nt : 0;
+        int incl = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int t = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += t;
+        }
+        if (e < E) ctl.tile_start[e] = running + incl - v;
+        running += __shfl_sync(0xffffffffu, incl, 31);
+      }
+      if (lane == 0) ctl.tile_start[E] = running;
+    }
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem_base = ctl.tmem_base;
+  const int total = ctl.tile_start[E];
+  tc::WaitCtl wc{p.status, &ctl.abort, p.wait_limit_ns, 0};
+  tc::WaitCtl wdrain{p.status, nullptr, 1000000000ull, 0};
+
+  if (warp == 0) {
+    // ================= TMA producer =================
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0, issued = 0, issued_par = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+        int e, mb, nb;
+        Tiles<KIND>::decode(ctl, E, mt, nt, tile, e, mb, nb);
+        const int rows0 = ctl.off[e];
+        const int m_e = ctl.off[e + 1] - rows0;
+        const int KB = KIND == kWgrad ? (m_e + BK - 1) / BK : KBfix;
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!tc::mbar_wait(tc::smem_u32(&ctl.empty[stage]), phase ^ 1, wc)) { ok = false; break; }
+          const uint32_t fb = tc::smem_u32(&ctl.full[stage]);
+          tc::mbar_arrive_expect_tx(fb, STAGE_BYTES);
+          const uint32_t a_dst = tc::smem_u32(sA + stage * A_BYTES);
+          const uint32_t b_dst = tc::smem_u32(sB + stage * B_BYTES);
+          if (KIND == kWgrad) {
+            const int krow = rows0 + kb * BK;
+#pragma unroll
+            for (int j = 0; j < 2; ++j) tc::tma_load_2d(a_dst + j * ATOM, &tmA, mb * BM + j * 64, krow, fb);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) tc::tma_load_2d(b_dst + j * ATOM, &tmB, nb * BN + j * 64, krow, fb);
+          } else {
+            tc::tma_load_2d(a_dst, &tmA, kb * BK, rows0 + mb * BM, fb);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) tma_load_3d(b_dst + j * ATOM, &tmB, nb * BN + j * 64, kb * BK, e, fb);
+          }
+          issued |= 1u << stage;
+          issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
+          if (++stage == STAGES) { stage = 0; phase ^= 1; }
+        }
+      }
+      for (int s = 0; s < STAGES; ++s)
+        if ((issued >> s) & 1u)
+          tc::mbar_wait(tc::smem_u32(&ctl.full[s]), (issued_par >> s) & 1u, wdrain);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ================= MMA issuer (whole warp: the wgrad tail is zeroed by all lanes) =====
+    constexpr uint32_t idesc = tc::idesc_bf16_f32(BM, BN, KIND == kWgrad, true);
+    int stage = 0, acc = 0;
+    uint32_t phase = 0, acc_phase = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+      int e, mb, nb;
+      Tiles<KIND>::decode(ctl, E, mt, nt, tile, e, mb, nb);
+      const int m_e = ctl.off[e + 1] - ctl.off[e];
+      const int KB = KIND == kWgrad ? (m_e + BK - 1) / BK : KBfix;
+      int w_ok = lane == 0 ? (int)tc::mbar_wait(tc::smem_u32(&ctl.tmem_empty[acc]), acc_phase ^ 1, wc) : 0;
+      if (!__shfl_sync(0xffffffffu, w_ok, 0)) break;
+      tc::fence_after_sync();
+      const uint32_t d = tmem_base + (uint32_t)(acc * BN);
+      for (int kb = 0; kb < KB; ++kb) {
+        w_ok = lane == 0 ? (int)tc::mbar_wait(tc::smem_u32(&ctl.full[stage]), phase, wc) : 0;
+        if (!__shfl_sync(0xffffffffu, w_ok, 0)) { ok = false; break; }
+        tc::fence_after_sync();
+        int nk = BK / 16;
+        if (KIND == kWgrad) {
+          const int v = m_e - kb * BK;  // valid K rows in this block
+          if (v < BK) {
+            // every writing lane acquires the completed TMA phase itself (it
+            // completed already: this returns at the first poll)
+            if (!tc::mbar_wait(tc::smem_u32(&ctl.full[stage]), phase, wc)) ok = false;
+            if (!__all_sync(0xffffffffu, ok)) {
+              ok = false;
+              break;
+            }
+            nk = (v + 15) / 16;
+            const int v16 = nk * 16;
+            // zero rows [v, v16) of the 2 A atoms and 4 B atoms (whole 128-B
+            // rows: the swizzle only permutes 16-B chunks inside a row)
+            const int nrows = v16 - v;
+            for (int i = lane; i < nrows * 8 * 6; i += 32) {
+              const int atom = i / (nrows * 8);
+              const int rem = i - atom * nrows * 8;
+              const int row = v + rem / 8, chunk = rem % 8;
+              uint8_t* base = atom < 2 ? sA + stage * A_BYTES + atom * ATOM
+                                       : sB + stage * B_BYTES + (atom - 2) * ATOM;
+              *reinterpret_cast<uint4*>(base + row * 128 + chunk * 16) = make_uint4(0, 0, 0, 0);
+            }
+            tc::fence_proxy_async_smem();
+            __syncwarp();
+          }
+        }
+        if (lane == 0) {
+          const uint32_t a0 = tc::smem_u32(sA + stage * A_BYTES);
+          const uint32_t b0 = tc::smem_u32(sB + stage * B_BYTES);
+          for (int k = 0; k < nk; ++k) {
+            const uint64_t ad = KIND == kWgrad ? tc::desc_mnmajor_sw128(a0 + k * 2048, ATOM)
+                                               : tc::desc_kmajor_sw128(a0 + k * 32);
+            const uint64_t bd = tc::desc_mnmajor_sw128(b0 + k * 2048, ATOM);
+            tc::mma_bf16(d, ad, bd, idesc, (kb | k) != 0);
+          }
+          tc::mma_commit(tc::smem_u32(&ctl.empty[stage]));
+        }
+        __syncwarp();
+        if (++stage == STAGES) { stage = 0; phase ^= 1; }
+      }
+      if (!ok) break;
+      if (lane == 0) tc::mma_commit(tc::smem_u32(&ctl.tmem_full[acc]));
+      __syncwarp();
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1;
+    }
+    if (lane == 0 && ctl.abort) {
+      tc::mma_commit(tc::smem_u32(&ctl.drain));
+      tc::mbar_wait(tc::smem_u32(&ctl.drain), 0, wdrain);
+    }
+    __syncwarp();
+  } else {
+    // ================= epilogue (warps 2..5) =================
+    const int q = warp & 3;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+      int e, mb, nb;
+      Tiles<KIND>::decode(ctl, E, mt, nt, tile, e, mb, nb);
+      if (!tc::mbar_wait(tc::smem_u32(&ctl.tmem_full[acc]), acc_phase, wc)) break;
+      tc::fence_after_sync();
+      const int m_e = ctl.off[e + 1] - ctl.off[e];
+      const uint32_t tbase = tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(q * 32) << 16);
+      if (KIND == kWgrad) {
+        const int m = mb * BM + q * 32 + lane;
+        __nv_bfloat16* orow = p.out + ((int64_t)e * p.M + m) * p.N;
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t r[32];
+          if (m_e > 0) tc::tmem_ld_32x32b_x32(tbase + c * 32, r);
+          const int n = nb * BN + c * 32;
+          if (m < p.M) {
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+              if (n + g * 8 >= p.N) break;
+              float v[8];
+#pragma unroll
+              for (int i = 0; i < 8; ++i) v[i] = m_e > 0 ? __uint_as_float(r[g * 8 + i]) : 0.f;
+              store8(orow + n + g * 8, v);
+            }
+          }
+        }
+      } else {
+        const int local_row = mb * BM + q * 32 + lane;
+        const bool valid = local_row < m_e;
+        const int64_t row = (int64_t)ctl.off[e] + local_row;
+        float pr = 1.f, dpr = 0.f;
+        if (KIND == kDgradSwiGLU && valid && p.prob) pr = __ldg(p.prob + row);
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t r[32];
+          tc::tmem_ld_32x32b_x32(tbase + c * 32, r);
+          const int n = nb * BN + c * 32;
+          if (!valid) continue;
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            const int n8 = n + g * 8;
+            if (n8 >= p.N) break;
+            float G[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) G[i] = __uint_as_float(r[g * 8 + i]);
+            if (KIND == kDgradPlain) {
+              store8(p.out + row * p.N + n8, G);
+            } else {
+              float gt[8], up[8], dg[8], du[8];
+              load8(p.H + row * 2 * p.N + n8, gt);
+              load8(p.H + row * 2 * p.N + p.N + n8, up);
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                const float s = sigmoid_f(gt[i]);
+                const float sl = gt[i] * s;
+                dpr = fmaf(G[i], sl * up[i], dpr);
+                const float dz = pr * G[i];
+                du[i] = dz * sl;
+                dg[i] = dz * up[i] * (s * (1.f + gt[i] * (1.f - s)));
+              }
+              store8(p.out + row * 2 * p.N + n8, dg);
+              store8(p.out + row * 2 * p.N + p.N + n8, du);
+            }
+          }
+        }
+        if (KIND == kDgradSwiGLU && valid && p.dprob_part) p.dprob_part[row * nt + nb] = dpr;
+      }
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(tc::smem_u32(&ctl.tmem_empty[acc]));
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1;
+    }
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      return reinterpret_cast<EncodeTiledFn>(ptr);
+    return (EncodeTiledFn) nullptr;
+  }();
+  return fn;
+}
+
+// bf16 map with a {64, rows} box: 2-D [rows, cols] when depth == 0, else
+// 3-D [depth][rows][cols].  128-byte swizzle, zero fill out of bounds.
+bool encode_map(CUtensorMap* m, const void* base, uint64_t depth, uint64_t rows, uint64_t cols,
+                uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {cols, rows, depth ? depth : 1};
+  const cuuint64_t strides[2] = {cols * 2, rows * cols * 2};
+  const cuuint32_t box[3] = {64, box_rows, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, depth ? 3 : 2, const_cast<void*>(base), dims,
+            strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int KIND>
+cudaError_t launch_kind(const CUtensorMap& a, const CUtensorMap& b, const BwdParams& p, int grid,
+                        cudaStream_t s) {
+  cudaError_t e = cudaFuncSetAttribute(grouped_gemm_tc_bwd_kernel<KIND>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+  if (e != cudaSuccess) return e;
+  grouped_gemm_tc_bwd_kernel<KIND><<<grid, kThreads, kSmemBytes, s>>>(a, b, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+// Data gradient through one expert weight: out = A W_e with A [rows, Kd]
+// (K-major) and W [E][Kd][N].  swiglu: also the fused dSwiGLU epilogue, with H
+// [rows, 2N], p [rows] (null: 1), out = dH [rows, 2N], dprob_part [rows, ceil(N/256)].
+cudaError_t launch_tc_dgrad(bool swiglu, int rows, const void* A, int Kd, const void* W, int E,
+                            int N, const int32_t* offsets, const float* prob, const void* H,
+                            void* out, float* dprob_part, int sms, int* status, cudaStream_t s) {
+  if (rows == 0) return cudaSuccess;
+  CUtensorMap ma, mb;
+  if (!encode_map(&ma, A, 0, (uint64_t)rows, (uint64_t)Kd, BM)) return cudaErrorInvalidValue;
+  if (!encode_map(&mb, W, (uint64_t)E, (uint64_t)Kd, (uint64_t)N, 64)) return cudaErrorInvalidValue;
+  BwdParams p{};
+  p.offsets = offsets; p.prob = prob; p.H = static_cast<const __nv_bfloat16*>(H);
+  p.out = static_cast<__nv_bfloat16*>(out); p.dprob_part = dprob_part;
+  p.E = E; p.Kd = Kd; p.M = 0; p.N = N; p.status = status; p.wait_limit_ns = 2000000000ull;
+  const int64_t tiles_max = (ceil_div(rows, BM) + E) * ceil_div(N, BN);
+  const int grid = (int)(tiles_max < sms ? tiles_max : sms);
+  return swiglu ? launch_kind<kDgradSwiGLU>(ma, mb, p, grid, s)
+                : launch_kind<kDgradPlain>(ma, mb, p, grid, s);
+}
+
+// Weight gradient of every expert: dW_e = A_e^T B_e with A [rows, M] and
+// B [rows, N] (the expert's rows offsets[e]..offsets[e+1]), out [E][M][N];
+// experts without rows get zeros.
+cudaError_t launch_tc_wgrad(int rows, const void* A, int M, const void* B, int N, int E,
+                            const int32_t* offsets, void* out, int sms, int* status,
+                            cudaStream_t s) {
+  CUtensorMap ma, mb;
+  const uint64_t r = rows > 0 ? (uint64_t)rows : 1;  // a map needs a non-empty extent
+  if (!encode_map(&ma, A, 0, r, (uint64_t)M, 64)) return cudaErrorInvalidValue;
+  if (!encode_map(&mb, B, 0, r, (uint64_t)N, 64)) return cudaErrorInvalidValue;
+  BwdParams p{};
+  p.offsets = offsets; p.out = static_cast<__nv_bfloat16*>(out);
+  p.E = E; p.Kd = 0; p.M = M; p.N = N; p.status = status; p.wait_limit_ns = 2000000000ull;
+  const int64_t tiles = (int64_t)E * ceil_div(M, BM) * ceil_div(N, BN);
+  const int grid = (int)(tiles < sms ? tiles : sms);
+  return launch_kind<kWgrad>(ma, mb, p, grid, s);
+}
+
+}  // namespace moe

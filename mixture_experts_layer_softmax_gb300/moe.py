@@ -59,6 +59,9 @@ _SIG = {
     "moe_unpermute_combine": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P]),
     "moe_layer_fwd": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                      ctypes.c_size_t, _P]),
+    "moe_grouped_mlp_bwd": (ctypes.c_int, [_CFG] + [_P] * 13 + [ctypes.c_size_t, _P]),
+    "moe_router_bwd": (ctypes.c_int, [_CFG] + [_P] * 14 + [ctypes.c_size_t, _P]),
+    "moe_layer_bwd": (ctypes.c_int, [_CFG] + [_P] * 15 + [ctypes.c_size_t, _P]),
     "moe_get_error": (ctypes.c_int, [_P]),
     "moe_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "moe_version": (ctypes.c_char_p, []),
@@ -197,6 +200,33 @@ def moe_layer_fwd(cfg, x, w_r, gate_bias, sel_bias, w1, b1, w2, b2, w1_shared, w
         ctypes.byref(cfg), _ptr(x), _ptr(w_r), _ptr(gate_bias), _ptr(sel_bias), _ptr(w1),
         _ptr(b1), _ptr(w2), _ptr(b2), _ptr(w1_shared), _ptr(w2_shared), _ptr(y),
         _ptr(topk_idx_out), _ptr(topk_prob_out), wp, wb, _stream(stream)))
+
+
+def moe_grouped_mlp_bwd(cfg, dy_perm, x_perm, act_save, a, offsets, perm_prob, w1, w2, dx_perm,
+                        dw1, dw2, dprob_perm, ws, stream=None):
+    wp, wb = _ws(ws)
+    _check("moe_grouped_mlp_bwd", _lib.moe_grouped_mlp_bwd(
+        ctypes.byref(cfg), _ptr(dy_perm), _ptr(x_perm), _ptr(act_save), _ptr(a), _ptr(offsets),
+        _ptr(perm_prob), _ptr(w1), _ptr(w2), _ptr(dx_perm), _ptr(dw1), _ptr(dw2), _ptr(dprob_perm),
+        wp, wb, _stream(stream)))
+
+
+def moe_router_bwd(cfg, x, logits, topk_idx, topk_prob, offsets, dst_row, src_token, dprob_perm,
+                   w_r, dl_topk, dw_r, db_r, dx_router, ws, stream=None):
+    wp, wb = _ws(ws)
+    _check("moe_router_bwd", _lib.moe_router_bwd(
+        ctypes.byref(cfg), _ptr(x), _ptr(logits), _ptr(topk_idx), _ptr(topk_prob), _ptr(offsets),
+        _ptr(dst_row), _ptr(src_token), _ptr(dprob_perm), _ptr(w_r), _ptr(dl_topk), _ptr(dw_r),
+        _ptr(db_r), _ptr(dx_router), wp, wb, _stream(stream)))
+
+
+def moe_layer_bwd(cfg, x, w_r, w1, w2, w1_shared, w2_shared, dy, dx, dw_r, db_r, dw1, dw2,
+                  dw1_shared, dw2_shared, ws, stream=None):
+    wp, wb = _ws(ws)
+    _check("moe_layer_bwd", _lib.moe_layer_bwd(
+        ctypes.byref(cfg), _ptr(x), _ptr(w_r), _ptr(w1), _ptr(w2), _ptr(w1_shared),
+        _ptr(w2_shared), _ptr(dy), _ptr(dx), _ptr(dw_r), _ptr(db_r), _ptr(dw1), _ptr(dw2),
+        _ptr(dw1_shared), _ptr(dw2_shared), wp, wb, _stream(stream)))
 
 
 def moe_get_error(stream=None) -> int:

@@ -504,6 +504,38 @@ def layer_bwd(x, w_r, w1, w2, dy, K, score, act, *, b1=None, b2=None, sel_bias=N
                 idx=idx, probs=probs, logits=logits)
 
 
+def grouped_mlp_bwd(x_perm, offsets, prob_perm, w1, w2, dy_perm):
+    """Backward of the bias-free SwiGLU expert FFNs over permuted rows (the
+    grouped-GEMM part of layer_bwd, written per expert on its own rows):
+    returns dx_perm [P,h], dw1 [E,2F,h], dw2 [E,h,F] and dprob_perm [P] with
+    dprob_perm[r] = <dy_perm[r], E_e(x_perm[r])>."""
+    x_perm = np.asarray(x_perm, np.float64)
+    dy_perm = np.asarray(dy_perm, np.float64)
+    prob_perm = np.asarray(prob_perm, np.float64)
+    E = len(offsets) - 1
+    dx = np.zeros_like(x_perm)
+    dprob = np.zeros(x_perm.shape[0])
+    dw1 = np.zeros((E,) + np.asarray(w1[0]).shape)
+    dw2 = np.zeros((E,) + np.asarray(w2[0]).shape)
+    for e in range(E):
+        r = slice(int(offsets[e]), int(offsets[e + 1]))
+        if offsets[e + 1] == offsets[e]:
+            continue
+        w1e = np.asarray(w1[e], np.float64)
+        w2e = np.asarray(w2[e], np.float64)
+        H, z = expert_hidden(x_perm[r], w1e, None, ACT_SWIGLU)
+        dprob[r] = (dy_perm[r] * (z @ w2e.T)).sum(axis=1)
+        dout = prob_perm[r, None] * dy_perm[r]
+        dw2[e] = dout.T @ z
+        dz = dout @ w2e
+        F = w1e.shape[0] // 2
+        g, u = H[:, :F], H[:, F:]
+        dH = np.concatenate([dz * u * silu_grad(g), dz * silu(g)], axis=1)
+        dw1[e] = dH.T @ x_perm[r]
+        dx[r] = dH @ w1e
+    return dict(dx_perm=dx, dw1=dw1, dw2=dw2, dprob_perm=dprob)
+
+
 # ---------------------------------------------------------------------------
 # Work accounting (closed forms used by the benchmark's roofline figures)
 # ---------------------------------------------------------------------------

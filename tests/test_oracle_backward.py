@@ -100,3 +100,18 @@ def test_unused_expert_gets_zero_gradient():
     kw["gate_bias"] = np.array([0.0, 0.0, 0.0, -1e9])  # expert 3 never selected
     g = O.layer_bwd(x, w_r, w1, w2, dy, 1, O.SCORE_SOFTMAX, O.ACT_SWIGLU, logits_dtype=np.float64, **kw)
     assert (g["dw1"][3] == 0).all() and (g["dw2"][3] == 0).all()
+
+
+def test_grouped_mlp_bwd_matches_layer_bwd():
+    # the permuted-row expert backward agrees with the layer backward's expert
+    # gradients, its dprob and (un-permuted) its dx contribution
+    x, w_r, w1, w2, dy, kw = _problem(34, O.SCORE_SIGMOID, O.ACT_SWIGLU, False, False, T=15, E=5, K=3)
+    full = O.layer_bwd(x, w_r, w1, w2, dy, 3, O.SCORE_SIGMOID, O.ACT_SWIGLU, logits_dtype=np.float64, **kw)
+    idx, probs = full["idx"], full["probs"]
+    counts, offsets, dst_row, src_token, src_slot = O.dispatch_maps(idx, 5)
+    g = O.grouped_mlp_bwd(x[src_token], offsets, probs[src_token, src_slot], w1, w2, dy[src_token])
+    np.testing.assert_allclose(g["dw1"], full["dw1"], rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(g["dw2"], full["dw2"], rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(g["dprob_perm"][dst_row], full["dprob"], rtol=1e-12, atol=1e-13)
+    routed_dx = O.unpermute_combine(g["dx_perm"], dst_row)
+    np.testing.assert_allclose(routed_dx + full["dlogits"] @ w_r, full["dx"], rtol=1e-11, atol=1e-12)
