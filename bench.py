@@ -48,6 +48,9 @@ def parse():
     p.add_argument("--workload", default=None, help="workload name (default: the Mixtral-shaped layer)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-graph", action="store_true",
+                   help="time eager launches only (default: the step is also captured in a CUDA "
+                        "graph and the graph replays give the headline time)")
     p.add_argument("--sample-tokens", type=int, default=0, help="oracle sample size (0: auto)")
     p.add_argument("--tokens", type=int, default=0,
                    help="override T (smaller cases for profiler captures; not a bench line)")
@@ -245,6 +248,8 @@ def workload_config(w):
             "act": "swiglu" if w.act == 1 else "gelu", "n_shared": w.n_shared,
             "routing": "force-balanced" if w.force_balance else "router",
             "l2": "flushed before every timed step (512 MB write, outside the events)",
+            "timing": "CUDA events per step; value from CUDA-graph replays of the step, stage "
+                      "breakdown from eager launches",
             "inputs": "seeded synthetic (SplitMix64 + Box-Muller), generated on the device"}
 
 
@@ -327,28 +332,58 @@ def run_ours(args, w):
     stream = torch.cuda.current_stream(dev)
 
     stages = ["route", "dispatch", "fc1", "fc2", "shared", "combine"]
+    train = w.backward
+    if train:
+        # training step: the whole forward (saving for backward) then the whole
+        # backward, each one C-ABI call, on the same workspace
+        cfg = M.config_for(w, M.MOE_FLAG_SAVE_FOR_BWD)
+        ws = torch.empty(M.moe_workspace_size(cfg), dtype=torch.uint8, device=dev)
+        dy = gen("dy", (T, h), bf, seed + 1)
+        dx = torch.empty(T, h, dtype=bf, device=dev)
+        dw_r = torch.empty(E, h, dtype=torch.float32, device=dev)
+        dw1 = torch.empty_like(w1)
+        dw2 = torch.empty_like(w2)
+        dw1s = torch.empty_like(w1s) if w.n_shared else None
+        dw2s = torch.empty_like(w2s) if w.n_shared else None
+        stages = ["forward", "backward"]
 
-    def step(ev=None):
-        def mark(i):
+        def step(ev=None):
             if ev is not None:
-                ev[i].record(stream)
-        mark(0)
-        M.moe_router_topk(cfg, x, w_r, gate_bias, sel_bias, None, idx, prob, None, ws)
-        mark(1)
-        M.moe_permute(cfg, x, idx, prob, x_perm, counts, offsets, dst_row, src_token, perm_prob, ws)
-        mark(2)
-        M.moe_expert_fc1(cfg, x_perm, offsets, perm_prob, w1, b1, None, a)
-        mark(3)
-        M.moe_expert_fc2(cfg, a, offsets, perm_prob, w2, b2, y_perm)
-        mark(4)
-        if w.n_shared:
-            M.moe_expert_fc1(cs, x, soff, None, w1s, None, None, a_s)
-            M.moe_expert_fc2(cs, a_s, soff, None, w2s, None, y_s)
-        mark(5)
-        M.moe_unpermute_combine(cfg, y_perm, dst_row, None, y_s if w.n_shared else None, y)
-        mark(6)
+                ev[0].record(stream)
+            M.moe_layer_fwd(cfg, x, w_r, gate_bias, sel_bias, w1, b1, w2, b2, w1s, w2s, y, None,
+                            None, ws)
+            if ev is not None:
+                ev[1].record(stream)
+            M.moe_layer_bwd(cfg, x, w_r, w1, w2, w1s, w2s, dy, dx, dw_r, None, dw1, dw2, dw1s,
+                            dw2s, ws)
+            if ev is not None:
+                ev[2].record(stream)
+    else:
+        def step(ev=None):
+            def mark(i):
+                if ev is not None:
+                    ev[i].record(stream)
+            mark(0)
+            M.moe_router_topk(cfg, x, w_r, gate_bias, sel_bias, None, idx, prob, None, ws)
+            mark(1)
+            M.moe_permute(cfg, x, idx, prob, x_perm, counts, offsets, dst_row, src_token,
+                          perm_prob, ws)
+            mark(2)
+            M.moe_expert_fc1(cfg, x_perm, offsets, perm_prob, w1, b1, None, a)
+            mark(3)
+            M.moe_expert_fc2(cfg, a, offsets, perm_prob, w2, b2, y_perm)
+            mark(4)
+            if w.n_shared:
+                M.moe_expert_fc1(cs, x, soff, None, w1s, None, None, a_s)
+                M.moe_expert_fc2(cs, a_s, soff, None, w2s, None, y_s)
+            mark(5)
+            M.moe_unpermute_combine(cfg, y_perm, dst_row, None, y_s if w.n_shared else None, y)
+            mark(6)
 
-    launches_per_step = (1 if E <= 32 else 2) + 4 + 2 + (2 if w.n_shared else 0) + 1
+    launches_per_step = (1 if E <= 32 else 2) + 4 + 2 + ((3 if train else 2) if w.n_shared else 0) + 1
+    if train:  # backward: scatter, 4 GEMMs (+4 shared), dprob, router, router wgrad, combine
+        launches_per_step += 1 + 4 + (4 if w.n_shared else 0) + 4
+    n_ev = len(stages) + 1
 
     for _ in range(max(args.warmup, 3)):
         flush_buf.fill_(1)
@@ -358,7 +393,7 @@ def run_ours(args, w):
     if st != M.MOE_OK:
         raise RuntimeError(f"device status after warm-up: {M.moe_status_string(st)}")
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in range(args.steps)]
     sampler = ClockSampler(local)
     sampler.start()
     time.sleep(0.3)
@@ -380,9 +415,41 @@ def run_ours(args, w):
     if st != M.MOE_OK:
         raise RuntimeError(f"device status after the timed steps: {M.moe_status_string(st)}")
 
-    per_step = [e[0].elapsed_time(e[6]) for e in evs]
+    per_step = [e[0].elapsed_time(e[n_ev - 1]) for e in evs]
     stage_ms = {s: statistics.mean(e[i].elapsed_time(e[i + 1]) for e in evs) for i, s in enumerate(stages)}
-    ms = statistics.mean(per_step)
+    ms_eager = ms = statistics.mean(per_step)
+
+    # The same step captured once in a CUDA graph (the layer never syncs or
+    # allocates, so it captures as is), replayed with the L2 flush in between.
+    graph_ms = None
+    if not args.no_graph:
+        try:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                step()
+            g.replay()
+            torch.cuda.synchronize()
+            gev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(args.steps)]
+            if world > 1:
+                torch.distributed.barrier()
+            torch.cuda.synchronize()
+            for i in range(args.steps):
+                flush_buf.fill_(1)
+                gev[i][0].record(stream)
+                g.replay()
+                gev[i][1].record(stream)
+            torch.cuda.synchronize()
+            if world > 1:
+                torch.distributed.barrier()
+            graph_ms = statistics.mean(a.elapsed_time(b) for a, b in gev)
+            st = M.moe_get_error()
+            if st != M.MOE_OK:
+                raise RuntimeError(M.moe_status_string(st))
+            ms = graph_ms
+        except Exception as exc:  # report, keep the eager number
+            print(f"graph capture unavailable: {exc}", file=sys.stderr)
+            graph_ms = None
     if world > 1:
         t = torch.tensor([ms], dtype=torch.float64, device=dev)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
@@ -391,7 +458,7 @@ def run_ours(args, w):
 
     # ---- end to end through moe_layer_fwd with host buffers ----
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and not train:
         x_host = x.cpu().pin_memory()
         y_host = torch.empty(T, h, dtype=bf).pin_memory()
         x_in = torch.empty_like(x)
@@ -434,36 +501,42 @@ def run_ours(args, w):
 
     pk, pk_kind = peaks()
     esz = 2 if w.dtype == "bf16" else 4
-    fc1_flops = 2.0 * P * h * w.w1_rows
-    fc2_flops = 2.0 * P * F * h
-    fc1_s = stage_ms["fc1"] / 1000.0
-    fc1_tf = fc1_flops / fc1_s / 1e12
-    gemm_tf = (fc1_flops + fc2_flops) / ((stage_ms["fc1"] + stage_ms["fc2"]) / 1000.0) / 1e12
-    perm_bytes = T * h * esz + P * h * esz
-    comb_bytes = P * h * esz + T * h * esz + (T * h * esz if w.n_shared else 0)
-    perm_gbs = perm_bytes / (stage_ms["dispatch"] / 1000.0) / 1e9
-    comb_gbs = comb_bytes / (stage_ms["combine"] / 1000.0) / 1e9
     peak_tf = pk["bf16_tflops_sustained"]
-    rec = traffic_record(w)
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "f32",
-        "data": "synthetic", "config": workload_config(w),
-        "roofline": {"kernel": "grouped_gemm_tc_kernel<SwiGLU FC1>", "bound": "tensor",
-                     "achieved": fc1_tf, "peak": peak_tf, "unit": "TFLOP/s", "frac": fc1_tf / peak_tf,
-                     "peak_kind": f"{pk_kind} bf16 sustained", "traffic": rec,
-                     "flops_per_launch": fc1_flops, "ms_per_launch": stage_ms["fc1"]},
-        "grouped_gemm_pct_bf16_peak": 100.0 * gemm_tf / peak_tf,
-        "grouped_gemm_tflops": gemm_tf,
-        "permute_pct_hbm": 100.0 * perm_gbs / pk["hbm_gbs"],
-        "combine_pct_hbm": 100.0 * comb_gbs / pk["hbm_gbs"],
-        "stages_ms": stage_ms,
-        "gpu_launches": launches_per_step * args.steps,
-        "clocks": clocks,
-        "e2e": e2e,
-        "wall_s_timed": t_wall,
+        "data": "synthetic", "config": workload_config(w), "stages_ms": stage_ms,
+        "gpu_launches": launches_per_step * args.steps, "clocks": clocks, "e2e": e2e,
+        "wall_s_timed": t_wall, "ms_per_step_eager": ms_eager, "cuda_graph": graph_ms is not None,
     }
+    if train:
+        fwd_fl = w.flops_fwd()
+        tot_fl = 3 * fwd_fl  # backward GEMMs: data + weight gradients = 2x forward
+        line["config"]["step"] = "forward + backward"
+        line["layer_tflops"] = tot_fl / (ms / 1000.0) / 1e12
+        line["layer_pct_bf16_peak"] = 100.0 * line["layer_tflops"] / peak_tf
+        line["forward_tflops"] = fwd_fl / (stage_ms["forward"] / 1000.0) / 1e12
+        line["backward_tflops"] = 2 * fwd_fl / (stage_ms["backward"] / 1000.0) / 1e12
+    else:
+        fc1_flops = 2.0 * P * h * w.w1_rows
+        fc2_flops = 2.0 * P * F * h
+        fc1_tf = fc1_flops / (stage_ms["fc1"] / 1000.0) / 1e12
+        gemm_tf = (fc1_flops + fc2_flops) / ((stage_ms["fc1"] + stage_ms["fc2"]) / 1000.0) / 1e12
+        perm_bytes = T * h * esz + P * h * esz
+        comb_bytes = P * h * esz + T * h * esz + (T * h * esz if w.n_shared else 0)
+        perm_gbs = perm_bytes / (stage_ms["dispatch"] / 1000.0) / 1e9
+        comb_gbs = comb_bytes / (stage_ms["combine"] / 1000.0) / 1e9
+        line["roofline"] = {"kernel": "grouped_gemm_tc_kernel<FC1>", "bound": "tensor",
+                            "achieved": fc1_tf, "peak": peak_tf, "unit": "TFLOP/s",
+                            "frac": fc1_tf / peak_tf, "peak_kind": f"{pk_kind} bf16 sustained",
+                            "traffic": traffic_record(w), "flops_per_launch": fc1_flops,
+                            "ms_per_launch": stage_ms["fc1"]}
+        line["grouped_gemm_pct_bf16_peak"] = 100.0 * gemm_tf / peak_tf
+        line["grouped_gemm_tflops"] = gemm_tf
+        line["permute_pct_hbm"] = 100.0 * perm_gbs / pk["hbm_gbs"]
+        line["combine_pct_hbm"] = 100.0 * comb_gbs / pk["hbm_gbs"]
+        line["route_ms"] = stage_ms["route"]
     if not args.no_cpu_baseline:
         S = args.sample_tokens or auto_sample(w)
         samp = OracleSample(w, S)

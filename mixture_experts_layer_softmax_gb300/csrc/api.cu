@@ -6,8 +6,10 @@
 #include "common.cuh"
 
 namespace moe {
+int router_parts_ld(int E);
 cudaError_t launch_router(const moe_config_t&, const void*, const float*, const float*,
-                          const float*, float*, int32_t*, float*, uint8_t*, cudaStream_t);
+                          const float*, float*, int32_t*, float*, uint8_t*, const RouterScratch&,
+                          int, int*, cudaStream_t);
 cudaError_t launch_router_select(const moe_config_t&, const float*, const float*, int32_t*,
                                  float*, uint8_t*, cudaStream_t);
 cudaError_t launch_permute_maps(const moe_config_t&, const int32_t*, const float*, int32_t*,
@@ -114,6 +116,16 @@ template <typename T> T* at(void* ws, size_t off) {
 
 moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
+RouterScratch router_scratch(const moe_config_t& c, void* ws) {
+  const Workspace w = workspace_layout(c);
+  RouterScratch rs;
+  rs.w3 = at<__nv_bfloat16>(ws, w.router_w3);
+  rs.parts = at<float>(ws, w.router_parts);
+  rs.ldp = router_parts_ld(c.E);
+  rs.offs = at<int32_t>(ws, w.router_off);
+  return rs;
+}
+
 __global__ void fill_shared_offsets(int32_t* off, int T) {
   off[0] = 0;
   off[1] = T;
@@ -201,14 +213,21 @@ moe_status_t moe_router_topk(const moe_config_t* cfg, const void* x, const float
   if (st != MOE_OK) return st;
   if (cfg->T > 0 && (!x || !w_r || !topk_idx || !topk_prob)) return MOE_ERR_INVALID_ARG;
   if (!al16(x) || !al16(w_r)) return MOE_ERR_INVALID_ARG;
-  const bool need_ws_logits = !logits && cfg->E > 32;
-  if (need_ws_logits && (st = check_ws(cfg, ws, ws_bytes)) != MOE_OK) return st;
+  // bf16 tokens: the tensor-core router keeps its split weight and partial
+  // sums in the workspace; fp32 tokens need it only for E > 32 without logits
+  const bool need_ws = cfg->dtype == MOE_BF16 || (!logits && cfg->E > 32);
+  if (need_ws && (st = check_ws(cfg, ws, ws_bytes)) != MOE_OK) return st;
   if (cfg->flags & MOE_FLAG_VALIDATE_ONLY) return MOE_OK;
   if (cfg->T == 0) return MOE_OK;
-  float* lg = logits ? logits : (need_ws_logits ? at<float>(ws, workspace_layout(*cfg).logits)
-                                                : nullptr);
+  const DeviceInfo* d = device_info();
+  if (!d) return MOE_ERR_CUDA;
+  float* lg = logits;
+  if (!lg && cfg->E > 32 && cfg->dtype != MOE_BF16) lg = at<float>(ws, workspace_layout(*cfg).logits);
+  RouterScratch rs{};
+  if (need_ws) rs = router_scratch(*cfg, ws);
   return cuda_status(launch_router(*cfg, x, w_r, gate_bias, sel_bias, lg, topk_idx, topk_prob,
-                                   routing_map, static_cast<cudaStream_t>(stream)));
+                                   routing_map, rs, d->sms, d->status,
+                                   static_cast<cudaStream_t>(stream)));
 }
 
 moe_status_t moe_router_topk_from_logits(const moe_config_t* cfg, const float* logits,
@@ -346,7 +365,7 @@ moe_status_t moe_layer_fwd(const moe_config_t* cfg, const void* x, const float* 
   float* perm_prob = at<float>(ws, w.perm_prob);
   // Route
   cudaError_t e = launch_router(c, x, w_r, gate_bias, sel_bias, at<float>(ws, w.logits), idx,
-                                prob, nullptr, s);
+                                prob, nullptr, router_scratch(c, ws), d->sms, d->status, s);
   // Dispatch
   if (e == cudaSuccess)
     e = launch_permute_maps(c, idx, prob, at<int32_t>(ws, w.hist), at<int32_t>(ws, w.chunk_base),

@@ -11,85 +11,92 @@
 
 namespace moe {
 
-template <typename T>
-__global__ void __launch_bounds__(256) combine_kernel(const T* __restrict__ y_perm,
+// One 128-thread block per token (the grid covers every token, so the block
+// scheduler balances the load); each thread owns 16-byte column vectors and
+// issues the loads of all K rows before it accumulates them.
+template <typename T, int KMAX>
+__global__ void __launch_bounds__(128) combine_kernel(const T* __restrict__ y_perm,
                                                       const int32_t* __restrict__ dst_row,
                                                       const float* __restrict__ w,
                                                       const T* __restrict__ shared_y, int ntok,
                                                       int K, int h, T* __restrict__ y,
                                                       int* status) {
   constexpr int V = Vec<T>::N;
-  constexpr int kMaxVec = 4;
-  const int lane = threadIdx.x & 31;
-  const int nvec = h / V;
+  __shared__ int64_t s_off[KMAX];
+  __shared__ float s_w[KMAX];
+  const int64_t t = blockIdx.x;
   const int64_t P = (int64_t)ntok * K;
-  for (int64_t t = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5); t < ntok;
-       t += (int64_t)gridDim.x * 8) {
-    int src[16];
-    float wk[16];
-    for (int k = 0; k < K; ++k) {
-      int r = __ldg(dst_row + t * K + k);
-      if (r < 0 || r >= P) {
+  if (threadIdx.x < KMAX) {
+    const int k = threadIdx.x;
+    int64_t off = -1;
+    float wk = 0.f;
+    if (k < K) {
+      const int r = __ldg(dst_row + t * K + k);
+      if (r >= 0 && r < P) {
+        off = (int64_t)r * h;
+        wk = w ? __ldg(w + t * K + k) : 1.f;
+      } else {
         report(status, MOE_ERR_DEVICE_BOUNDS);
-        r = -1;
-      }
-      src[k] = r;
-      wk[k] = w ? __ldg(w + t * K + k) : 1.f;
-    }
-    for (int v0 = 0; v0 < nvec; v0 += 32 * kMaxVec) {
-      float acc[kMaxVec][V];
-#pragma unroll
-      for (int i = 0; i < kMaxVec; ++i)
-#pragma unroll
-        for (int q = 0; q < V; ++q) acc[i][q] = 0.f;
-      for (int k = 0; k < K; ++k) {
-        if (src[k] < 0) continue;
-        const T* row = y_perm + (int64_t)src[k] * h;
-#pragma unroll
-        for (int i = 0; i < kMaxVec; ++i) {
-          const int v = v0 + i * 32 + lane;
-          if (v < nvec) {
-            const Vec<T> u = ld16_stream(row + (int64_t)v * V);
-#pragma unroll
-            for (int q = 0; q < V; ++q) acc[i][q] = fmaf(wk[k], to_f32(u.v[q]), acc[i][q]);
-          }
-        }
-      }
-#pragma unroll
-      for (int i = 0; i < kMaxVec; ++i) {
-        const int v = v0 + i * 32 + lane;
-        if (v >= nvec) continue;
-        if (shared_y) {
-          const Vec<T> u = ld16_stream(shared_y + t * h + (int64_t)v * V);
-#pragma unroll
-          for (int q = 0; q < V; ++q) acc[i][q] += to_f32(u.v[q]);
-        }
-        Vec<T> o;
-#pragma unroll
-        for (int q = 0; q < V; ++q) o.v[q] = from_f32<T>(acc[i][q]);
-        st16(y + t * h + (int64_t)v * V, o);
       }
     }
+    s_off[k] = off;
+    s_w[k] = wk;
+  }
+  __syncthreads();
+  const int nvec = h / V;
+  for (int v = threadIdx.x; v < nvec; v += blockDim.x) {
+    Vec<T> u[KMAX];
+#pragma unroll
+    for (int k = 0; k < KMAX; ++k)
+      if (s_off[k] >= 0) u[k] = ld16_stream(y_perm + s_off[k] + (int64_t)v * V);
+    float acc[V];
+#pragma unroll
+    for (int q = 0; q < V; ++q) acc[q] = 0.f;
+#pragma unroll
+    for (int k = 0; k < KMAX; ++k)
+      if (s_off[k] >= 0) {
+#pragma unroll
+        for (int q = 0; q < V; ++q) acc[q] = fmaf(s_w[k], to_f32(u[k].v[q]), acc[q]);
+      }
+    if (shared_y) {
+      const Vec<T> sv = ld16_stream(shared_y + t * h + (int64_t)v * V);
+#pragma unroll
+      for (int q = 0; q < V; ++q) acc[q] += to_f32(sv.v[q]);
+    }
+    Vec<T> o;
+#pragma unroll
+    for (int q = 0; q < V; ++q) o.v[q] = from_f32<T>(acc[q]);
+    st16(y + t * h + (int64_t)v * V, o);
   }
 }
 
-int scatter_grid(int ntok, int sms);
+template <typename T>
+static cudaError_t combine_t(const moe_config_t& c, const void* y_perm, const int32_t* dst_row,
+                             const float* w, const void* shared_y, void* y, int* status,
+                             cudaStream_t s) {
+  const unsigned grid = (unsigned)c.T;
+  const T* yp = static_cast<const T*>(y_perm);
+  const T* sy = static_cast<const T*>(shared_y);
+  T* out = static_cast<T*>(y);
+  if (c.K <= 2)
+    combine_kernel<T, 2><<<grid, 128, 0, s>>>(yp, dst_row, w, sy, c.T, c.K, c.h, out, status);
+  else if (c.K <= 4)
+    combine_kernel<T, 4><<<grid, 128, 0, s>>>(yp, dst_row, w, sy, c.T, c.K, c.h, out, status);
+  else if (c.K <= 8)
+    combine_kernel<T, 8><<<grid, 128, 0, s>>>(yp, dst_row, w, sy, c.T, c.K, c.h, out, status);
+  else
+    combine_kernel<T, 16><<<grid, 128, 0, s>>>(yp, dst_row, w, sy, c.T, c.K, c.h, out, status);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_combine(const moe_config_t& c, const void* y_perm, const int32_t* dst_row,
                            const float* w, const void* shared_y, void* y, int sms, int* status,
                            cudaStream_t s) {
+  (void)sms;
   if (c.T == 0) return cudaSuccess;
-  const int grid = scatter_grid(c.T, sms);
   if (c.dtype == MOE_BF16)
-    combine_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(
-        static_cast<const __nv_bfloat16*>(y_perm), dst_row, w,
-        static_cast<const __nv_bfloat16*>(shared_y), c.T, c.K, c.h,
-        static_cast<__nv_bfloat16*>(y), status);
-  else
-    combine_kernel<float><<<grid, 256, 0, s>>>(static_cast<const float*>(y_perm), dst_row, w,
-                                               static_cast<const float*>(shared_y), c.T, c.K, c.h,
-                                               static_cast<float*>(y), status);
-  return cudaGetLastError();
+    return combine_t<__nv_bfloat16>(c, y_perm, dst_row, w, shared_y, y, status, s);
+  return combine_t<float>(c, y_perm, dst_row, w, shared_y, y, status, s);
 }
 
 }  // namespace moe

@@ -64,11 +64,20 @@ MOE_D float gelu_f(float z) { return 0.5f * z * (1.0f + erff(z * 0.7071067811865
 MOE_D float sigmoid_f(float z) { return 1.0f / (1.0f + expf(-z)); }
 MOE_D float silu_f(float z) { return z * sigmoid_f(z); }
 
+// Scratch of the tensor-core router (in the workspace): w3 [3E, h] bf16 (the
+// exactly split router weight), parts [T, ldp] fp32 partial logits, offs [2].
+struct RouterScratch {
+  __nv_bfloat16* w3;
+  float* parts;
+  int ldp;
+  int32_t* offs;
+};
+
 // ---- workspace layout ----------------------------------------------------
 // One layout per config, shared by every entry point, so the backward can find
 // what a SAVE_FOR_BWD forward left behind.
 struct Workspace {
-  size_t logits, topk_idx, topk_prob, hist, chunk_base, counts, offsets, dst_row, src_token,
+  size_t router_w3, router_parts, router_off, logits, topk_idx, topk_prob, hist, chunk_base, counts, offsets, dst_row, src_token,
       perm_prob, x_perm, act_save, a, y_perm, shared_off, shared_h, shared_a, shared_y,
       // backward (MOE_FLAG_SAVE_FOR_BWD only)
       dy_perm, dh, dx_perm, dprob_part, dprob_perm, dl_topk, dl_perm, shared_dh, shared_dx,
@@ -91,6 +100,11 @@ inline Workspace workspace_layout(const moe_config_t& c) {
     off = align_up(off + bytes, 256);
     return o;
   };
+  const size_t ldp = (3 * E + 7) / 8 * 8;
+  const bool tc_router = c.dtype == MOE_BF16;
+  w.router_w3 = take(tc_router ? 3 * E * h * 2 : 0);
+  w.router_parts = take(tc_router ? T * ldp * 4 : 0);
+  w.router_off = take(2 * 4);
   w.logits = take(T * E * 4);
   w.topk_idx = take(P * 4);
   w.topk_prob = take(P * 4);

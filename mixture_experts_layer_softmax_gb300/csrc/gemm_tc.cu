@@ -43,7 +43,7 @@ constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int kThreads = 192;
 
-enum TcMode { kTcSwiGLU = 0, kTcGelu = 1, kTcFc2 = 2 };
+enum TcMode { kTcSwiGLU = 0, kTcGelu = 1, kTcFc2 = 2, kTcF32 = 3 };
 
 struct TcParams {
   const int32_t* offsets;        // [E+1]
@@ -51,6 +51,8 @@ struct TcParams {
   const __nv_bfloat16* bias;     // GELU FC1: b1 [E][N]; FC2: b2 [E][N]; or null
   __nv_bfloat16* out;            // [P, N]
   __nv_bfloat16* act_save;       // [P, Nb] or null (FC1 only)
+  float* out_f32;                // kTcF32: [P, ldo] fp32
+  int ldo;
   int E, Kd, N, Nb;              // output columns N; B rows per expert Nb
   int prob_here;                 // apply p in this epilogue
   int* status;
@@ -287,6 +289,16 @@ __global__ void __launch_bounds__(kThreads, 1)
               const int n8 = n + gq * 8;
               if (n8 >= p.N) break;
               float v[8], o[8];
+              if (MODE == kTcF32) {  // plain fp32 result (the router's split-weight GEMM)
+                float* dst = p.out_f32 + row * p.ldo + n8;
+                *reinterpret_cast<float4*>(dst) =
+                    make_float4(__uint_as_float(r[gq * 8]), __uint_as_float(r[gq * 8 + 1]),
+                                __uint_as_float(r[gq * 8 + 2]), __uint_as_float(r[gq * 8 + 3]));
+                *reinterpret_cast<float4*>(dst + 4) =
+                    make_float4(__uint_as_float(r[gq * 8 + 4]), __uint_as_float(r[gq * 8 + 5]),
+                                __uint_as_float(r[gq * 8 + 6]), __uint_as_float(r[gq * 8 + 7]));
+                continue;
+              }
 #pragma unroll
               for (int i = 0; i < 8; ++i) {
                 v[i] = __uint_as_float(r[gq * 8 + i]);
@@ -384,6 +396,7 @@ cudaError_t launch_grouped_gemm_tc(int mode, int P, const void* A, int Kd, const
   p.out = static_cast<__nv_bfloat16*>(out);
   p.act_save = static_cast<__nv_bfloat16*>(act_save);
   p.E = E; p.Kd = Kd; p.N = N; p.Nb = Nb; p.prob_here = prob_here;
+  p.out_f32 = nullptr; p.ldo = 0;
   p.status = status;
   p.wait_limit_ns = 2000000000ull;  // 2 s: far above any real wait
   const int nblk = mode == kTcSwiGLU ? (N + BN / 2 - 1) / (BN / 2) : (N + BN - 1) / BN;
@@ -392,6 +405,7 @@ cudaError_t launch_grouped_gemm_tc(int mode, int P, const void* A, int Kd, const
   switch (mode) {
     case kTcSwiGLU: return launch_mode<kTcSwiGLU>(ma, mb, p, grid, s);
     case kTcGelu: return launch_mode<kTcGelu>(ma, mb, p, grid, s);
+    case kTcF32: return launch_mode<kTcF32>(ma, mb, p, grid, s);
     default: return launch_mode<kTcFc2>(ma, mb, p, grid, s);
   }
 }
@@ -409,6 +423,27 @@ cudaError_t launch_expert_gemm_tc(const moe_config_t& c, int fc, int P, const vo
                                   bias, out, act_save, sms, status, s);
   return launch_grouped_gemm_tc(kTcFc2, P, A, c.F, w, c.h, c.E, c.h, offsets, prob, prob_after,
                                 bias, out, nullptr, sms, status, s);
+}
+
+// Router gating on the tensor cores: parts[t, j] = x[t] . w3[j] for the 3E
+// rows of the exactly split router weight (fp32 result, row stride ldo);
+// offsets = {0, T} (one group).
+cudaError_t launch_router_gemm_tc(int T, const void* x, int h, const void* w3, int E3,
+                                  float* parts, int ldo, const int32_t* offsets, int sms,
+                                  int* status, cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  CUtensorMap ma, mb;
+  if (!encode_2d(&ma, x, (uint64_t)T, (uint64_t)h, BM)) return cudaErrorInvalidValue;
+  if (!encode_2d(&mb, w3, (uint64_t)E3, (uint64_t)h, BN)) return cudaErrorInvalidValue;
+  TcParams p{};
+  p.offsets = offsets;
+  p.E = 1; p.Kd = h; p.N = E3; p.Nb = E3; p.prob_here = 0;
+  p.out_f32 = parts; p.ldo = ldo;
+  p.status = status;
+  p.wait_limit_ns = 2000000000ull;
+  const int64_t tiles = ceil_div(T, BM) * ceil_div(E3, BN);
+  const int grid = (int)(tiles < sms ? tiles : sms);
+  return launch_mode<kTcF32>(ma, mb, p, grid, s);
 }
 
 // ---- test hook: a wait nothing will complete ---------------------------------

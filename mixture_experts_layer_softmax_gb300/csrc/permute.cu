@@ -147,43 +147,48 @@ __global__ void __launch_bounds__(256) chunk_ranks_kernel(
   }
 }
 
-// One warp per token: read the row once, write it to its K destinations.
-template <typename T>
+// One warp per token (the grid covers every token, so the block scheduler
+// balances the load): read the row once, 16-byte vectors, up to 8 vectors per
+// lane in flight, and write it to its K destinations.
+template <typename T, int KMAX>
 __global__ void __launch_bounds__(256) scatter_rows_kernel(const T* __restrict__ x,
                                                            const int32_t* __restrict__ dst_row,
                                                            int ntok, int K, int h,
                                                            T* __restrict__ x_perm, int* status) {
   constexpr int V = Vec<T>::N;
-  constexpr int kMaxVec = 8;  // per lane per pass: 32 lanes x 8 x 16 B = 4 KB
+  constexpr int kMaxVec = 8;
   const int lane = threadIdx.x & 31;
+  const int64_t t = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (t >= ntok) return;
   const int nvec = h / V;
-  for (int64_t t = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5); t < ntok;
-       t += (int64_t)gridDim.x * 8) {
-    int dst[16];
-    const int64_t P = (int64_t)ntok * K;
-    for (int k = 0; k < K; ++k) {
-      dst[k] = __ldg(dst_row + t * K + k);
-      if (dst[k] < 0 || dst[k] >= P) {
-        if (dst[k] >= P) report(status, MOE_ERR_DEVICE_BOUNDS);
-        dst[k] = -1;
-      }
+  const int64_t P = (int64_t)ntok * K;
+  T* dst[KMAX];
+#pragma unroll
+  for (int k = 0; k < KMAX; ++k) {
+    dst[k] = nullptr;
+    if (k < K) {
+      const int r = __ldg(dst_row + t * K + k);
+      if (r >= 0 && r < P)
+        dst[k] = x_perm + (int64_t)r * h;
+      else if (r >= P)
+        report(status, MOE_ERR_DEVICE_BOUNDS);
     }
-    const T* src = x + t * h;
-    for (int v0 = 0; v0 < nvec; v0 += 32 * kMaxVec) {
-      Vec<T> buf[kMaxVec];
+  }
+  const T* src = x + t * h;
+  for (int v0 = 0; v0 < nvec; v0 += 32 * kMaxVec) {
+    Vec<T> buf[kMaxVec];
+#pragma unroll
+    for (int i = 0; i < kMaxVec; ++i) {
+      const int v = v0 + i * 32 + lane;
+      if (v < nvec) buf[i] = ld16_stream(src + (int64_t)v * V);
+    }
+#pragma unroll
+    for (int k = 0; k < KMAX; ++k) {
+      if (!dst[k]) continue;
 #pragma unroll
       for (int i = 0; i < kMaxVec; ++i) {
         const int v = v0 + i * 32 + lane;
-        if (v < nvec) buf[i] = ld16_stream(src + (int64_t)v * V);
-      }
-      for (int k = 0; k < K; ++k) {
-        if (dst[k] < 0) continue;
-        T* d = x_perm + (int64_t)dst[k] * h;
-#pragma unroll
-        for (int i = 0; i < kMaxVec; ++i) {
-          const int v = v0 + i * 32 + lane;
-          if (v < nvec) st16(d + (int64_t)v * V, buf[i]);
-        }
+        if (v < nvec) st16(dst[k] + (int64_t)v * V, buf[i]);
       }
     }
   }
@@ -217,18 +222,29 @@ int scatter_grid(int ntok, int sms) {
   return (int)(need < cap ? (need > 0 ? need : 1) : cap);
 }
 
+template <typename T>
+static cudaError_t scatter_t(const moe_config_t& c, const void* x, const int32_t* dst_row,
+                             void* x_perm, int* status, cudaStream_t s) {
+  const unsigned grid = (unsigned)ceil_div(c.T, 8);
+  const T* xs = static_cast<const T*>(x);
+  T* xp = static_cast<T*>(x_perm);
+  if (c.K <= 2)
+    scatter_rows_kernel<T, 2><<<grid, 256, 0, s>>>(xs, dst_row, c.T, c.K, c.h, xp, status);
+  else if (c.K <= 4)
+    scatter_rows_kernel<T, 4><<<grid, 256, 0, s>>>(xs, dst_row, c.T, c.K, c.h, xp, status);
+  else if (c.K <= 8)
+    scatter_rows_kernel<T, 8><<<grid, 256, 0, s>>>(xs, dst_row, c.T, c.K, c.h, xp, status);
+  else
+    scatter_rows_kernel<T, 16><<<grid, 256, 0, s>>>(xs, dst_row, c.T, c.K, c.h, xp, status);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_scatter_rows(const moe_config_t& c, const void* x, const int32_t* dst_row,
                                 void* x_perm, int sms, int* status, cudaStream_t s) {
+  (void)sms;
   if (c.T == 0) return cudaSuccess;
-  const int grid = scatter_grid(c.T, sms);
-  if (c.dtype == MOE_BF16)
-    scatter_rows_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(
-        static_cast<const __nv_bfloat16*>(x), dst_row, c.T, c.K, c.h,
-        static_cast<__nv_bfloat16*>(x_perm), status);
-  else
-    scatter_rows_kernel<float><<<grid, 256, 0, s>>>(static_cast<const float*>(x), dst_row, c.T,
-                                                    c.K, c.h, static_cast<float*>(x_perm), status);
-  return cudaGetLastError();
+  if (c.dtype == MOE_BF16) return scatter_t<__nv_bfloat16>(c, x, dst_row, x_perm, status, s);
+  return scatter_t<float>(c, x, dst_row, x_perm, status, s);
 }
 
 }  // namespace moe

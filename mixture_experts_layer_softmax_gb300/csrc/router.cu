@@ -8,6 +8,12 @@
 // selected scores by their sum (MOE_FLAG_RENORM).
 //
 // Kernels:
+//  * bf16 tokens (every E): the gating GEMM runs on the tensor cores.  W_r
+//    (fp32) is split exactly into three bf16 parts, w = hi + mid + lo (24
+//    mantissa bits = 3 x 8), stacked as 3E rows; x (bf16, exact) times each part
+//    is exact in fp32 and accumulates in fp32 in TMEM (grouped GEMM kernel,
+//    fp32 output [T, 3E]); router_select adds the three partial sums (+ b_r).
+//  * fp32 tokens:
 //  * router_fused_small: E <= 32.  One block stages W_r chunks in shared
 //    memory; each warp accumulates the gating dot products of a few tokens,
 //    reduces them across the warp (31 shuffles for 32 sums), then selects
@@ -15,6 +21,8 @@
 //  * router_gemm: E > 32.  SIMT fp32 tiled GEMM logits = x W_r^T (+ b_r).
 //  * router_select: warp per token top-k + probabilities on fp32 logits.
 #include <float.h>
+
+#include <algorithm>
 
 #include "common.cuh"
 
@@ -157,8 +165,15 @@ MOE_D void select_and_write(const float (&logit)[J], int t, const RouterArgs& a,
 }
 
 // ---- top-k on given logits: one warp per token --------------------------
+// logits: [T, E] fp32; or, when parts is given, l = (part_lo + part_mid) +
+// part_hi (+ gate_bias), smallest first from parts [T, ldp] (columns e, E + e, 2E + e), and l
+// is written to logits_out when that is given.
 template <int J>
 __global__ void __launch_bounds__(256) router_select_kernel(const float* __restrict__ logits,
+                                                             const float* __restrict__ parts,
+                                                             int ldp,
+                                                             const float* __restrict__ gate_bias,
+                                                             float* __restrict__ logits_out,
                                                              RouterArgs a) {
   const int lane = threadIdx.x & 31;
   const int64_t t = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -167,9 +182,43 @@ __global__ void __launch_bounds__(256) router_select_kernel(const float* __restr
 #pragma unroll
   for (int j = 0; j < J; ++j) {
     const int e = lane + 32 * j;
-    l[j] = e < a.E ? __ldg(logits + t * a.E + e) : 0.f;
+    if (e >= a.E) {
+      l[j] = 0.f;
+      continue;
+    }
+    if (parts) {
+      const float* pr = parts + t * ldp;
+      float v = __fadd_rn(__fadd_rn(__ldg(pr + 2 * a.E + e), __ldg(pr + a.E + e)), __ldg(pr + e));
+      if (gate_bias) v = __fadd_rn(v, __ldg(gate_bias + e));
+      l[j] = v;
+      if (logits_out) logits_out[t * a.E + e] = v;
+    } else {
+      l[j] = __ldg(logits + t * a.E + e);
+    }
   }
   select_and_write<J>(l, (int)t, a, lane);
+}
+
+// w3 rows [0, E) = bf16(w), [E, 2E) = bf16(w - hi), [2E, 3E) = bf16(w - hi - mid):
+// each difference is exact in fp32 and hi + mid + lo == w.
+__global__ void split_router_weight_kernel(const float* __restrict__ w_r, int64_t n,
+                                           __nv_bfloat16* __restrict__ w3) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const float w = __ldg(w_r + i);
+    const __nv_bfloat16 hi = __float2bfloat16_rn(w);
+    const float r1 = w - __bfloat162float(hi);
+    const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
+    const float r2 = r1 - __bfloat162float(mid);
+    w3[i] = hi;
+    w3[n + i] = mid;
+    w3[2 * n + i] = __float2bfloat16_rn(r2);
+  }
+}
+
+__global__ void fill_group_offsets(int32_t* off, int rows) {
+  off[0] = 0;
+  off[1] = rows;
 }
 
 // ---- fused gating + top-k for E <= 32 ------------------------------------
@@ -353,19 +402,25 @@ static RouterArgs make_args(const moe_config_t& c, const float* sel_bias, int32_
   return a;
 }
 
-cudaError_t launch_router_select(const moe_config_t& c, const float* logits, const float* sel_bias,
-                                 int32_t* idx, float* prob, uint8_t* map, cudaStream_t s) {
-  if (c.T == 0) return cudaSuccess;
-  RouterArgs a = make_args(c, sel_bias, idx, prob, map);
+static cudaError_t select_launch(const moe_config_t& c, const float* logits, const float* parts,
+                                 int ldp, const float* gate_bias, float* logits_out,
+                                 RouterArgs a, cudaStream_t s) {
   const int blocks = (int)ceil_div(c.T, 8);
   const int J = (int)ceil_div(c.E, 32);
   switch (J) {
-    case 1: router_select_kernel<1><<<blocks, 256, 0, s>>>(logits, a); break;
-    case 2: router_select_kernel<2><<<blocks, 256, 0, s>>>(logits, a); break;
-    case 3: case 4: router_select_kernel<4><<<blocks, 256, 0, s>>>(logits, a); break;
-    default: router_select_kernel<8><<<blocks, 256, 0, s>>>(logits, a); break;
+    case 1: router_select_kernel<1><<<blocks, 256, 0, s>>>(logits, parts, ldp, gate_bias, logits_out, a); break;
+    case 2: router_select_kernel<2><<<blocks, 256, 0, s>>>(logits, parts, ldp, gate_bias, logits_out, a); break;
+    case 3: case 4: router_select_kernel<4><<<blocks, 256, 0, s>>>(logits, parts, ldp, gate_bias, logits_out, a); break;
+    default: router_select_kernel<8><<<blocks, 256, 0, s>>>(logits, parts, ldp, gate_bias, logits_out, a); break;
   }
   return cudaGetLastError();
+}
+
+cudaError_t launch_router_select(const moe_config_t& c, const float* logits, const float* sel_bias,
+                                 int32_t* idx, float* prob, uint8_t* map, cudaStream_t s) {
+  if (c.T == 0) return cudaSuccess;
+  return select_launch(c, logits, nullptr, 0, nullptr, nullptr,
+                       make_args(c, sel_bias, idx, prob, map), s);
 }
 
 template <typename Tin, int EP>
@@ -380,32 +435,39 @@ static cudaError_t launch_fused(const moe_config_t& c, const Tin* x, const float
   return cudaGetLastError();
 }
 
+cudaError_t launch_router_gemm_tc(int T, const void* x, int h, const void* w3, int E3,
+                                  float* parts, int ldp, const int32_t* offsets, int sms,
+                                  int* status, cudaStream_t s);
+
+int router_parts_ld(int E) { return (int)((3 * (int64_t)E + 7) / 8 * 8); }
+
 cudaError_t launch_router(const moe_config_t& c, const void* x, const float* w_r,
                           const float* gate_bias, const float* sel_bias, float* logits,
-                          int32_t* idx, float* prob, uint8_t* map, cudaStream_t s) {
+                          int32_t* idx, float* prob, uint8_t* map, const RouterScratch& rs,
+                          int sms, int* status, cudaStream_t s) {
   if (c.T == 0) return cudaSuccess;
   RouterArgs a = make_args(c, sel_bias, idx, prob, map);
-  const bool bf = c.dtype == MOE_BF16;
+  if (c.dtype == MOE_BF16) {
+    const int64_t n = (int64_t)c.E * c.h;
+    const int blocks = (int)std::min<int64_t>(ceil_div(n, 256), (int64_t)sms * 8);
+    split_router_weight_kernel<<<blocks, 256, 0, s>>>(w_r, n, rs.w3);
+    fill_group_offsets<<<1, 1, 0, s>>>(rs.offs, c.T);
+    cudaError_t e = cudaGetLastError();
+    if (e == cudaSuccess)
+      e = launch_router_gemm_tc(c.T, x, c.h, rs.w3, 3 * c.E, rs.parts, rs.ldp, rs.offs, sms,
+                                status, s);
+    if (e != cudaSuccess) return e;
+    return select_launch(c, nullptr, rs.parts, rs.ldp, gate_bias, logits, a, s);
+  }
+  const float* xf = static_cast<const float*>(x);
   if (c.E <= 32) {
     const int EP = c.E <= 8 ? 8 : (c.E <= 16 ? 16 : 32);
-    if (bf) {
-      const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
-      if (EP == 8) return launch_fused<__nv_bfloat16, 8>(c, xb, w_r, gate_bias, logits, a, s);
-      if (EP == 16) return launch_fused<__nv_bfloat16, 16>(c, xb, w_r, gate_bias, logits, a, s);
-      return launch_fused<__nv_bfloat16, 32>(c, xb, w_r, gate_bias, logits, a, s);
-    }
-    const float* xf = static_cast<const float*>(x);
     if (EP == 8) return launch_fused<float, 8>(c, xf, w_r, gate_bias, logits, a, s);
     if (EP == 16) return launch_fused<float, 16>(c, xf, w_r, gate_bias, logits, a, s);
     return launch_fused<float, 32>(c, xf, w_r, gate_bias, logits, a, s);
   }
   dim3 grid((unsigned)ceil_div(c.E, 64), (unsigned)ceil_div(c.T, 64));
-  if (bf)
-    router_gemm_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(
-        static_cast<const __nv_bfloat16*>(x), w_r, gate_bias, logits, c.T, c.E, c.h);
-  else
-    router_gemm_kernel<float><<<grid, 256, 0, s>>>(static_cast<const float*>(x), w_r, gate_bias,
-                                                   logits, c.T, c.E, c.h);
+  router_gemm_kernel<float><<<grid, 256, 0, s>>>(xf, w_r, gate_bias, logits, c.T, c.E, c.h);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   return launch_router_select(c, logits, sel_bias, idx, prob, map, s);

@@ -191,6 +191,18 @@ def selection_margin(logits, K, score, sel_bias=None):
     return s[:, K - 1] - s[:, K]
 
 
+def order_margin(logits, K, score, sel_bias=None):
+    """Smallest gap between consecutive keys among the top K+1 (top K when
+    K == E): below it, a different valid fp32 rounding of the logits may list
+    the selected experts in another order (the selected set is decided by
+    selection_margin alone)."""
+    keys = np.asarray(selection_keys(logits, score, sel_bias), np.float64)
+    s = -np.sort(-keys, axis=1)[:, :min(K + 1, keys.shape[1])]
+    if s.shape[1] < 2:
+        return np.full(keys.shape[0], np.inf)
+    return (s[:, :-1] - s[:, 1:]).min(axis=1)
+
+
 # ---------------------------------------------------------------------------
 # Dispatch
 # ---------------------------------------------------------------------------
@@ -431,12 +443,13 @@ def router_grad_logits(logits, idx, probs, dprob, score, renorm=True):
 
 def layer_bwd(x, w_r, w1, w2, dy, K, score, act, *, b1=None, b2=None, sel_bias=None,
               gate_bias=None, renorm=True, force_balance=False, w1_shared=None, w2_shared=None,
-              logits_dtype=np.float32, routing=None):
+              logits_dtype=np.float32, routing=None, weight_grads=True):
     """Gradients of sum(dy * y) for the layer: returns a dict with dx [T,h],
     dw_r [E,h], dw1, dw2 (and db1, db2 when biased), dw1_shared, dw2_shared,
     dprob [T,K] and dlogits [T,E].  Experts with no tokens get zero gradient.
     The selection bias gets none (it only selects); the gate bias gets
-    db_r = sum_t dl_t."""
+    db_r = sum_t dl_t.  weight_grads=False skips the expert weight gradients
+    (dx, dprob and the router gradients only), for large expert counts."""
     x64 = np.asarray(x, np.float64)
     dy = np.asarray(dy, np.float64)
     T, h = x64.shape
@@ -449,8 +462,10 @@ def layer_bwd(x, w_r, w1, w2, dy, K, score, act, *, b1=None, b2=None, sel_bias=N
     counts, offsets, dst_row, src_token, src_slot = dispatch_maps(idx, E)
     dx = np.zeros((T, h), np.float64)
     dprob = np.zeros(idx.shape, np.float64)
-    dw1 = np.zeros((E,) + np.asarray(w1[0]).shape, np.float64)
-    dw2 = np.zeros((E,) + np.asarray(w2[0]).shape, np.float64)
+    dw1 = dw2 = None
+    if weight_grads:
+        dw1 = np.zeros((E,) + np.asarray(w1[0]).shape, np.float64)
+        dw2 = np.zeros((E,) + np.asarray(w2[0]).shape, np.float64)
     db1 = None if b1 is None else np.zeros(np.asarray(b1).shape, np.float64)
     db2 = None if b2 is None else np.zeros(np.asarray(b2).shape, np.float64)
     for e in range(E):
@@ -470,7 +485,8 @@ def layer_bwd(x, w_r, w1, w2, dy, K, score, act, *, b1=None, b2=None, sel_bias=N
         dyr = dy[t_r]
         dprob[t_r, k_r] = (dyr * out).sum(axis=1)
         dout = p * dyr
-        dw2[e] = dout.T @ z
+        if weight_grads:
+            dw2[e] = dout.T @ z
         if db2 is not None:
             db2[e] = dout.sum(axis=0)
         dz = dout @ w2e
@@ -480,7 +496,8 @@ def layer_bwd(x, w_r, w1, w2, dy, K, score, act, *, b1=None, b2=None, sel_bias=N
             dH = np.concatenate([dz * u * silu_grad(g), dz * silu(g)], axis=1)
         else:
             dH = dz * gelu_grad(H)
-        dw1[e] = dH.T @ xr
+        if weight_grads:
+            dw1[e] = dH.T @ xr
         if db1 is not None:
             db1[e] = dH.sum(axis=0)
         np.add.at(dx, t_r, dH @ w1e)
@@ -489,12 +506,12 @@ def layer_bwd(x, w_r, w1, w2, dy, K, score, act, *, b1=None, b2=None, sel_bias=N
         w1s = np.asarray(w1_shared, np.float64)
         w2s = np.asarray(w2_shared, np.float64)
         H, z = expert_hidden(x64, w1s, None, act)
-        dw2_s = dy.T @ z
+        dw2_s = dy.T @ z if weight_grads else None
         dz = dy @ w2s
         F = w1s.shape[0] // 2
         g, u = H[:, :F], H[:, F:]
         dH = np.concatenate([dz * u * silu_grad(g), dz * silu(g)], axis=1)
-        dw1_s = dH.T @ x64
+        dw1_s = dH.T @ x64 if weight_grads else None
         dx += dH @ w1s
     dl = router_grad_logits(logits, idx, probs, dprob, score, renorm)
     dw_r = dl.T @ x64

@@ -42,6 +42,31 @@ def tol_ok(gpu, ref, dtype):
     return err <= bound, err, bound
 
 
+def check_routing(gpu_idx, gpu_prob, ref_idx, ref_prob, logits, K, score, sel_bias=None,
+                  force_balance=False, prob_rtol=1e-5):
+    """Routing parity: the selected set of every token whose K-th/(K+1)-th key
+    gap is >= 1e-5, the listing order where every gap inside the top K+1 is
+    >= 1e-5 (near-equal keys may be listed either way), probabilities per
+    (token, expert).  Returns the mask of tokens whose selection is unique."""
+    T = ref_idx.shape[0]
+    if force_balance:
+        sel_ok = ord_ok = np.ones(T, bool)
+    else:
+        sel_ok = O.selection_margin(logits, K, score, sel_bias) >= 1e-5
+        ord_ok = sel_ok & (O.order_margin(logits, K, score, sel_bias) >= 1e-5)
+    assert sel_ok.mean() > 0.98
+    np.testing.assert_array_equal(gpu_idx[ord_ok], ref_idx[ord_ok])
+    gs, rs = np.argsort(gpu_idx, 1), np.argsort(ref_idx, 1)
+    g_sorted = np.take_along_axis(gpu_idx, gs, 1)
+    r_sorted = np.take_along_axis(ref_idx, rs, 1)
+    np.testing.assert_array_equal(g_sorted[sel_ok], r_sorted[sel_ok])
+    if gpu_prob is not None:
+        np.testing.assert_allclose(np.take_along_axis(gpu_prob, gs, 1)[sel_ok],
+                                   np.take_along_axis(ref_prob, rs, 1)[sel_ok],
+                                   rtol=prob_rtol, atol=1e-6)
+    return sel_ok
+
+
 class Layer:
     """A workload's seeded host inputs and their device copies."""
 

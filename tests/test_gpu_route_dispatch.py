@@ -68,8 +68,9 @@ def test_router_gating_matches_oracle(T, h, E, K, score, dtype, gate_bias):
     logits = torch.empty(T, E, dtype=torch.float32, device="cuda")
     idx = torch.empty(T, K, dtype=torch.int32, device="cuda")
     prob = torch.empty(T, K, dtype=torch.float32, device="cuda")
+    ws = torch.empty(M.moe_workspace_size(cfg), dtype=torch.uint8, device="cuda")
     M.moe_router_topk(cfg, to_dev(x, dtype), to_dev(w_r, "f32"), None if gb is None else to_dev(gb, "f32"),
-                      None, logits, idx, prob)
+                      None, logits, idx, prob, None, ws)
     torch.cuda.synchronize()
     ol = O.gating_logits(x, w_r, gb)
     gl = to_np(logits)

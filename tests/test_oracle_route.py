@@ -159,3 +159,10 @@ def test_routing_map_rows():
     assert (m.sum(1) == 3).all()
     for t in range(50):
         assert set(np.nonzero(m[t])[0]) == set(idx[t])
+
+
+def test_order_margin():
+    l = np.array([[3.0, 1.0, 0.999, 0.25], [5.0, 4.0, 3.0, 2.0]], np.float32)
+    om = O.order_margin(l, 2, O.SCORE_SOFTMAX)
+    assert om[0] == pytest.approx(0.001, rel=1e-3) and om[1] == pytest.approx(1.0)
+    assert np.isinf(O.order_margin(l[:, :1], 1, O.SCORE_SOFTMAX)).all()
