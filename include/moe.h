@@ -75,7 +75,12 @@ enum {
   /* moe_layer_fwd keeps, in the workspace, what moe_layer_bwd needs. */
   MOE_FLAG_SAVE_FOR_BWD = 16u,
   /* Use the SIMT grouped GEMM for bf16 too (slow; a cross-check path). */
-  MOE_FLAG_GEMM_SIMT = 32u
+  MOE_FLAG_GEMM_SIMT = 32u,
+  /* Tensor-core expert GEMM tiling: by default CTA pairs (256-row tiles,
+   * tcgen05 cta_group::2) when experts average >= 512 rows, single CTAs
+   * (128-row tiles) otherwise.  These force one or the other. */
+  MOE_FLAG_GEMM_1CTA = 64u,
+  MOE_FLAG_GEMM_2CTA = 128u
 };
 
 typedef struct {

@@ -89,8 +89,10 @@ moe_status_t check_config(const moe_config_t* c) {
   if ((c->has_bias != 0 && c->has_bias != 1) || (c->n_shared != 0 && c->n_shared != 1))
     return MOE_ERR_INVALID_ARG;
   const uint32_t known = MOE_FLAG_RENORM | MOE_FLAG_FORCE_BALANCE | MOE_FLAG_VALIDATE_ONLY |
-                         MOE_FLAG_SAVE_FOR_BWD | MOE_FLAG_GEMM_SIMT;
+                         MOE_FLAG_SAVE_FOR_BWD | MOE_FLAG_GEMM_SIMT | MOE_FLAG_GEMM_1CTA |
+                         MOE_FLAG_GEMM_2CTA;
   if (c->flags & ~known) return MOE_ERR_INVALID_ARG;
+  if ((c->flags & MOE_FLAG_GEMM_1CTA) && (c->flags & MOE_FLAG_GEMM_2CTA)) return MOE_ERR_INVALID_ARG;
   if (c->E > 256 || c->K > 16) return MOE_ERR_UNSUPPORTED;
   if (c->act == MOE_ACT_SWIGLU && c->has_bias) return MOE_ERR_UNSUPPORTED;
   const int vec = c->dtype == MOE_BF16 ? 8 : 4;

@@ -36,12 +36,21 @@ namespace moe {
 
 namespace {
 
-constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
+constexpr int BM = 128, BK = 64;
 constexpr int A_BYTES = BM * BK * 2;  // 16 KB
-constexpr int B_BYTES = BN * BK * 2;  // 32 KB
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr uint32_t TMEM_COLS = 512;
 constexpr int kThreads = 192;
+
+// Tile width BN (accumulator columns; 256 for the expert GEMMs, narrower for
+// the router's few output columns) fixes the B stage size, the ring depth
+// that fits in ~200 KB of shared memory, and the TMEM double buffer (2 x BN).
+template <int BNT>
+struct Tile {
+  static constexpr int BN = BNT;
+  static constexpr int B_BYTES = BNT * BK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int STAGES = (200 * 1024 / STAGE_BYTES) < 8 ? (200 * 1024 / STAGE_BYTES) : 8;
+  static constexpr uint32_t TMEM_COLS = 2 * BNT;
+};
 
 enum TcMode { kTcSwiGLU = 0, kTcGelu = 1, kTcFc2 = 2, kTcF32 = 3 };
 
@@ -59,6 +68,7 @@ struct TcParams {
   uint64_t wait_limit_ns;
 };
 
+template <int STAGES>
 struct SmemCtl {
   uint64_t full[STAGES], empty[STAGES], tmem_full[2], tmem_empty[2], drain;
   uint32_t tmem_base;
@@ -67,9 +77,14 @@ struct SmemCtl {
   int off[257];
 };
 
-constexpr size_t kSmemBytes = 1024 + (size_t)STAGES * STAGE_BYTES + sizeof(SmemCtl);
+template <int BNT>
+constexpr size_t smem_bytes() {
+  return 1024 + (size_t)Tile<BNT>::STAGES * Tile<BNT>::STAGE_BYTES +
+         sizeof(SmemCtl<Tile<BNT>::STAGES>);
+}
 
-MOE_D void decode_tile(const SmemCtl& c, int E, int nblk, int tile, int& e, int& mb, int& nb) {
+template <typename Ctl>
+MOE_D void decode_tile(const Ctl& c, int E, int nblk, int tile, int& e, int& mb, int& nb) {
   int lo = 0, hi = E - 1;  // largest e with tile_start[e] <= tile
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
@@ -96,16 +111,21 @@ MOE_D void store8(__nv_bfloat16* dst, const float* v) {
   *reinterpret_cast<uint4*>(dst) = u;
 }
 
-template <int MODE>
+template <int MODE, int BNT>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                            const __grid_constant__ CUtensorMap tmB, const TcParams p) {
+  constexpr int BN = Tile<BNT>::BN;
+  constexpr int B_BYTES = Tile<BNT>::B_BYTES;
+  constexpr int STAGE_BYTES = Tile<BNT>::STAGE_BYTES;
+  constexpr int STAGES = Tile<BNT>::STAGES;
+  constexpr uint32_t TMEM_COLS = Tile<BNT>::TMEM_COLS;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* sA = smem;
   uint8_t* sB = smem + STAGES * A_BYTES;
-  SmemCtl& ctl = *reinterpret_cast<SmemCtl*>(smem + STAGES * STAGE_BYTES);
+  SmemCtl<STAGES>& ctl = *reinterpret_cast<SmemCtl<STAGES>*>(smem + STAGES * STAGE_BYTES);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int E = p.E;
@@ -366,14 +386,14 @@ bool encode_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, u
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int MODE>
+template <int MODE, int BNT = 256>
 cudaError_t launch_mode(const CUtensorMap& a, const CUtensorMap& b, const TcParams& p, int grid,
                         cudaStream_t s) {
-  cudaError_t e = cudaFuncSetAttribute(grouped_gemm_tc_kernel<MODE>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)kSmemBytes);
+  constexpr size_t bytes = smem_bytes<BNT>();
+  cudaError_t e = cudaFuncSetAttribute(grouped_gemm_tc_kernel<MODE, BNT>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
   if (e != cudaSuccess) return e;
-  grouped_gemm_tc_kernel<MODE><<<grid, kThreads, kSmemBytes, s>>>(a, b, p);
+  grouped_gemm_tc_kernel<MODE, BNT><<<grid, kThreads, bytes, s>>>(a, b, p);
   return cudaGetLastError();
 }
 
@@ -388,6 +408,7 @@ cudaError_t launch_grouped_gemm_tc(int mode, int P, const void* A, int Kd, const
   if (P == 0) return cudaSuccess;
   CUtensorMap ma, mb;
   if (!encode_2d(&ma, A, (uint64_t)P, (uint64_t)Kd, BM)) return cudaErrorInvalidValue;
+  constexpr int BN = 256;
   const uint32_t brows = mode == kTcSwiGLU ? BN / 2 : BN;
   if (!encode_2d(&mb, B, (uint64_t)E * Nb, (uint64_t)Kd, brows)) return cudaErrorInvalidValue;
   TcParams p;
@@ -410,19 +431,27 @@ cudaError_t launch_grouped_gemm_tc(int mode, int P, const void* A, int Kd, const
   }
 }
 
-// One of the two expert GEMMs (fc = 1: x_perm -> a, fc = 2: a -> y_perm).
+cudaError_t launch_grouped_gemm_tc2(int mode, int P, const void* A, int Kd, const void* B, int Nb,
+                                    int E, int N, const int32_t* offsets, const float* prob,
+                                    int prob_here, const void* bias, void* out, void* act_save,
+                                    int sms, int* status, cudaStream_t s);
+
+// One of the two expert GEMMs (fc = 1: x_perm -> a, fc = 2: a -> y_perm), on
+// CTA pairs when the experts are large enough to fill 256-row tiles.
 cudaError_t launch_expert_gemm_tc(const moe_config_t& c, int fc, int P, const void* A,
                                   const int32_t* offsets, const float* prob, const void* w,
                                   const void* bias, void* act_save, void* out, int sms,
                                   int* status, cudaStream_t s) {
   const bool swiglu = c.act == MOE_ACT_SWIGLU;
   const bool prob_after = c.has_bias != 0;
+  const bool pair = (c.flags & MOE_FLAG_GEMM_2CTA) ||
+                    (!(c.flags & MOE_FLAG_GEMM_1CTA) && (int64_t)P >= 512LL * c.E);
+  auto run = pair ? launch_grouped_gemm_tc2 : launch_grouped_gemm_tc;
   if (fc == 1)
-    return launch_grouped_gemm_tc(swiglu ? kTcSwiGLU : kTcGelu, P, A, c.h, w,
-                                  swiglu ? 2 * c.F : c.F, c.E, c.F, offsets, prob, !prob_after,
-                                  bias, out, act_save, sms, status, s);
-  return launch_grouped_gemm_tc(kTcFc2, P, A, c.F, w, c.h, c.E, c.h, offsets, prob, prob_after,
-                                bias, out, nullptr, sms, status, s);
+    return run(swiglu ? kTcSwiGLU : kTcGelu, P, A, c.h, w, swiglu ? 2 * c.F : c.F, c.E, c.F,
+               offsets, prob, !prob_after, bias, out, act_save, sms, status, s);
+  return run(kTcFc2, P, A, c.F, w, c.h, c.E, c.h, offsets, prob, prob_after, bias, out, nullptr,
+             sms, status, s);
 }
 
 // Router gating on the tensor cores: parts[t, j] = x[t] . w3[j] for the 3E
@@ -433,17 +462,24 @@ cudaError_t launch_router_gemm_tc(int T, const void* x, int h, const void* w3, i
                                   int* status, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
   CUtensorMap ma, mb;
+  // narrowest tile that covers the 3E output columns (at most 256 per tile)
+  const int bn = E3 <= 32 ? 32 : E3 <= 64 ? 64 : E3 <= 128 ? 128 : 256;
   if (!encode_2d(&ma, x, (uint64_t)T, (uint64_t)h, BM)) return cudaErrorInvalidValue;
-  if (!encode_2d(&mb, w3, (uint64_t)E3, (uint64_t)h, BN)) return cudaErrorInvalidValue;
+  if (!encode_2d(&mb, w3, (uint64_t)E3, (uint64_t)h, (uint32_t)bn)) return cudaErrorInvalidValue;
   TcParams p{};
   p.offsets = offsets;
   p.E = 1; p.Kd = h; p.N = E3; p.Nb = E3; p.prob_here = 0;
   p.out_f32 = parts; p.ldo = ldo;
   p.status = status;
   p.wait_limit_ns = 2000000000ull;
-  const int64_t tiles = ceil_div(T, BM) * ceil_div(E3, BN);
+  const int64_t tiles = ceil_div(T, BM) * ceil_div(E3, bn);
   const int grid = (int)(tiles < sms ? tiles : sms);
-  return launch_mode<kTcF32>(ma, mb, p, grid, s);
+  switch (bn) {
+    case 32: return launch_mode<kTcF32, 32>(ma, mb, p, grid, s);
+    case 64: return launch_mode<kTcF32, 64>(ma, mb, p, grid, s);
+    case 128: return launch_mode<kTcF32, 128>(ma, mb, p, grid, s);
+    default: return launch_mode<kTcF32, 256>(ma, mb, p, grid, s);
+  }
 }
 
 // ---- test hook: a wait nothing will complete ---------------------------------

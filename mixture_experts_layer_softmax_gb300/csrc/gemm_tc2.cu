@@ -1,0 +1,451 @@
+// Forward expert GEMMs on CTA pairs (tcgen05.mma.cta_group::2): the same
+// computation as grouped_gemm_tc_kernel (gemm_tc.cu), for experts with many
+// rows.  "Scalable Training of Mixture-of-Experts Models with Megatron Core"
+// (review), §2.1 / §4.3.1: every expert in one grouped GEMM call.
+//
+// A cluster of two CTAs computes a 256 x 256 tile: CTA r holds rows
+// [128r, 128r+128) of A and B rows [128r, 128r+128) of the tile's 256 B rows
+// (for SwiGLU: CTA 0 the 128 gate rows, CTA 1 the matching up rows), the even
+// CTA issues one M256 N256 K16 MMA over both CTAs' shared memory, and each
+// CTA's TMEM receives its own 128 rows x 256 fp32 columns.  Against the 1-CTA
+// kernel this halves the B bytes each SM pulls from L2 and its shared-memory
+// stage (32 KB, so 6 stages fit).
+//
+// Protocol (all waits bounded):
+//   full[s]       even CTA, count 1: its producer posts expect_tx for both CTAs'
+//                 bytes; both CTAs' TMA loads complete on it (.cta_group::2).
+//   empty[s]      both CTAs: the even CTA's MMA commit arrives on both (multicast).
+//   tmem_full[a]  both CTAs: multicast commit after a tile's last MMA.
+//   tmem_empty[a] even CTA, count 8: the 4 epilogue warps of each CTA.
+//   drain         both CTAs: a final multicast commit, so no MMA completion can
+//                 still be in flight towards a CTA that is leaving.
+// TMEM is allocated and freed with cta_group::2 by one warp of each CTA.
+#include "tc_ptx.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int BM = 128;  // rows per CTA; the cluster tile is 256 rows
+constexpr int BMC = 256;
+constexpr int BN = 256;  // accumulator columns
+constexpr int BNL = 128; // B rows each CTA loads
+constexpr int BK = 64;
+constexpr int A_BYTES = BM * BK * 2;   // 16 KB
+constexpr int B_BYTES = BNL * BK * 2;  // 16 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int STAGES = 6;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr int kThreads = 192;
+
+enum Tc2Mode { kSwiGLU = 0, kGelu = 1, kFc2 = 2 };
+
+struct Tc2Params {
+  const int32_t* offsets;
+  const float* prob;
+  const __nv_bfloat16* bias;
+  __nv_bfloat16* out;
+  __nv_bfloat16* act_save;
+  int E, Kd, N, Nb;
+  int prob_here;
+  int* status;
+  uint64_t wait_limit_ns;
+};
+
+struct SmemCtl {
+  uint64_t full[STAGES], empty[STAGES], tmem_full[2], tmem_empty[2], drain;
+  uint32_t tmem_base;
+  int abort;
+  int tile_start[257];
+  int off[257];
+};
+
+constexpr size_t kSmemBytes = 1024 + (size_t)STAGES * STAGE_BYTES + sizeof(SmemCtl);
+
+// ---- cluster / pair PTX ------------------------------------------------------
+MOE_D uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+MOE_D uint32_t mapa(uint32_t addr, uint32_t rank) {
+  uint32_t out;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(out) : "r"(addr), "r"(rank));
+  return out;
+}
+MOE_D void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
+MOE_D void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, int32_t c0, int32_t c1,
+                            uint32_t bar_cluster) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar_cluster)
+      : "memory");
+}
+MOE_D void tmem_alloc_pair(uint32_t holder, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(holder),
+               "r"(ncols)
+               : "memory");
+}
+MOE_D void tmem_relinquish_pair() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+MOE_D void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+MOE_D void mma_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                    uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Arrive (once) on the barrier at this shared offset in every CTA of `mask`
+// when all MMAs issued so far by this thread are complete.
+MOE_D void commit_pair_multicast(uint32_t bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(bar),
+      "h"(mask)
+      : "memory");
+}
+MOE_D void arrive_cluster(uint32_t bar_cluster) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster)
+               : "memory");
+}
+
+MOE_D void decode_tile(const SmemCtl& c, int E, int nblk, int tile, int& e, int& mb, int& nb) {
+  int lo = 0, hi = E - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (c.tile_start[mid] <= tile) lo = mid; else hi = mid - 1;
+  }
+  e = lo;
+  const int local = tile - c.tile_start[e];
+  const int mblk = (c.off[e + 1] - c.off[e] + BMC - 1) / BMC;
+  nb = local / mblk;
+  mb = local - nb * mblk;
+}
+
+MOE_D uint32_t pack_bf16x2(float a, float b) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+MOE_D void store8(__nv_bfloat16* dst, const float* v) {
+  uint4 u;
+  u.x = pack_bf16x2(v[0], v[1]);
+  u.y = pack_bf16x2(v[2], v[3]);
+  u.z = pack_bf16x2(v[4], v[5]);
+  u.w = pack_bf16x2(v[6], v[7]);
+  *reinterpret_cast<uint4*>(dst) = u;
+}
+
+template <int MODE>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    grouped_gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmA,
+                            const __grid_constant__ CUtensorMap tmB, const Tc2Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + STAGES * A_BYTES;
+  SmemCtl& ctl = *reinterpret_cast<SmemCtl*>(smem + STAGES * STAGE_BYTES);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool even = rank == 0;
+  const int cid = blockIdx.x >> 1, ncl = gridDim.x >> 1;
+  const int E = p.E;
+  const int nblk = MODE == kSwiGLU ? (p.N + BNL - 1) / BNL : (p.N + BN - 1) / BN;
+  const int KB = (p.Kd + BK - 1) / BK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      tc::mbar_init(tc::smem_u32(&ctl.full[s]), 1);
+      tc::mbar_init(tc::smem_u32(&ctl.empty[s]), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      tc::mbar_init(tc::smem_u32(&ctl.tmem_full[a]), 1);
+      tc::mbar_init(tc::smem_u32(&ctl.tmem_empty[a]), 8);
+    }
+    tc::mbar_init(tc::smem_u32(&ctl.drain), 1);
+    ctl.abort = 0;
+    tc::fence_barrier_init();
+    tc::prefetch_tensormap(&tmA);
+    tc::prefetch_tensormap(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(tc::smem_u32(&ctl.tmem_base), TMEM_COLS);
+    tmem_relinquish_pair();
+  }
+  for (int e = threadIdx.x; e <= E; e += kThreads) ctl.off[e] = __ldg(p.offsets + e);
+  __syncthreads();
+  if (warp == 2) {
+    int running = 0;
+    for (int e0 = 0; e0 < E; e0 += 32) {
+      const int e = e0 + lane;
+      const int v = e < E ? ((ctl.off[e + 1] - ctl.off[e] + BMC - 1) / BMC) * nblk : 0;
+      int incl = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+      }
+      if (e < E) ctl.tile_start[e] = running + incl - v;
+      running += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) ctl.tile_start[E] = running;
+  }
+  tc::fence_before_sync();
+  __syncthreads();
+  cluster_sync();  // both CTAs' barriers exist before any remote arrive or TMA signal
+  tc::fence_after_sync();
+  const uint32_t tmem_base = ctl.tmem_base;
+  const int total = ctl.tile_start[E];
+  tc::WaitCtl wc{p.status, &ctl.abort, p.wait_limit_ns, 0};
+  tc::WaitCtl wdrain{p.status, nullptr, 1000000000ull, 0};
+
+  if (warp == 0) {
+    // ================= TMA producer (both CTAs) =================
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0, issued = 0, issued_par = 0;
+      bool ok = true;
+      for (int tile = cid; tile < total && ok; tile += ncl) {
+        int e, mb, nb;
+        decode_tile(ctl, E, nblk, tile, e, mb, nb);
+        const int a_row = ctl.off[e] + mb * BMC + (int)rank * BM;
+        const int b_row = MODE == kSwiGLU ? e * p.Nb + (int)rank * p.N + nb * BNL
+                                          : e * p.Nb + nb * BN + (int)rank * BNL;
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!tc::mbar_wait(tc::smem_u32(&ctl.empty[stage]), phase ^ 1, wc)) { ok = false; break; }
+          const uint32_t full_local = tc::smem_u32(&ctl.full[stage]);
+          if (even) tc::mbar_arrive_expect_tx(full_local, 2 * STAGE_BYTES);
+          const uint32_t full_even = mapa(full_local, 0);
+          tma_load_2d_pair(tc::smem_u32(sA + stage * A_BYTES), &tmA, kb * BK, a_row, full_even);
+          tma_load_2d_pair(tc::smem_u32(sB + stage * B_BYTES), &tmB, kb * BK, b_row, full_even);
+          issued |= 1u << stage;
+          issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
+          if (++stage == STAGES) { stage = 0; phase ^= 1; }
+        }
+      }
+      // Every issued stage must have been consumed (the even CTA's MMA commit
+      // arrives on both CTAs' empty barriers only after the bytes landed and
+      // the MMAs reading them finished) before the CTA may leave.
+      for (int s = 0; s < STAGES; ++s)
+        if ((issued >> s) & 1u)
+          tc::mbar_wait(tc::smem_u32(&ctl.empty[s]), (issued_par >> s) & 1u, wdrain);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ================= MMA issuer (even CTA) =================
+    if (even && lane == 0) {
+      constexpr uint32_t idesc = tc::idesc_bf16_f32(BMC, BN);
+      int stage = 0, acc = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      bool ok = true;
+      for (int tile = cid; tile < total && ok; tile += ncl) {
+        if (!tc::mbar_wait(tc::smem_u32(&ctl.tmem_empty[acc]), acc_phase ^ 1, wc)) break;
+        tc::fence_after_sync();
+        const uint32_t d = tmem_base + (uint32_t)(acc * BN);
+        for (int kb = 0; kb < KB; ++kb) {
+          if (!tc::mbar_wait(tc::smem_u32(&ctl.full[stage]), phase, wc)) { ok = false; break; }
+          tc::fence_after_sync();
+          const uint32_t a0 = tc::smem_u32(sA + stage * A_BYTES);
+          const uint32_t b0 = tc::smem_u32(sB + stage * B_BYTES);
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k)
+            mma_pair(d, tc::desc_kmajor_sw128(a0 + k * 32), tc::desc_kmajor_sw128(b0 + k * 32), idesc,
+                     (kb | k) != 0);
+          commit_pair_multicast(tc::smem_u32(&ctl.empty[stage]), 0x3);
+          if (++stage == STAGES) { stage = 0; phase ^= 1; }
+        }
+        if (!ok) break;
+        commit_pair_multicast(tc::smem_u32(&ctl.tmem_full[acc]), 0x3);
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1;
+      }
+      commit_pair_multicast(tc::smem_u32(&ctl.drain), 0x3);
+    }
+    __syncwarp();
+  } else {
+    // ================= epilogue (warps 2..5, both CTAs) =================
+    const int q = warp & 3;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    const uint32_t tmem_empty_even0 = mapa(tc::smem_u32(&ctl.tmem_empty[0]), 0);
+    const uint32_t tmem_empty_even1 = mapa(tc::smem_u32(&ctl.tmem_empty[1]), 0);
+    for (int tile = cid; tile < total; tile += ncl) {
+      int e, mb, nb;
+      decode_tile(ctl, E, nblk, tile, e, mb, nb);
+      if (!tc::mbar_wait(tc::smem_u32(&ctl.tmem_full[acc]), acc_phase, wc)) break;
+      tc::fence_after_sync();
+      const int m_e = ctl.off[e + 1] - ctl.off[e];
+      const int local_row = mb * BMC + (int)rank * BM + q * 32 + lane;
+      const bool valid = local_row < m_e;
+      const int64_t row = (int64_t)ctl.off[e] + local_row;
+      const float pr = (p.prob && p.prob_here && valid) ? __ldg(p.prob + row) : 1.f;
+      const uint32_t tbase = tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(q * 32) << 16);
+      if (MODE == kSwiGLU) {
+#pragma unroll 1
+        for (int c = 0; c < BNL / 32; ++c) {
+          uint32_t g[32], u[32];
+          tc::tmem_ld_32x32b_x32(tbase + c * 32, g);
+          tc::tmem_ld_32x32b_x32(tbase + BNL + c * 32, u);
+          const int n = nb * BNL + c * 32;
+          if (valid) {
+#pragma unroll
+            for (int gq = 0; gq < 4; ++gq) {
+              if (n + gq * 8 >= p.N) break;
+              float o[8], gv[8], uv[8];
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                gv[i] = __uint_as_float(g[gq * 8 + i]);
+                uv[i] = __uint_as_float(u[gq * 8 + i]);
+                o[i] = pr * (silu_f(gv[i]) * uv[i]);
+              }
+              store8(p.out + row * p.N + n + gq * 8, o);
+              if (p.act_save) {
+                store8(p.act_save + row * p.Nb + n + gq * 8, gv);
+                store8(p.act_save + row * p.Nb + p.N + n + gq * 8, uv);
+              }
+            }
+          }
+        }
+      } else {
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t r[32];
+          tc::tmem_ld_32x32b_x32(tbase + c * 32, r);
+          const int n = nb * BN + c * 32;
+          if (valid) {
+#pragma unroll
+            for (int gq = 0; gq < 4; ++gq) {
+              const int n8 = n + gq * 8;
+              if (n8 >= p.N) break;
+              float v[8], o[8];
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                v[i] = __uint_as_float(r[gq * 8 + i]);
+                if (p.bias) v[i] += __bfloat162float(p.bias[(int64_t)e * p.N + n8 + i]);
+              }
+              if (MODE == kGelu) {
+                if (p.act_save) store8(p.act_save + row * p.Nb + n8, v);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) o[i] = pr * gelu_f(v[i]);
+              } else {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) o[i] = pr * v[i];
+              }
+              store8(p.out + row * p.N + n8, o);
+            }
+          }
+        }
+      }
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) arrive_cluster(acc == 0 ? tmem_empty_even0 : tmem_empty_even1);
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1;
+    }
+  }
+  // the even CTA's final multicast commit lands after every MMA and every
+  // earlier commit: once it is seen, nothing is in flight towards this CTA
+  if (threadIdx.x == 0) tc::mbar_wait(tc::smem_u32(&ctl.drain), 0, wdrain);
+  tc::fence_before_sync();
+  __syncthreads();
+  cluster_sync();
+  if (warp == 1) {
+    tc::fence_after_sync();
+    tmem_dealloc_pair(tmem_base, TMEM_COLS);
+  }
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      return reinterpret_cast<EncodeTiledFn>(ptr);
+    return (EncodeTiledFn) nullptr;
+  }();
+  return fn;
+}
+
+bool encode(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * 2};
+  const cuuint32_t box[2] = {(cuuint32_t)BK, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int MODE>
+cudaError_t launch_mode2(const CUtensorMap& a, const CUtensorMap& b, const Tc2Params& p,
+                         int64_t tiles, int sms, cudaStream_t s) {
+  cudaError_t e = cudaFuncSetAttribute(grouped_gemm_tc2_kernel<MODE>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+  if (e != cudaSuccess) return e;
+  // as many pairs as can be resident at once (a pair needs two SMs of one
+  // cluster-capable group), capped by the tile count
+  int max_clusters = 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * (unsigned)((sms + 1) / 2));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = s;
+  if (cudaOccupancyMaxActiveClusters(&max_clusters, grouped_gemm_tc2_kernel<MODE>, &cfg) !=
+          cudaSuccess ||
+      max_clusters < 1)
+    max_clusters = sms / 2;
+  const int64_t pairs = tiles < max_clusters ? tiles : max_clusters;
+  grouped_gemm_tc2_kernel<MODE><<<(unsigned)(2 * pairs), kThreads, kSmemBytes, s>>>(a, b, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+// Pair-tile version of launch_grouped_gemm_tc (same modes: 0 SwiGLU FC1,
+// 1 GELU FC1, 2 FC2; same arguments).
+cudaError_t launch_grouped_gemm_tc2(int mode, int P, const void* A, int Kd, const void* B, int Nb,
+                                    int E, int N, const int32_t* offsets, const float* prob,
+                                    int prob_here, const void* bias, void* out, void* act_save,
+                                    int sms, int* status, cudaStream_t s) {
+  if (P == 0) return cudaSuccess;
+  CUtensorMap ma, mb;
+  if (!encode(&ma, A, (uint64_t)P, (uint64_t)Kd, BM)) return cudaErrorInvalidValue;
+  if (!encode(&mb, B, (uint64_t)E * Nb, (uint64_t)Kd, BNL)) return cudaErrorInvalidValue;
+  Tc2Params p;
+  p.offsets = offsets; p.prob = prob;
+  p.bias = static_cast<const __nv_bfloat16*>(bias);
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.act_save = static_cast<__nv_bfloat16*>(act_save);
+  p.E = E; p.Kd = Kd; p.N = N; p.Nb = Nb; p.prob_here = prob_here;
+  p.status = status;
+  p.wait_limit_ns = 2000000000ull;
+  const int nblk = mode == kSwiGLU ? (N + BNL - 1) / BNL : (N + BN - 1) / BN;
+  const int64_t tiles = (ceil_div(P, BMC) + E) * (int64_t)nblk;
+  switch (mode) {
+    case kSwiGLU: return launch_mode2<kSwiGLU>(ma, mb, p, tiles, sms, s);
+    case kGelu: return launch_mode2<kGelu>(ma, mb, p, tiles, sms, s);
+    default: return launch_mode2<kFc2>(ma, mb, p, tiles, sms, s);
+  }
+}
+
+}  // namespace moe

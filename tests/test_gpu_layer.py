@@ -34,23 +34,28 @@ def _grouped_case(P_tokens, h, E, K, F, act, bias, dtype, skew=False, seed=0):
 
 
 GROUPED = [
-    # tokens, h, E, K, F, act, bias, dtype, skew, simt
-    (600, 512, 8, 2, 768, O.ACT_SWIGLU, False, "bf16", False, False),
-    (300, 200, 5, 2, 136, O.ACT_SWIGLU, False, "bf16", True, False),
-    (700, 256, 1, 1, 384, O.ACT_SWIGLU, False, "bf16", False, False),
-    (150, 128, 16, 4, 264, O.ACT_GELU, False, "bf16", True, False),
-    (150, 128, 16, 4, 264, O.ACT_GELU, True, "bf16", False, False),
-    (600, 512, 8, 2, 768, O.ACT_SWIGLU, False, "bf16", False, True),
-    (256, 128, 8, 2, 512, O.ACT_GELU, True, "f32", False, False),
-    (100, 96, 3, 2, 52, O.ACT_SWIGLU, False, "f32", True, False),
+    # tokens, h, E, K, F, act, bias, dtype, skew, path
+    (600, 512, 8, 2, 768, O.ACT_SWIGLU, False, "bf16", False, "1cta"),
+    (600, 512, 8, 2, 768, O.ACT_SWIGLU, False, "bf16", False, "2cta"),
+    (300, 200, 5, 2, 136, O.ACT_SWIGLU, False, "bf16", True, "1cta"),
+    (300, 200, 5, 2, 136, O.ACT_SWIGLU, False, "bf16", True, "2cta"),
+    (700, 256, 1, 1, 384, O.ACT_SWIGLU, False, "bf16", False, "2cta"),
+    (2100, 256, 4, 2, 384, O.ACT_SWIGLU, False, "bf16", False, "default"),
+    (150, 128, 16, 4, 264, O.ACT_GELU, False, "bf16", True, "1cta"),
+    (150, 128, 16, 4, 264, O.ACT_GELU, True, "bf16", False, "1cta"),
+    (150, 128, 16, 4, 264, O.ACT_GELU, True, "bf16", False, "2cta"),
+    (600, 512, 8, 2, 768, O.ACT_SWIGLU, False, "bf16", False, "simt"),
+    (256, 128, 8, 2, 512, O.ACT_GELU, True, "f32", False, "default"),
+    (100, 96, 3, 2, 52, O.ACT_SWIGLU, False, "f32", True, "default"),
 ]
 
 
-@pytest.mark.parametrize("T,h,E,K,F,act,bias,dtype,skew,simt", GROUPED)
-def test_grouped_mlp_matches_oracle(T, h, E, K, F, act, bias, dtype, skew, simt):
+@pytest.mark.parametrize("T,h,E,K,F,act,bias,dtype,skew,path", GROUPED)
+def test_grouped_mlp_matches_oracle(T, h, E, K, F, act, bias, dtype, skew, path):
     M = lib()
     c = _grouped_case(T, h, E, K, F, act, bias, dtype, skew, seed=T + F)
-    flags = M.MOE_FLAG_RENORM | (M.MOE_FLAG_GEMM_SIMT if simt else 0)
+    flags = M.MOE_FLAG_RENORM | {"simt": M.MOE_FLAG_GEMM_SIMT, "1cta": M.MOE_FLAG_GEMM_1CTA,
+                                 "2cta": M.MOE_FLAG_GEMM_2CTA, "default": 0}[path]
     cfg = M.make_config(T, h, E, K, F, M.MOE_BF16 if dtype == "bf16" else M.MOE_F32,
                         M.MOE_SCORE_SOFTMAX, act, int(bias), 0, flags)
     ws = torch.empty(M.moe_workspace_size(cfg), dtype=torch.uint8, device="cuda")
@@ -118,6 +123,18 @@ def test_layer_forward_is_deterministic(w):
     assert torch.equal(y1.view(torch.int16) if y1.dtype == torch.bfloat16 else y1,
                        y2.view(torch.int16) if y2.dtype == torch.bfloat16 else y2)
     assert torch.equal(i1, i2) and torch.equal(p1, p2)
+
+
+@pytest.mark.parametrize("w", small_workloads()[1:6], ids=lambda w: w.name)
+def test_layer_forward_on_cta_pairs_matches_oracle(w):
+    M = lib()
+    L = Layer(w)
+    y, idx, prob, _ = L.run_fwd(M, flags_extra=M.MOE_FLAG_GEMM_2CTA)
+    ref = L.oracle_fwd()
+    ok_tok = check_routing(to_np(idx), to_np(prob), ref["idx"], ref["probs"], ref["logits"], w.K,
+                           w.score, L.h.get("sel_bias"), w.force_balance)
+    good, err, bound = tol_ok(to_np(y)[ok_tok], ref["y"][ok_tok], w.dtype)
+    assert good, (err, bound)
 
 
 def test_layer_simt_and_tensor_core_paths_agree():
