@@ -100,73 +100,105 @@ __global__ void __launch_bounds__(256) router_wgrad_kernel(
   }
 }
 
-// Warp per token: dx[t] = sum_k dx_perm[dst_row[t,k]] (+ dx_shared[t])
-//                        + sum_k dl_topk[t,k] * W_r[idx[t,k]]   (when dl_topk given)
+// One 128-thread block per token:
+//   dx[t] = sum_k dx_perm[dst_row[t,k]] (+ dx_shared[t]) + sum_k dl_topk[t,k] * W_r[idx[t,k]]
+// each thread owns 8-column vectors and issues the K row loads before adding;
 // fp32 accumulation in a fixed order, one rounding to the output type.
-template <typename T>
-__global__ void __launch_bounds__(256) bwd_combine_kernel(
+template <typename T, int KMAX>
+__global__ void __launch_bounds__(128) bwd_combine_kernel(
     const T* __restrict__ dx_perm, const int32_t* __restrict__ dst_row,
     const T* __restrict__ dx_shared, const float* __restrict__ dl_topk,
     const int32_t* __restrict__ idx, const float* __restrict__ w_r, int ntok, int K, int E, int h,
     T* __restrict__ dx, float* __restrict__ dx_f32, int* status) {
-  constexpr int V = 8;  // columns per lane per pass (one 16-B bf16 vector)
-  const int lane = threadIdx.x & 31;
+  constexpr int V = 8;
+  __shared__ int64_t s_src[KMAX];
+  __shared__ int64_t s_w[KMAX];
+  __shared__ float s_dl[KMAX];
+  const int64_t t = blockIdx.x;
   const int64_t P = (int64_t)ntok * K;
-  for (int64_t t = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5); t < ntok;
-       t += (int64_t)gridDim.x * 8) {
-    int src[16], ex[16];
-    float dl[16];
-    for (int k = 0; k < K; ++k) {
-      int r = dx_perm ? __ldg(dst_row + t * K + k) : 0;
-      if (dx_perm && (r < 0 || r >= P)) {
-        report(status, MOE_ERR_DEVICE_BOUNDS);
-        r = -1;
-      }
-      src[k] = r;
-      int e = dl_topk ? __ldg(idx + t * K + k) : 0;
-      if (e < 0 || e >= E) {
-        report(status, MOE_ERR_DEVICE_BOUNDS);
-        e = -1;
-      }
-      ex[k] = e;
-      dl[k] = dl_topk ? __ldg(dl_topk + t * K + k) : 0.f;
-    }
-    for (int c = lane * V; c < h; c += 32 * V) {
-      float acc[V] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  if (threadIdx.x < KMAX) {
+    const int k = threadIdx.x;
+    int64_t src = -1, wo = -1;
+    float d = 0.f;
+    if (k < K) {
       if (dx_perm) {
-        for (int k = 0; k < K; ++k) {
-          if (src[k] < 0) continue;
-          const T* row = dx_perm + (int64_t)src[k] * h + c;
-#pragma unroll
-          for (int i = 0; i < V; ++i) acc[i] += to_f32(row[i]);
-        }
-      }
-      if (dx_shared) {
-        const T* row = dx_shared + t * h + c;
-#pragma unroll
-        for (int i = 0; i < V; ++i) acc[i] += to_f32(row[i]);
+        const int r = __ldg(dst_row + t * K + k);
+        if (r >= 0 && r < P) src = (int64_t)r * h; else report(status, MOE_ERR_DEVICE_BOUNDS);
       }
       if (dl_topk) {
-        for (int k = 0; k < K; ++k) {
-          if (ex[k] < 0) continue;
-          const float* wr = w_r + (int64_t)ex[k] * h + c;
-#pragma unroll
-          for (int i = 0; i < V; ++i) acc[i] = fmaf(dl[k], __ldg(wr + i), acc[i]);
+        const int e = __ldg(idx + t * K + k);
+        if (e >= 0 && e < E) {
+          wo = (int64_t)e * h;
+          d = __ldg(dl_topk + t * K + k);
+        } else {
+          report(status, MOE_ERR_DEVICE_BOUNDS);
         }
       }
-      if (dx) {
+    }
+    s_src[k] = src;
+    s_w[k] = wo;
+    s_dl[k] = d;
+  }
+  __syncthreads();
+  for (int c = threadIdx.x * V; c < h; c += blockDim.x * V) {
+    float acc[V];
+#pragma unroll
+    for (int i = 0; i < V; ++i) acc[i] = 0.f;
+    if (dx_perm) {
+      Vec<T> u[KMAX];
+#pragma unroll
+      for (int k = 0; k < KMAX; ++k)
+        if (s_src[k] >= 0) {
+          if constexpr (sizeof(T) == 2) {
+            u[k] = ld16_stream(dx_perm + s_src[k] + c);
+          }
+        }
+#pragma unroll
+      for (int k = 0; k < KMAX; ++k)
+        if (s_src[k] >= 0) {
+          if constexpr (sizeof(T) == 2) {
+#pragma unroll
+            for (int i = 0; i < V; ++i) acc[i] += to_f32(u[k].v[i]);
+          } else {
+#pragma unroll
+            for (int i = 0; i < V; ++i) acc[i] += to_f32(dx_perm[s_src[k] + c + i]);
+          }
+        }
+    }
+    if (dx_shared) {
+#pragma unroll
+      for (int i = 0; i < V; ++i) acc[i] += to_f32(dx_shared[t * h + c + i]);
+    }
+    if (dl_topk) {
+#pragma unroll
+      for (int k = 0; k < KMAX; ++k)
+        if (s_w[k] >= 0) {
+          const float4 a = __ldg(reinterpret_cast<const float4*>(w_r + s_w[k] + c));
+          const float4 b = __ldg(reinterpret_cast<const float4*>(w_r + s_w[k] + c + 4));
+          const float d = s_dl[k];
+          acc[0] = fmaf(d, a.x, acc[0]); acc[1] = fmaf(d, a.y, acc[1]);
+          acc[2] = fmaf(d, a.z, acc[2]); acc[3] = fmaf(d, a.w, acc[3]);
+          acc[4] = fmaf(d, b.x, acc[4]); acc[5] = fmaf(d, b.y, acc[5]);
+          acc[6] = fmaf(d, b.z, acc[6]); acc[7] = fmaf(d, b.w, acc[7]);
+        }
+    }
+    if (dx) {
+      if constexpr (sizeof(T) == 2) {
+        Vec<T> o;
+#pragma unroll
+        for (int i = 0; i < V; ++i) o.v[i] = from_f32<T>(acc[i]);
+        st16(dx + t * h + c, o);
+      } else {
 #pragma unroll
         for (int i = 0; i < V; ++i) dx[t * h + c + i] = from_f32<T>(acc[i]);
       }
-      if (dx_f32) {
-#pragma unroll
-        for (int i = 0; i < V; ++i) dx_f32[t * h + c + i] = acc[i];
-      }
+    }
+    if (dx_f32) {
+      *reinterpret_cast<float4*>(dx_f32 + t * h + c) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+      *reinterpret_cast<float4*>(dx_f32 + t * h + c + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
     }
   }
 }
-
-int scatter_grid(int ntok, int sms);
 
 cudaError_t launch_dprob_reduce(const float* part, int rows, int nt, float* dprob_perm,
                                 cudaStream_t s) {
@@ -198,22 +230,37 @@ cudaError_t launch_router_wgrad(const moe_config_t& c, const void* x, const int3
   return cudaGetLastError();
 }
 
+template <typename T>
+static cudaError_t bwd_combine_t(const moe_config_t& c, const void* dx_perm,
+                                 const int32_t* dst_row, const void* dx_shared,
+                                 const float* dl_topk, const int32_t* idx, const float* w_r,
+                                 void* dx, float* dx_f32, int* status, cudaStream_t s) {
+  const unsigned grid = (unsigned)c.T;
+  const T* dp = static_cast<const T*>(dx_perm);
+  const T* ds = static_cast<const T*>(dx_shared);
+  T* o = static_cast<T*>(dx);
+#define MOE_BWD_COMBINE(KM)                                                                    \
+  bwd_combine_kernel<T, KM><<<grid, 128, 0, s>>>(dp, dst_row, ds, dl_topk, idx, w_r, c.T, c.K, \
+                                                 c.E, c.h, o, dx_f32, status)
+  if (c.K <= 2) MOE_BWD_COMBINE(2);
+  else if (c.K <= 4) MOE_BWD_COMBINE(4);
+  else if (c.K <= 8) MOE_BWD_COMBINE(8);
+  else MOE_BWD_COMBINE(16);
+#undef MOE_BWD_COMBINE
+  return cudaGetLastError();
+}
+
 cudaError_t launch_bwd_combine(const moe_config_t& c, const void* dx_perm, const int32_t* dst_row,
                                const void* dx_shared, const float* dl_topk, const int32_t* idx,
                                const float* w_r, void* dx, float* dx_f32, int sms, int* status,
                                cudaStream_t s) {
+  (void)sms;
   if (c.T == 0) return cudaSuccess;
-  const int grid = scatter_grid(c.T, sms);
   if (c.dtype == MOE_BF16)
-    bwd_combine_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(
-        static_cast<const __nv_bfloat16*>(dx_perm), dst_row,
-        static_cast<const __nv_bfloat16*>(dx_shared), dl_topk, idx, w_r, c.T, c.K, c.E, c.h,
-        static_cast<__nv_bfloat16*>(dx), dx_f32, status);
-  else
-    bwd_combine_kernel<float><<<grid, 256, 0, s>>>(
-        static_cast<const float*>(dx_perm), dst_row, static_cast<const float*>(dx_shared), dl_topk,
-        idx, w_r, c.T, c.K, c.E, c.h, static_cast<float*>(dx), dx_f32, status);
-  return cudaGetLastError();
+    return bwd_combine_t<__nv_bfloat16>(c, dx_perm, dst_row, dx_shared, dl_topk, idx, w_r, dx,
+                                        dx_f32, status, s);
+  return bwd_combine_t<float>(c, dx_perm, dst_row, dx_shared, dl_topk, idx, w_r, dx, dx_f32,
+                              status, s);
 }
 
 }  // namespace moe

@@ -30,7 +30,7 @@
 namespace moe {
 namespace {
 
-constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
+constexpr int BM = 128, BN = 256, BK = 64, MAX_STAGES = 4;
 constexpr int A_BYTES = BM * BK * 2;  // 16 KB
 constexpr int B_BYTES = BN * BK * 2;  // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
@@ -52,14 +52,34 @@ struct BwdParams {
 };
 
 struct SmemCtl {
-  uint64_t full[STAGES], empty[STAGES], tmem_full[2], tmem_empty[2], drain;
+  uint64_t full[MAX_STAGES], empty[MAX_STAGES], tmem_full[2], tmem_empty[2], drain;
   uint32_t tmem_base;
   int abort;
   int tile_start[257];
   int off[257];
 };
 
-constexpr size_t kSmemBytes = 1024 + (size_t)STAGES * STAGE_BYTES + sizeof(SmemCtl);
+// The weight-gradient kernel writes its 128 x 256 output tile through shared
+// memory and TMA stores (64 KB of staging), so it keeps 3 stages instead of 4:
+// its reduction is only one expert's rows (a few 64-row blocks) anyway.
+constexpr int STAGING_BYTES = BM * BN * 2;
+template <int KIND> constexpr int stages_of() { return KIND == 2 ? 3 : 4; }
+template <int KIND>
+constexpr size_t smem_bytes() {
+  return 1024 + (size_t)stages_of<KIND>() * STAGE_BYTES + (KIND == 2 ? STAGING_BYTES : 0) +
+         sizeof(SmemCtl);
+}
+
+MOE_D void tma_store_3d(const CUtensorMap* map, int32_t c0, int32_t c1, int32_t c2, uint32_t src) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(c0), "r"(c1), "r"(c2), "r"(src)
+      : "memory");
+}
+MOE_D void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+MOE_D void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+MOE_D void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 MOE_D void tma_load_3d(uint32_t dst, const CUtensorMap* map, int32_t c0, int32_t c1, int32_t c2,
                        uint32_t bar) {
@@ -118,13 +138,16 @@ struct Tiles {
 template <int KIND>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_tc_bwd_kernel(const __grid_constant__ CUtensorMap tmA,
-                               const __grid_constant__ CUtensorMap tmB, const BwdParams p) {
+                               const __grid_constant__ CUtensorMap tmB,
+                               const __grid_constant__ CUtensorMap tmC, const BwdParams p) {
+  constexpr int STAGES = stages_of<KIND>();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* sA = smem;
   uint8_t* sB = smem + STAGES * A_BYTES;
-  SmemCtl& ctl = *reinterpret_cast<SmemCtl*>(smem + STAGES * STAGE_BYTES);
+  uint8_t* sC = smem + STAGES * STAGE_BYTES;  // wgrad output staging (64 KB)
+  SmemCtl& ctl = *reinterpret_cast<SmemCtl*>(sC + (KIND == kWgrad ? STAGING_BYTES : 0));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int E = p.E;
   const int nt = (p.N + BN - 1) / BN;
@@ -146,6 +169,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::fence_proxy_async_smem();
     tc::prefetch_tensormap(&tmA);
     tc::prefetch_tensormap(&tmB);
+    if (KIND == kWgrad) tc::prefetch_tensormap(&tmC);
   }
   if (warp == 1) {
     tc::tmem_alloc(tc::smem_u32(&ctl.tmem_base), TMEM_COLS);
@@ -305,23 +329,41 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int m_e = ctl.off[e + 1] - ctl.off[e];
       const uint32_t tbase = tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(q * 32) << 16);
       if (KIND == kWgrad) {
-        const int m = mb * BM + q * 32 + lane;
-        __nv_bfloat16* orow = p.out + ((int64_t)e * p.M + m) * p.N;
+        // this warp's 32 rows x 256 columns go to 4 swizzled {64 col, 32 row}
+        // boxes in shared memory (row `lane`, 16-B chunk c at c ^ (lane & 7)),
+        // then one lane stores them with TMA (rows past M are clipped).
+        uint8_t* box0 = sC + q * 4 * 4096;
+        if (lane == 0) bulk_wait_read0();  // the previous tile's stores have read the staging
+        __syncwarp();
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
           uint32_t r[32];
-          if (m_e > 0) tc::tmem_ld_32x32b_x32(tbase + c * 32, r);
-          const int n = nb * BN + c * 32;
-          if (m < p.M) {
+          if (m_e > 0) {
+            tc::tmem_ld_32x32b_x32(tbase + c * 32, r);
+          } else {
 #pragma unroll
-            for (int g = 0; g < 4; ++g) {
-              if (n + g * 8 >= p.N) break;
-              float v[8];
-#pragma unroll
-              for (int i = 0; i < 8; ++i) v[i] = m_e > 0 ? __uint_as_float(r[g * 8 + i]) : 0.f;
-              store8(orow + n + g * 8, v);
-            }
+            for (int i = 0; i < 32; ++i) r[i] = 0u;
           }
+          uint8_t* row = box0 + (c >> 1) * 4096 + lane * 128;
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            const int chunk = (c & 1) * 4 + g;
+            uint4 u;
+            u.x = pack2(__uint_as_float(r[g * 8 + 0]), __uint_as_float(r[g * 8 + 1]));
+            u.y = pack2(__uint_as_float(r[g * 8 + 2]), __uint_as_float(r[g * 8 + 3]));
+            u.z = pack2(__uint_as_float(r[g * 8 + 4]), __uint_as_float(r[g * 8 + 5]));
+            u.w = pack2(__uint_as_float(r[g * 8 + 6]), __uint_as_float(r[g * 8 + 7]));
+            *reinterpret_cast<uint4*>(row + ((chunk ^ (lane & 7)) << 4)) = u;
+          }
+        }
+        tc::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            tma_store_3d(&tmC, nb * BN + j * 64, mb * BM + q * 32, e,
+                         tc::smem_u32(box0 + j * 4096));
+          bulk_commit();
         }
       } else {
         const int local_row = mb * BM + q * 32 + lane;
@@ -370,6 +412,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1;
     }
+    if (KIND == kWgrad && lane == 0) bulk_wait0();  // every TMA store has completed
   }
   tc::fence_before_sync();
   __syncthreads();
@@ -413,12 +456,13 @@ bool encode_map(CUtensorMap* m, const void* base, uint64_t depth, uint64_t rows,
 }
 
 template <int KIND>
-cudaError_t launch_kind(const CUtensorMap& a, const CUtensorMap& b, const BwdParams& p, int grid,
-                        cudaStream_t s) {
+cudaError_t launch_kind(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c,
+                        const BwdParams& p, int grid, cudaStream_t s) {
+  constexpr size_t bytes = smem_bytes<KIND>();
   cudaError_t e = cudaFuncSetAttribute(grouped_gemm_tc_bwd_kernel<KIND>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
   if (e != cudaSuccess) return e;
-  grouped_gemm_tc_bwd_kernel<KIND><<<grid, kThreads, kSmemBytes, s>>>(a, b, p);
+  grouped_gemm_tc_bwd_kernel<KIND><<<grid, kThreads, bytes, s>>>(a, b, c, p);
   return cudaGetLastError();
 }
 
@@ -440,8 +484,8 @@ cudaError_t launch_tc_dgrad(bool swiglu, int rows, const void* A, int Kd, const 
   p.E = E; p.Kd = Kd; p.M = 0; p.N = N; p.status = status; p.wait_limit_ns = 2000000000ull;
   const int64_t tiles_max = (ceil_div(rows, BM) + E) * ceil_div(N, BN);
   const int grid = (int)(tiles_max < sms ? tiles_max : sms);
-  return swiglu ? launch_kind<kDgradSwiGLU>(ma, mb, p, grid, s)
-                : launch_kind<kDgradPlain>(ma, mb, p, grid, s);
+  return swiglu ? launch_kind<kDgradSwiGLU>(ma, mb, mb, p, grid, s)
+                : launch_kind<kDgradPlain>(ma, mb, mb, p, grid, s);
 }
 
 // Weight gradient of every expert: dW_e = A_e^T B_e with A [rows, M] and
@@ -459,7 +503,9 @@ cudaError_t launch_tc_wgrad(int rows, const void* A, int M, const void* B, int N
   p.E = E; p.Kd = 0; p.M = M; p.N = N; p.status = status; p.wait_limit_ns = 2000000000ull;
   const int64_t tiles = (int64_t)E * ceil_div(M, BM) * ceil_div(N, BN);
   const int grid = (int)(tiles < sms ? tiles : sms);
-  return launch_kind<kWgrad>(ma, mb, p, grid, s);
+  CUtensorMap mc;  // the output dW [E][M][N], stored in {64, 32, 1} boxes
+  if (!encode_map(&mc, out, (uint64_t)E, (uint64_t)M, (uint64_t)N, 32)) return cudaErrorInvalidValue;
+  return launch_kind<kWgrad>(ma, mb, mc, p, grid, s);
 }
 
 }  // namespace moe
