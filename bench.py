@@ -260,7 +260,7 @@ def workload_config(w):
 # ---------------------------------------------------------------------------
 def kernel_hash():
     h = hashlib.sha256()
-    for f in ("gemm_tc.cu", "tc_ptx.cuh", "common.cuh"):
+    for f in ("gemm_tc.cu", "gemm_tc2.cu", "tc_ptx.cuh", "common.cuh"):
         h.update(open(os.path.join(ROOT, "mixture_experts_layer_softmax_gb300", "csrc", f), "rb").read())
     return h.hexdigest()[:16]
 
@@ -533,7 +533,10 @@ def run_ours(args, w):
         comb_bytes = P * h * esz + T * h * esz + (T * h * esz if w.n_shared else 0)
         perm_gbs = perm_bytes / (stage_ms["dispatch"] / 1000.0) / 1e9
         comb_gbs = comb_bytes / (stage_ms["combine"] / 1000.0) / 1e9
-        line["roofline"] = {"kernel": "grouped_gemm_tc_kernel<FC1>", "bound": "tensor",
+        pair = args.tiling == "2cta" or (args.tiling == "auto" and P >= 512 * E)
+        fc1_kernel = ("grouped_gemm_tc2_kernel<FC1> (CTA pairs)" if pair
+                      else "grouped_gemm_tc_kernel<FC1>")
+        line["roofline"] = {"kernel": fc1_kernel, "bound": "tensor",
                             "achieved": fc1_tf, "peak": peak_tf, "unit": "TFLOP/s",
                             "frac": fc1_tf / peak_tf, "peak_kind": f"{pk_kind} bf16 burst (cuBLAS)",
                             "traffic": traffic_record(w), "flops_per_launch": fc1_flops,
