@@ -56,6 +56,8 @@ def parse():
                    help="expert GEMM tiling: auto (CTA pairs when experts average >= 512 rows)")
     p.add_argument("--tokens", type=int, default=0,
                    help="override T (smaller cases for profiler captures; not a bench line)")
+    p.add_argument("--shape", default="",
+                   help="override workload fields, e.g. T=512,h=4096,E=32,F=2048 (profiler cases)")
     return p.parse_args()
 
 
@@ -604,6 +606,10 @@ def main():
     w = workloads.ALL[args.workload] if args.workload else workloads.MIXTRAL
     if args.tokens:
         w = w.replace(name=f"{w.name}_T{args.tokens}", T=args.tokens)
+    if args.shape:
+        kv = dict(item.split("=") for item in args.shape.split(","))
+        w = w.replace(name=f"{w.name}_{args.shape.replace(',', '_').replace('=', '')}",
+                      **{k: int(v) for k, v in kv.items()})
     if args.impl == "reference":
         run_reference(args, w)
     else:
