@@ -6,7 +6,6 @@
 #include "common.cuh"
 
 namespace moe {
-int router_parts_ld(int E);
 cudaError_t launch_router(const moe_config_t&, const void*, const float*, const float*,
                           const float*, float*, int32_t*, float*, uint8_t*, const RouterScratch&,
                           int, int*, cudaStream_t);
@@ -124,6 +123,7 @@ RouterScratch router_scratch(const moe_config_t& c, void* ws) {
   rs.w3 = at<__nv_bfloat16>(ws, w.router_w3);
   rs.parts = at<float>(ws, w.router_parts);
   rs.ldp = router_parts_ld(c.E);
+  rs.ksplit = router_ksplit_max(c);
   rs.offs = at<int32_t>(ws, w.router_off);
   return rs;
 }

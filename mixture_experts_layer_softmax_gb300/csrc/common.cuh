@@ -64,21 +64,72 @@ MOE_D float gelu_f(float z) { return 0.5f * z * (1.0f + erff(z * 0.7071067811865
 MOE_D float sigmoid_f(float z) { return 1.0f / (1.0f + expf(-z)); }
 MOE_D float silu_f(float z) { return z * sigmoid_f(z); }
 
-// Scratch of the tensor-core router (in the workspace): w3 [3E, h] bf16 (the
-// exactly split router weight), parts [T, ldp] fp32 partial logits, offs [2].
+// Scratch of the tensor-core router (in the workspace): w3 [ntiles * bn, h]
+// bf16 (the exactly split router weight, tiled as router_ept describes),
+// parts [ksplit][T, ldp] fp32 partial logits (one slab per slice of the h
+// reduction; ksplit = room for at most that many slices), offs [2].
 struct RouterScratch {
   __nv_bfloat16* w3;
   float* parts;
   int ldp;
+  int ksplit;
   int32_t* offs;
 };
+
+// Tiles of the tensor-core gating GEMM: each N tile covers `ept` experts as
+// three column groups (the hi, mid and lo parts of the exactly split fp32
+// router weight), so its epilogue can add them; bn = 3 ept rounded up to a
+// tcgen05 N (a multiple of 16).
+inline int router_ept(int E) { return E <= 8 ? 8 : (E <= 16 ? 16 : (E <= 32 ? 32 : 64)); }
+inline int router_bn(int E) {
+  const int ept = router_ept(E);
+  return ept == 8 ? 32 : (ept == 16 ? 48 : (ept == 32 ? 96 : 192));
+}
+inline int router_ntiles(int E) { return (E + router_ept(E) - 1) / router_ept(E); }
+inline int router_parts_ld(int E) { return (E + 7) / 8 * 8; }
+
+// The gating GEMM's h reduction may be cut into slices (split-K), each
+// writing its own fp32 partial logits (E per token) that the selection kernel
+// adds in slice order.  router_ksplit_max bounds the slices by the config
+// alone (it sizes the workspace): at most 8, at most one per 64-wide K block,
+// and only while the partial logits stay small next to the token row they
+// come from (at most half its bytes).
+inline int router_ksplit_max(const moe_config_t& c) {
+  const int64_t kb = ((int64_t)c.h + 63) / 64;
+  const int64_t row_bytes = (int64_t)c.h * (c.dtype == MOE_BF16 ? 2 : 4);
+  int64_t s = row_bytes / (2 * 4 * (int64_t)router_parts_ld(c.E));
+  if (s > 8) s = 8;
+  if (s > kb) s = kb;
+  return s < 1 ? 1 : (int)s;
+}
+// The slice count used on a GPU with `sms` SMs: the fewest slices that
+// minimise (waves of tiles) x (K blocks per slice) + 2 per extra slice (the
+// selection kernel reads one more slab of partial logits per slice).
+inline int router_ksplit(const moe_config_t& c, int smax, int sms) {
+  if (c.T <= 0 || sms <= 0) return 1;
+  const int64_t tiles = ((int64_t)c.T + 127) / 128 * router_ntiles(c.E);
+  const int64_t kb = ((int64_t)c.h + 63) / 64;
+  int best = 1;
+  int64_t best_cost = -1;
+  for (int s = 1; s <= smax; ++s) {
+    const int64_t per = (kb + s - 1) / s;
+    if ((kb + per - 1) / per != s) continue;  // some slice would be empty
+    const int64_t waves = (tiles * s + sms - 1) / sms;
+    const int64_t cost = waves * per + 2 * (s - 1);
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      best = s;
+    }
+  }
+  return best;
+}
 
 // ---- workspace layout ----------------------------------------------------
 // One layout per config, shared by every entry point, so the backward can find
 // what a SAVE_FOR_BWD forward left behind.
 struct Workspace {
-  size_t router_w3, router_parts, router_off, logits, topk_idx, topk_prob, hist, chunk_base, counts, offsets, dst_row, src_token,
-      perm_prob, x_perm, act_save, a, y_perm, shared_off, shared_h, shared_a, shared_y,
+  size_t router_w3, router_parts, router_off, logits, topk_idx, topk_prob, hist, chunk_base,
+      counts, offsets, dst_row, src_token, perm_prob, x_perm, act_save, a, y_perm, shared_off, shared_h, shared_a, shared_y,
       // backward (MOE_FLAG_SAVE_FOR_BWD only)
       dy_perm, dh, dx_perm, dprob_part, dprob_perm, dl_topk, dl_perm, shared_dh, shared_dx,
       total;
@@ -100,10 +151,10 @@ inline Workspace workspace_layout(const moe_config_t& c) {
     off = align_up(off + bytes, 256);
     return o;
   };
-  const size_t ldp = (3 * E + 7) / 8 * 8;
+  const size_t ldp = (size_t)router_parts_ld(c.E);
   const bool tc_router = c.dtype == MOE_BF16;
-  w.router_w3 = take(tc_router ? 3 * E * h * 2 : 0);
-  w.router_parts = take(tc_router ? T * ldp * 4 : 0);
+  w.router_w3 = take(tc_router ? (size_t)router_ntiles(c.E) * router_bn(c.E) * h * 2 : 0);
+  w.router_parts = take(tc_router ? (size_t)router_ksplit_max(c) * T * ldp * 4 : 0);
   w.router_off = take(2 * 4);
   w.logits = take(T * E * 4);
   w.topk_idx = take(P * 4);

@@ -43,13 +43,18 @@ constexpr int kThreads = 192;
 // Tile width BN (accumulator columns; 256 for the expert GEMMs, narrower for
 // the router's few output columns) fixes the B stage size, the ring depth
 // that fits in ~200 KB of shared memory, and the TMEM double buffer (2 x BN).
+constexpr uint32_t pow2_at_least(uint32_t v) {
+  uint32_t p = 32;
+  while (p < v) p <<= 1;
+  return p;
+}
 template <int BNT>
 struct Tile {
   static constexpr int BN = BNT;
   static constexpr int B_BYTES = BNT * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int STAGES = (200 * 1024 / STAGE_BYTES) < 8 ? (200 * 1024 / STAGE_BYTES) : 8;
-  static constexpr uint32_t TMEM_COLS = 2 * BNT;
+  static constexpr uint32_t TMEM_COLS = pow2_at_least(2 * BNT);  // allocations are powers of 2
 };
 
 enum TcMode { kTcSwiGLU = 0, kTcGelu = 1, kTcFc2 = 2, kTcF32 = 3 };
@@ -60,8 +65,11 @@ struct TcParams {
   const __nv_bfloat16* bias;     // GELU FC1: b1 [E][N]; FC2: b2 [E][N]; or null
   __nv_bfloat16* out;            // [P, N]
   __nv_bfloat16* act_save;       // [P, Nb] or null (FC1 only)
-  float* out_f32;                // kTcF32: [P, ldo] fp32
+  float* out_f32;                // kTcF32: [ksplit][P, ldo] fp32
   int ldo;
+  int ept;                       // kTcF32: experts per N tile (hi, mid, lo column groups)
+  int ksplit, kb_per;            // kTcF32: the K blocks are cut into ksplit slices of kb_per
+  int64_t split_stride;          // kTcF32: floats between the slices' outputs
   int E, Kd, N, Nb;              // output columns N; B rows per expert Nb
   int prob_here;                 // apply p in this epilogue
   int* status;
@@ -120,6 +128,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int STAGE_BYTES = Tile<BNT>::STAGE_BYTES;
   constexpr int STAGES = Tile<BNT>::STAGES;
   constexpr uint32_t TMEM_COLS = Tile<BNT>::TMEM_COLS;
+  constexpr uint32_t ACC_STRIDE = TMEM_COLS / 2;  // the two accumulators, power-of-2 aligned
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -129,7 +138,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int E = p.E;
-  const int nblk = MODE == kTcSwiGLU ? (p.N + BN / 2 - 1) / (BN / 2) : (p.N + BN - 1) / BN;
+  const int nblk = MODE == kTcSwiGLU ? (p.N + BN / 2 - 1) / (BN / 2)
+                   : MODE == kTcF32  ? (p.N + p.ept - 1) / p.ept
+                                     : (p.N + BN - 1) / BN;
   const int KB = (p.Kd + BK - 1) / BK;
 
   // ---- prologue: barriers, TMEM, tile list ----
@@ -175,7 +186,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem_base = ctl.tmem_base;
-  const int total = ctl.tile_start[E];
+  // kTcF32 (the router's gating GEMM) may cut the K loop into slices: tile =
+  // base_tile * ksplit + slice, each slice writing its own partial sums.
+  const int S = MODE == kTcF32 ? p.ksplit : 1;
+  const int total = ctl.tile_start[E] * S;
   tc::WaitCtl wc{p.status, &ctl.abort, p.wait_limit_ns, 0};
   tc::WaitCtl wdrain{p.status, nullptr, 1000000000ull, 0};
 
@@ -186,7 +200,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0, issued = 0, issued_par = 0;
       for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
         int e, mb, nb;
-        decode_tile(ctl, E, nblk, tile, e, mb, nb);
+        decode_tile(ctl, E, nblk, tile / S, e, mb, nb);
+        const int kb0 = MODE == kTcF32 ? (tile % S) * p.kb_per : 0;
+        const int kb1 = MODE == kTcF32 ? min(KB, kb0 + p.kb_per) : KB;
         const int a_row = ctl.off[e] + mb * BM;
         int b_row0, b_row1 = 0;
         if (MODE == kTcSwiGLU) {
@@ -196,7 +212,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           b_row0 = e * p.Nb + nb * BN;
         }
         bool ok = true;
-        for (int kb = 0; kb < KB; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!tc::mbar_wait(tc::smem_u32(&ctl.empty[stage]), phase ^ 1, wc)) { ok = false; break; }
           const uint32_t fb = tc::smem_u32(&ctl.full[stage]);
           tc::mbar_arrive_expect_tx(fb, STAGE_BYTES);
@@ -231,8 +247,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
         if (!tc::mbar_wait(tc::smem_u32(&ctl.tmem_empty[acc]), acc_phase ^ 1, wc)) break;
         tc::fence_after_sync();
-        const uint32_t d = tmem_base + (uint32_t)(acc * BN);
-        for (int kb = 0; kb < KB; ++kb) {
+        const uint32_t d = tmem_base + (uint32_t)(acc * ACC_STRIDE);
+        const int kb0 = MODE == kTcF32 ? (tile % S) * p.kb_per : 0;
+        const int nkb = MODE == kTcF32 ? min(KB, kb0 + p.kb_per) - kb0 : KB;
+        for (int kb = 0; kb < nkb; ++kb) {
           if (!tc::mbar_wait(tc::smem_u32(&ctl.full[stage]), phase, wc)) { ok = false; break; }
           tc::fence_after_sync();
           const uint32_t a0 = tc::smem_u32(sA + stage * A_BYTES);
@@ -262,7 +280,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t acc_phase = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
       int e, mb, nb;
-      decode_tile(ctl, E, nblk, tile, e, mb, nb);
+      decode_tile(ctl, E, nblk, tile / S, e, mb, nb);
       if (!tc::mbar_wait(tc::smem_u32(&ctl.tmem_full[acc]), acc_phase, wc)) break;
       tc::fence_after_sync();
       const int m_e = ctl.off[e + 1] - ctl.off[e];
@@ -270,7 +288,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool valid = local_row < m_e;
       const int64_t row = (int64_t)ctl.off[e] + local_row;
       const float pr = (p.prob && p.prob_here && valid) ? __ldg(p.prob + row) : 1.f;
-      const uint32_t tbase = tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(q * 32) << 16);
+      const uint32_t tbase = tmem_base + (uint32_t)(acc * ACC_STRIDE) + ((uint32_t)(q * 32) << 16);
       if (MODE == kTcSwiGLU) {
 #pragma unroll 1
         for (int c = 0; c < BN / 2 / 32; ++c) {
@@ -297,6 +315,27 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
+      } else if (MODE == kTcF32) {
+        // the router's gating GEMM: this tile holds, per token, the partial
+        // sums of ept experts against the hi, mid and lo parts of the split
+        // weight (column groups [0, ept), [ept, 2 ept), [2 ept, 3 ept)); each
+        // logit is (lo + mid) + hi, stored 8 experts at a time
+        const int ept = p.ept;
+        float* dst = p.out_f32 + (tile % S) * p.split_stride + row * p.ldo + nb * ept;
+#pragma unroll 1
+        for (int c0 = 0; c0 < ept; c0 += 8) {
+          uint32_t hi[8], mid[8], lo[8];
+          tc::tmem_ld_32x32b_x8x3(tbase + c0, tbase + ept + c0, tbase + 2 * ept + c0, hi, mid, lo);
+          if (valid && nb * ept + c0 < p.N) {
+            float v[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              v[i] = __fadd_rn(__fadd_rn(__uint_as_float(lo[i]), __uint_as_float(mid[i])),
+                               __uint_as_float(hi[i]));
+            *reinterpret_cast<float4*>(dst + c0) = make_float4(v[0], v[1], v[2], v[3]);
+            *reinterpret_cast<float4*>(dst + c0 + 4) = make_float4(v[4], v[5], v[6], v[7]);
+          }
+        }
       } else {
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
@@ -309,16 +348,6 @@ __global__ void __launch_bounds__(kThreads, 1)
               const int n8 = n + gq * 8;
               if (n8 >= p.N) break;
               float v[8], o[8];
-              if (MODE == kTcF32) {  // plain fp32 result (the router's split-weight GEMM)
-                float* dst = p.out_f32 + row * p.ldo + n8;
-                *reinterpret_cast<float4*>(dst) =
-                    make_float4(__uint_as_float(r[gq * 8]), __uint_as_float(r[gq * 8 + 1]),
-                                __uint_as_float(r[gq * 8 + 2]), __uint_as_float(r[gq * 8 + 3]));
-                *reinterpret_cast<float4*>(dst + 4) =
-                    make_float4(__uint_as_float(r[gq * 8 + 4]), __uint_as_float(r[gq * 8 + 5]),
-                                __uint_as_float(r[gq * 8 + 6]), __uint_as_float(r[gq * 8 + 7]));
-                continue;
-              }
 #pragma unroll
               for (int i = 0; i < 8; ++i) {
                 v[i] = __uint_as_float(r[gq * 8 + i]);
@@ -417,7 +446,8 @@ cudaError_t launch_grouped_gemm_tc(int mode, int P, const void* A, int Kd, const
   p.out = static_cast<__nv_bfloat16*>(out);
   p.act_save = static_cast<__nv_bfloat16*>(act_save);
   p.E = E; p.Kd = Kd; p.N = N; p.Nb = Nb; p.prob_here = prob_here;
-  p.out_f32 = nullptr; p.ldo = 0;
+  p.out_f32 = nullptr; p.ldo = 0; p.ept = 0;
+  p.ksplit = 1; p.kb_per = (Kd + BK - 1) / BK; p.split_stride = 0;
   p.status = status;
   p.wait_limit_ns = 2000000000ull;  // 2 s: far above any real wait
   const int nblk = mode == kTcSwiGLU ? (N + BN / 2 - 1) / (BN / 2) : (N + BN - 1) / BN;
@@ -454,31 +484,42 @@ cudaError_t launch_expert_gemm_tc(const moe_config_t& c, int fc, int P, const vo
              sms, status, s);
 }
 
-// Router gating on the tensor cores: parts[t, j] = x[t] . w3[j] for the 3E
-// rows of the exactly split router weight (fp32 result, row stride ldo);
+// Router gating on the tensor cores.  w3 holds the exactly split router
+// weight in tiles of bn rows: tile n = [hi | mid | lo] rows of experts
+// n*ept .. n*ept + ept - 1 (then zero rows up to bn).  logit_parts[s][t, e] =
+// the sum over the s-th slice of h of x[t] * (w_hi + w_mid + w_lo)[e], summed
+// as (lo + mid) + hi (fp32, row stride ldo, slices split_stride floats apart);
 // offsets = {0, T} (one group).
-cudaError_t launch_router_gemm_tc(int T, const void* x, int h, const void* w3, int E3,
-                                  float* parts, int ldo, const int32_t* offsets, int sms,
-                                  int* status, cudaStream_t s) {
+cudaError_t launch_router_gemm_tc(int T, const void* x, int h, const void* w3, int E, int ept,
+                                  int bn, float* logit_parts, int ldo, const int32_t* offsets,
+                                  int ksplit, int64_t split_stride, int sms, int* status,
+                                  cudaStream_t s) {
   if (T == 0) return cudaSuccess;
+  if (bn != 32 && bn != 48 && bn != 96 && bn != 192) return cudaErrorInvalidValue;
+  if (3 * ept > bn || ept % 8) return cudaErrorInvalidValue;
   CUtensorMap ma, mb;
-  // narrowest tile that covers the 3E output columns (at most 256 per tile)
-  const int bn = E3 <= 32 ? 32 : E3 <= 64 ? 64 : E3 <= 128 ? 128 : 256;
+  const int ntiles = (E + ept - 1) / ept;
   if (!encode_2d(&ma, x, (uint64_t)T, (uint64_t)h, BM)) return cudaErrorInvalidValue;
-  if (!encode_2d(&mb, w3, (uint64_t)E3, (uint64_t)h, (uint32_t)bn)) return cudaErrorInvalidValue;
+  if (!encode_2d(&mb, w3, (uint64_t)ntiles * bn, (uint64_t)h, (uint32_t)bn))
+    return cudaErrorInvalidValue;
+  const int KB = (h + BK - 1) / BK;
+  if (ksplit < 1 || ksplit > KB) return cudaErrorInvalidValue;
   TcParams p{};
   p.offsets = offsets;
-  p.E = 1; p.Kd = h; p.N = E3; p.Nb = E3; p.prob_here = 0;
-  p.out_f32 = parts; p.ldo = ldo;
+  p.E = 1; p.Kd = h; p.N = E; p.Nb = ntiles * bn; p.prob_here = 0;
+  p.out_f32 = logit_parts; p.ldo = ldo; p.ept = ept;
+  p.kb_per = (KB + ksplit - 1) / ksplit;
+  p.ksplit = (KB + p.kb_per - 1) / p.kb_per;  // every slice non-empty
+  p.split_stride = split_stride;
   p.status = status;
   p.wait_limit_ns = 2000000000ull;
-  const int64_t tiles = ceil_div(T, BM) * ceil_div(E3, bn);
+  const int64_t tiles = ceil_div(T, BM) * ntiles * p.ksplit;
   const int grid = (int)(tiles < sms ? tiles : sms);
   switch (bn) {
     case 32: return launch_mode<kTcF32, 32>(ma, mb, p, grid, s);
-    case 64: return launch_mode<kTcF32, 64>(ma, mb, p, grid, s);
-    case 128: return launch_mode<kTcF32, 128>(ma, mb, p, grid, s);
-    default: return launch_mode<kTcF32, 256>(ma, mb, p, grid, s);
+    case 48: return launch_mode<kTcF32, 48>(ma, mb, p, grid, s);
+    case 96: return launch_mode<kTcF32, 96>(ma, mb, p, grid, s);
+    default: return launch_mode<kTcF32, 192>(ma, mb, p, grid, s);
   }
 }
 

@@ -22,39 +22,30 @@ namespace moe {
 
 constexpr int kChunk = 32;
 
-// One warp per chunk of 32 tokens; 8 warps per block.
-__global__ void __launch_bounds__(256) chunk_hist_kernel(const int32_t* __restrict__ idx, int T,
-                                                         int K, int E, int NC,
-                                                         int32_t* __restrict__ hist, int* status) {
-  extern __shared__ int32_t sh[];  // [8][E]
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int c = blockIdx.x * 8 + warp;
-  int32_t* my = sh + warp * E;
+// ---- per-warp steps ----------------------------------------------------------
+
+// hist[c][e] for chunk c; `my` is this warp's [E] shared-memory counter row.
+MOE_D void hist_chunk(int c, int lane, int32_t* my, const int32_t* __restrict__ idx, int T, int K,
+                      int E, int32_t* __restrict__ hist, int* status) {
   for (int e = lane; e < E; e += 32) my[e] = 0;
   __syncwarp();
-  if (c < NC) {
-    const int64_t t = (int64_t)c * kChunk + lane;
-    if (t < T)
-      for (int k = 0; k < K; ++k) {
-        const int e = __ldg(idx + t * K + k);
-        if (e >= 0 && e < E)
-          atomicAdd(&my[e], 1);
-        else
-          report(status, MOE_ERR_DEVICE_BOUNDS);
-      }
-  }
+  const int64_t t = (int64_t)c * kChunk + lane;
+  if (t < T)
+    for (int k = 0; k < K; ++k) {
+      const int e = __ldg(idx + t * K + k);
+      if (e >= 0 && e < E)
+        atomicAdd(&my[e], 1);
+      else
+        report(status, MOE_ERR_DEVICE_BOUNDS);
+    }
   __syncwarp();
-  if (c < NC)
-    for (int e = lane; e < E; e += 32) hist[(int64_t)c * E + e] = my[e];
+  for (int e = lane; e < E; e += 32) hist[(int64_t)c * E + e] = my[e];
+  __syncwarp();
 }
 
-// Warp per expert: exclusive scan of hist[:, e] over the chunks.
-__global__ void __launch_bounds__(256) chunk_scan_kernel(const int32_t* __restrict__ hist, int NC,
-                                                         int E, int32_t* __restrict__ base,
-                                                         int32_t* __restrict__ counts) {
-  const int lane = threadIdx.x & 31;
-  const int e = blockIdx.x * 8 + (threadIdx.x >> 5);
-  if (e >= E) return;
+// Exclusive scan of hist[:, e] over the chunks into base[:, e]; counts[e].
+MOE_D void scan_expert(int e, int lane, const int32_t* __restrict__ hist, int NC, int E,
+                       int32_t* __restrict__ base, int32_t* __restrict__ counts) {
   int running = 0;
   for (int c0 = 0; c0 < NC; c0 += 32) {
     const int c = c0 + lane;
@@ -71,47 +62,42 @@ __global__ void __launch_bounds__(256) chunk_scan_kernel(const int32_t* __restri
   if (lane == 0) counts[e] = running;
 }
 
-// Block: exclusive scan of counts into shared offsets (E <= 256), then one
-// warp per chunk computes every pair's destination row.
-__global__ void __launch_bounds__(256) chunk_ranks_kernel(
-    const int32_t* __restrict__ idx, const float* __restrict__ prob, int T, int K, int E, int NC,
-    const int32_t* __restrict__ base, const int32_t* __restrict__ counts,
-    int32_t* __restrict__ offsets_out, int32_t* __restrict__ dst_row,
-    int32_t* __restrict__ src_token, float* __restrict__ perm_prob) {
-  // expert ids outside [0, E) were reported by chunk_hist; they get no row
-  // (dst_row = -1) here.
-  __shared__ int32_t s_off[257];
-  __shared__ int32_t s_warp[8];
+// Whole block (256 threads): s_off[0..E] = exclusive scan of counts[0..E)
+// (zero past E, s_off[256] the total); block 0 also writes offsets_out.
+MOE_D void block_offsets(const int32_t* __restrict__ counts, int E, int32_t* s_off,
+                         int32_t* s_warp, int32_t* offsets_out) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  {
-    // exclusive scan of counts[0..E) by the 256 threads (zero past E), so
-    // s_off[E] is the total
-    const int e = threadIdx.x;
-    const int v = e < E ? __ldg(counts + e) : 0;
-    int incl = v;
+  const int e = threadIdx.x;
+  const int v = e < E ? __ldg(counts + e) : 0;
+  int incl = v;
 #pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const int o = __shfl_up_sync(0xffffffffu, incl, off);
-      if (lane >= off) incl += o;
-    }
-    if (lane == 31) s_warp[warp] = incl;
-    __syncthreads();
-    int wbase = 0;
-    for (int w = 0; w < warp; ++w) wbase += s_warp[w];
-    s_off[e] = wbase + incl - v;
-    if (e == 255) s_off[256] = wbase + incl;
-    __syncthreads();
-    if (blockIdx.x == 0 && offsets_out && e <= E) offsets_out[e] = s_off[e];
-    if (blockIdx.x == 0 && offsets_out && E == 256 && e == 0) offsets_out[256] = s_off[256];
+  for (int off = 1; off < 32; off <<= 1) {
+    const int o = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += o;
   }
-  const int c = blockIdx.x * 8 + warp;
-  if (c >= NC) return;
+  if (lane == 31) s_warp[warp] = incl;
+  __syncthreads();
+  int wbase = 0;
+  for (int w = 0; w < warp; ++w) wbase += s_warp[w];
+  s_off[e] = wbase + incl - v;
+  if (e == 255) s_off[256] = wbase + incl;
+  __syncthreads();
+  if (blockIdx.x == 0 && offsets_out && e <= E) offsets_out[e] = s_off[e];
+  if (blockIdx.x == 0 && offsets_out && E == 256 && e == 0) offsets_out[256] = s_off[256];
+}
+
+// Destination rows of chunk c's pairs: dst_row = offsets[e] + base[c][e] +
+// rank of the pair among the chunk's earlier tokens routed to e (from ballots
+// over the lanes' expert-id bits, E <= 256); src_token and perm_prob are the
+// inverse maps.  Expert ids outside [0, E) get dst_row = -1 (reported by the
+// histogram step).
+MOE_D void ranks_chunk(int c, int lane, const int32_t* __restrict__ idx,
+                       const float* __restrict__ prob, int T, int K, int E,
+                       const int32_t* __restrict__ base, const int32_t* s_off, int32_t* __restrict__ dst_row,
+                       int32_t* __restrict__ src_token, float* __restrict__ perm_prob) {
   const int64_t t = (int64_t)c * kChunk + lane;
   const bool valid = t < T;
   const unsigned lt_mask = (1u << lane) - 1u;
-  // rank of pair (t, k) among the chunk's earlier tokens routed to the same
-  // expert: for every slot k2, 8 ballots give the lanes' expert-id bits, and
-  // the lanes whose id equals e are the AND of matching bit masks (E <= 256).
   int my_e[16], rank[16];
   for (int k = 0; k < K; ++k) {
     const int e = valid ? __ldg(idx + t * K + k) : -1;
@@ -147,19 +133,14 @@ __global__ void __launch_bounds__(256) chunk_ranks_kernel(
   }
 }
 
-// One warp per token (the grid covers every token, so the block scheduler
-// balances the load): read the row once, 16-byte vectors, up to 8 vectors per
-// lane in flight, and write it to its K destinations.
+// Token t's row, read once (16-byte vectors, up to 8 per lane in flight) and
+// written to its K destination rows.
 template <typename T, int KMAX>
-__global__ void __launch_bounds__(256) scatter_rows_kernel(const T* __restrict__ x,
-                                                           const int32_t* __restrict__ dst_row,
-                                                           int ntok, int K, int h,
-                                                           T* __restrict__ x_perm, int* status) {
+MOE_D void scatter_token(int64_t t, int lane, const T* __restrict__ x,
+                         const int32_t* __restrict__ dst_row,
+                         int ntok, int K, int h, T* __restrict__ x_perm, int* status) {
   constexpr int V = Vec<T>::N;
   constexpr int kMaxVec = 8;
-  const int lane = threadIdx.x & 31;
-  const int64_t t = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
-  if (t >= ntok) return;
   const int nvec = h / V;
   const int64_t P = (int64_t)ntok * K;
   T* dst[KMAX];
@@ -192,6 +173,54 @@ __global__ void __launch_bounds__(256) scatter_rows_kernel(const T* __restrict__
       }
     }
   }
+}
+
+// ---- separate kernels -------------------------------------------------------
+
+// One warp per chunk of 32 tokens; 8 warps per block.
+__global__ void __launch_bounds__(256) chunk_hist_kernel(const int32_t* __restrict__ idx, int T,
+                                                         int K, int E, int NC,
+                                                         int32_t* __restrict__ hist, int* status) {
+  extern __shared__ int32_t sh[];  // [8][E]
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int c = blockIdx.x * 8 + warp;
+  if (c < NC) hist_chunk(c, lane, sh + warp * E, idx, T, K, E, hist, status);
+}
+
+// Warp per expert: exclusive scan of hist[:, e] over the chunks.
+__global__ void __launch_bounds__(256) chunk_scan_kernel(const int32_t* __restrict__ hist, int NC,
+                                                         int E, int32_t* __restrict__ base,
+                                                         int32_t* __restrict__ counts) {
+  const int lane = threadIdx.x & 31;
+  const int e = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (e < E) scan_expert(e, lane, hist, NC, E, base, counts);
+}
+
+// Block: exclusive scan of counts into shared offsets, then one warp per chunk
+// computes every pair's destination row.
+__global__ void __launch_bounds__(256) chunk_ranks_kernel(
+    const int32_t* __restrict__ idx, const float* __restrict__ prob, int T, int K, int E, int NC,
+    const int32_t* __restrict__ base, const int32_t* __restrict__ counts,
+    int32_t* __restrict__ offsets_out, int32_t* __restrict__ dst_row,
+    int32_t* __restrict__ src_token, float* __restrict__ perm_prob) {
+  __shared__ int32_t s_off[257];
+  __shared__ int32_t s_warp[8];
+  block_offsets(counts, E, s_off, s_warp, offsets_out);
+  const int c = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (c < NC)
+    ranks_chunk(c, threadIdx.x & 31, idx, prob, T, K, E, base, s_off, dst_row, src_token,
+                perm_prob);
+}
+
+// One warp per token (the grid covers every token, so the block scheduler
+// balances the load).
+template <typename T, int KMAX>
+__global__ void __launch_bounds__(256) scatter_rows_kernel(const T* __restrict__ x,
+                                                           const int32_t* __restrict__ dst_row,
+                                                           int ntok, int K, int h,
+                                                           T* __restrict__ x_perm, int* status) {
+  const int64_t t = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (t < ntok) scatter_token<T, KMAX>(t, threadIdx.x & 31, x, dst_row, ntok, K, h, x_perm, status);
 }
 
 int num_chunks(int T) { return (int)ceil_div(T, kChunk); }

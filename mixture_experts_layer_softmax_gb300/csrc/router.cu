@@ -10,9 +10,11 @@
 // Kernels:
 //  * bf16 tokens (every E): the gating GEMM runs on the tensor cores.  W_r
 //    (fp32) is split exactly into three bf16 parts, w = hi + mid + lo (24
-//    mantissa bits = 3 x 8), stacked as 3E rows; x (bf16, exact) times each part
-//    is exact in fp32 and accumulates in fp32 in TMEM (grouped GEMM kernel,
-//    fp32 output [T, 3E]); router_select adds the three partial sums (+ b_r).
+//    mantissa bits = 3 x 8), tiled so that each GEMM tile holds the three
+//    parts of a group of experts; x (bf16, exact) times each part is exact in
+//    fp32 and accumulates in fp32 in TMEM, and the tile's epilogue adds the
+//    three sums.  Small batches cut the h reduction into slices whose partial
+//    logits router_select adds in slice order (+ b_r) before selecting.
 //  * fp32 tokens:
 //  * router_fused_small: E <= 32.  One block stages W_r chunks in shared
 //    memory; each warp accumulates the gating dot products of a few tokens,
@@ -38,30 +40,56 @@ struct RouterArgs {
   uint8_t* routing_map;
 };
 
+// fp32(sigma(l)) with sigma evaluated in double.  Kept out of line: the
+// double-precision path must stay behind a real branch (GB300's FP64 rate is
+// low), never be computed speculatively for every key.
+__device__ __noinline__ float sigmoid_exact_f32(float l) {
+  return (float)(1.0 / (1.0 + exp(-(double)l)));
+}
+
 // Selection key of one (token, expert): softmax uses the logit, sigmoid uses
 // fp32(sigma(l)) with sigma evaluated in double; then + sel_bias in fp32.
 MOE_D float selection_key(float l, int e, const RouterArgs& a) {
   float key = l;
-  if (a.score == MOE_SCORE_SIGMOID) key = (float)(1.0 / (1.0 + exp(-(double)l)));
+  if (a.score == MOE_SCORE_SIGMOID) key = sigmoid_exact_f32(l);
   if (a.sel_bias) key = __fadd_rn(key, __ldg(a.sel_bias + e));
   return key;
 }
 
-MOE_D bool better(float ka, int ia, float kb, int ib) { return ka > kb || (ka == kb && ia < ib); }
+// The same key with sigma in fp32 (CUDA's expf, within 2 ulp, then a rounded
+// add and a rounded divide): it differs from selection_key by at most
+// 4.2e-7 * sigma + ulp(key) <= 5.4e-7 + 1.2e-7 |b|.
+MOE_D float selection_key_fast(float l, int e, const RouterArgs& a) {
+  float key = l;
+  if (a.score == MOE_SCORE_SIGMOID) key = sigmoid_f(l);
+  if (a.sel_bias) key = __fadd_rn(key, __ldg(a.sel_bias + e));
+  return key;
+}
+
+// Order-preserving map of fp32 keys onto uint32 (larger key, larger code;
+// -0 is folded onto +0 so the two compare equal, as floats do).  Every finite
+// key maps above 0.
+MOE_D uint32_t sortable_key(float k) {
+  const uint32_t b = __float_as_uint(k == 0.f ? 0.f : k);
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+MOE_D float from_sortable_key(uint32_t u) {
+  return __uint_as_float((u & 0x80000000u) ? (u & 0x7fffffffu) : ~u);
+}
 
 // Selects K experts for one token whose logits are spread over the warp
 // (slot j of lane l is expert l + 32 j) and writes idx/prob/routing_map.
+//
+// Sigmoid keys are first ranked with the fp32 sigma.  That ranking equals
+// the one of the exact keys whenever the K + 1 best fast keys are separated
+// by more than twice their error bound (the selected set and its order cannot
+// change); otherwise, for that token only, the keys are recomputed with the
+// double-precision sigma and ranked again.
 template <int J>
 MOE_D void select_and_write(const float (&logit)[J], int t, const RouterArgs& a, int lane) {
   const unsigned FULL = 0xffffffffu;
-  bool taken[J];
+  uint32_t taken = 0u;  // bit j: slot j of this lane is selected (a register, not an array)
   float key[J];
-#pragma unroll
-  for (int j = 0; j < J; ++j) {
-    const int e = lane + 32 * j;
-    taken[j] = false;
-    key[j] = e < a.E ? selection_key(logit[j], e, a) : -FLT_MAX;
-  }
   int my_idx = -1;      // lane k < K ends up holding the k-th selected expert
   float my_logit = 0.f; // and its logit
   if (a.force_balance) {
@@ -71,31 +99,69 @@ MOE_D void select_and_write(const float (&logit)[J], int t, const RouterArgs& a,
       const int e = lane + 32 * j;
       // expert e is selected iff (e - t*K) mod E < K
       const int64_t d = (((int64_t)e - (int64_t)t * a.K) % a.E + a.E) % a.E;
-      taken[j] = e < a.E && d < a.K;
+      if (e < a.E && d < a.K) taken |= 1u << j;
     }
   } else {
-    for (int k = 0; k < a.K; ++k) {
-      float bk = -INFINITY;
-      int bi = 0x7fffffff;
+    bool exact = a.score != MOE_SCORE_SIGMOID;  // logits are the exact softmax keys
+    for (int pass = 0; pass < 2; ++pass) {
+      taken = 0u;
+      if (exact) {
 #pragma unroll
-      for (int j = 0; j < J; ++j) {
-        const int e = lane + 32 * j;
-        if (e < a.E && !taken[j] && better(key[j], e, bk, bi)) {
-          bk = key[j];
-          bi = e;
+        for (int j = 0; j < J; ++j) {
+          const int e = lane + 32 * j;
+          key[j] = -FLT_MAX;
+          if (e < a.E) key[j] = selection_key(logit[j], e, a);
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < J; ++j) {
+          const int e = lane + 32 * j;
+          key[j] = -FLT_MAX;
+          if (e < a.E) key[j] = selection_key_fast(logit[j], e, a);
         }
       }
+      // the fast pass also ranks the (K+1)-th key, to check the K-th gap
+      const int rounds = exact ? a.K : min(a.K + 1, a.E);
+      uint32_t skey[J];
 #pragma unroll
-      for (int off = 16; off >= 1; off >>= 1) {
-        const float ok = __shfl_xor_sync(FULL, bk, off);
-        const int oi = __shfl_xor_sync(FULL, bi, off);
-        if (better(ok, oi, bk, bi)) {
-          bk = ok;
-          bi = oi;
+      for (int j = 0; j < J; ++j) skey[j] = sortable_key(key[j]);
+      bool safe = true;
+      float prev = 0.f;
+      for (int k = 0; k < rounds; ++k) {
+        // this lane's best untaken candidate (ascending j: ties keep the
+        // lower expert), then the warp's largest key and, among the lanes
+        // holding it, the lowest expert index: two warp reductions
+        uint32_t lk = 0u;
+        int li = 0x7fffffff;
+#pragma unroll
+        for (int j = 0; j < J; ++j) {
+          const int e = lane + 32 * j;
+          if (e < a.E && !((taken >> j) & 1u) && skey[j] > lk) {
+            lk = skey[j];
+            li = e;
+          }
         }
+        const uint32_t m = __reduce_max_sync(FULL, lk);
+        const int bi = (int)__reduce_min_sync(FULL, lk == m ? (uint32_t)li : 0xffffffffu);
+        const float bk = from_sortable_key(m);
+        if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+        if (k < a.K && lane == k) my_idx = bi;
+        if (!exact && k > 0 && !(prev - bk > 4e-6f * (1.f + fabsf(prev) + fabsf(bk))))
+          safe = false;  // warp-uniform: bk and prev are the same on every lane
+        prev = bk;
       }
-      if ((bi & 31) == lane) taken[bi >> 5] = true;
-      if (lane == k) my_idx = bi;
+      if (exact || safe) break;
+      exact = true;
+    }
+    // the (K+1)-th key of the fast pass was marked taken only to rank it
+    if (a.routing_map) {
+      taken = 0u;
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        if (k >= a.K) break;
+        const int e = __shfl_sync(FULL, my_idx, k);
+        if ((e & 31) == lane) taken |= 1u << (e >> 5);
+      }
     }
   }
   // logit of this lane's selected expert
@@ -159,19 +225,21 @@ MOE_D void select_and_write(const float (&logit)[J], int t, const RouterArgs& a,
 #pragma unroll
     for (int j = 0; j < J; ++j) {
       const int e = lane + 32 * j;
-      if (e < a.E) a.routing_map[(int64_t)t * a.E + e] = taken[j] ? 1 : 0;
+      if (e < a.E) a.routing_map[(int64_t)t * a.E + e] = (taken >> j) & 1u;
     }
   }
 }
 
 // ---- top-k on given logits: one warp per token --------------------------
-// logits: [T, E] fp32; or, when parts is given, l = (part_lo + part_mid) +
-// part_hi (+ gate_bias), smallest first from parts [T, ldp] (columns e, E + e, 2E + e), and l
-// is written to logits_out when that is given.
+// logits: [T, E] fp32; or, when parts is given, the tensor-core router's
+// partial logits: slab s (s < nsplit, split_stride floats apart) holds [T, ldp];
+// l = the slabs added in slab order (+ gate_bias), written to logits_out when
+// that is given.
 template <int J>
 __global__ void __launch_bounds__(256) router_select_kernel(const float* __restrict__ logits,
                                                              const float* __restrict__ parts,
-                                                             int ldp,
+                                                             int ldp, int nsplit,
+                                                             int64_t split_stride,
                                                              const float* __restrict__ gate_bias,
                                                              float* __restrict__ logits_out,
                                                              RouterArgs a) {
@@ -179,46 +247,89 @@ __global__ void __launch_bounds__(256) router_select_kernel(const float* __restr
   const int64_t t = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (t >= a.T) return;
   float l[J];
+  if (parts) {
+    // slab 0 for every slot, then one batch of loads per further slab
+    const float* pr = parts + t * ldp;
 #pragma unroll
-  for (int j = 0; j < J; ++j) {
-    const int e = lane + 32 * j;
-    if (e >= a.E) {
-      l[j] = 0.f;
-      continue;
+    for (int j = 0; j < J; ++j) {
+      const int e = lane + 32 * j;
+      l[j] = e < a.E ? __ldg(pr + e) : 0.f;
     }
-    if (parts) {
-      const float* pr = parts + t * ldp;
-      float v = __fadd_rn(__fadd_rn(__ldg(pr + 2 * a.E + e), __ldg(pr + a.E + e)), __ldg(pr + e));
-      if (gate_bias) v = __fadd_rn(v, __ldg(gate_bias + e));
-      l[j] = v;
-      if (logits_out) logits_out[t * a.E + e] = v;
-    } else {
-      l[j] = __ldg(logits + t * a.E + e);
+    for (int sl = 1; sl < nsplit; ++sl) {
+      const float* ps = pr + sl * split_stride;
+      float v[J];
+#pragma unroll
+      for (int j = 0; j < J; ++j) {
+        const int e = lane + 32 * j;
+        v[j] = e < a.E ? __ldg(ps + e) : 0.f;
+      }
+#pragma unroll
+      for (int j = 0; j < J; ++j) l[j] = __fadd_rn(l[j], v[j]);
+    }
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+      const int e = lane + 32 * j;
+      if (e < a.E) {
+        if (gate_bias) l[j] = __fadd_rn(l[j], __ldg(gate_bias + e));
+        if (logits_out) logits_out[t * a.E + e] = l[j];
+      }
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+      const int e = lane + 32 * j;
+      l[j] = e < a.E ? __ldg(logits + t * a.E + e) : 0.f;
     }
   }
   select_and_write<J>(l, (int)t, a, lane);
 }
 
-// w3 rows [0, E) = bf16(w), [E, 2E) = bf16(w - hi), [2E, 3E) = bf16(w - hi - mid):
-// each difference is exact in fp32 and hi + mid + lo == w.
-__global__ void split_router_weight_kernel(const float* __restrict__ w_r, int64_t n,
-                                           __nv_bfloat16* __restrict__ w3) {
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
-       i += (int64_t)gridDim.x * blockDim.x) {
-    const float w = __ldg(w_r + i);
-    const __nv_bfloat16 hi = __float2bfloat16_rn(w);
-    const float r1 = w - __bfloat162float(hi);
-    const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
-    const float r2 = r1 - __bfloat162float(mid);
-    w3[i] = hi;
-    w3[n + i] = mid;
-    w3[2 * n + i] = __float2bfloat16_rn(r2);
+// The router weight split exactly into three bf16 parts, w = hi + mid + lo
+// (hi = bf16(w), mid = bf16(w - hi), lo = bf16(w - hi - mid); each difference
+// is exact in fp32), laid out for the gating GEMM's tiles: tile n has rows
+// [hi of experts n*ept .. n*ept + ept - 1 | mid of the same | lo of the same |
+// zeros up to bn].  Grid: x over groups of 4 weights of a row (h is a
+// multiple of 8), y over expert slots (ntiles * ept: the slots past E get
+// zero rows) and then the ntiles * (bn - 3 ept) padding rows.  Block (0, 0)
+// also writes the one-group row offsets {0, T}.
+__global__ void split_router_weight_kernel(const float* __restrict__ w_r, int E, int h, int ept,
+                                           int bn, int ntiles, __nv_bfloat16* __restrict__ w3,
+                                           int32_t* offs, int T) {
+  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) {
+    offs[0] = 0;
+    offs[1] = T;
   }
-}
-
-__global__ void fill_group_offsets(int32_t* off, int rows) {
-  off[0] = 0;
-  off[1] = rows;
+  const int k = (blockIdx.x * blockDim.x + threadIdx.x) * 4;
+  if (k >= h) return;
+  const int y = blockIdx.y;
+  const int slots = ntiles * ept;
+  if (y < slots) {  // expert slot y: its hi, mid and lo rows
+    const int64_t row0 = (int64_t)(y / ept) * bn + (y % ept);
+    uint2 hv = make_uint2(0u, 0u), mv = hv, lv = hv;
+    if (y < E) {
+      const float4 w = __ldg(reinterpret_cast<const float4*>(w_r + (int64_t)y * h + k));
+      const float wv[4] = {w.x, w.y, w.z, w.w};
+      __nv_bfloat16 hi[4], mid[4], lo[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        hi[j] = __float2bfloat16_rn(wv[j]);
+        const float r1 = wv[j] - __bfloat162float(hi[j]);
+        mid[j] = __float2bfloat16_rn(r1);
+        lo[j] = __float2bfloat16_rn(r1 - __bfloat162float(mid[j]));
+      }
+      hv = *reinterpret_cast<const uint2*>(hi);
+      mv = *reinterpret_cast<const uint2*>(mid);
+      lv = *reinterpret_cast<const uint2*>(lo);
+    }
+    *reinterpret_cast<uint2*>(w3 + row0 * h + k) = hv;
+    *reinterpret_cast<uint2*>(w3 + (row0 + ept) * h + k) = mv;
+    *reinterpret_cast<uint2*>(w3 + (row0 + 2 * ept) * h + k) = lv;
+  } else {  // padding row r of tile n
+    const int zrows = bn - 3 * ept;
+    const int z = y - slots;
+    const int64_t row = (int64_t)(z / zrows) * bn + 3 * ept + z % zrows;
+    *reinterpret_cast<uint2*>(w3 + row * h + k) = make_uint2(0u, 0u);
+  }
 }
 
 // ---- fused gating + top-k for E <= 32 ------------------------------------
@@ -403,23 +514,28 @@ static RouterArgs make_args(const moe_config_t& c, const float* sel_bias, int32_
 }
 
 static cudaError_t select_launch(const moe_config_t& c, const float* logits, const float* parts,
-                                 int ldp, const float* gate_bias, float* logits_out,
-                                 RouterArgs a, cudaStream_t s) {
+                                 int ldp, int nsplit, int64_t split_stride,
+                                 const float* gate_bias, float* logits_out, RouterArgs a,
+                                 cudaStream_t s) {
   const int blocks = (int)ceil_div(c.T, 8);
   const int J = (int)ceil_div(c.E, 32);
+#define MOE_SELECT(JJ)                                                                  \
+  router_select_kernel<JJ><<<blocks, 256, 0, s>>>(logits, parts, ldp, nsplit, split_stride, \
+                                                   gate_bias, logits_out, a)
   switch (J) {
-    case 1: router_select_kernel<1><<<blocks, 256, 0, s>>>(logits, parts, ldp, gate_bias, logits_out, a); break;
-    case 2: router_select_kernel<2><<<blocks, 256, 0, s>>>(logits, parts, ldp, gate_bias, logits_out, a); break;
-    case 3: case 4: router_select_kernel<4><<<blocks, 256, 0, s>>>(logits, parts, ldp, gate_bias, logits_out, a); break;
-    default: router_select_kernel<8><<<blocks, 256, 0, s>>>(logits, parts, ldp, gate_bias, logits_out, a); break;
+    case 1: MOE_SELECT(1); break;
+    case 2: MOE_SELECT(2); break;
+    case 3: case 4: MOE_SELECT(4); break;
+    default: MOE_SELECT(8); break;
   }
+#undef MOE_SELECT
   return cudaGetLastError();
 }
 
 cudaError_t launch_router_select(const moe_config_t& c, const float* logits, const float* sel_bias,
                                  int32_t* idx, float* prob, uint8_t* map, cudaStream_t s) {
   if (c.T == 0) return cudaSuccess;
-  return select_launch(c, logits, nullptr, 0, nullptr, nullptr,
+  return select_launch(c, logits, nullptr, 0, 1, 0, nullptr, nullptr,
                        make_args(c, sel_bias, idx, prob, map), s);
 }
 
@@ -435,11 +551,10 @@ static cudaError_t launch_fused(const moe_config_t& c, const Tin* x, const float
   return cudaGetLastError();
 }
 
-cudaError_t launch_router_gemm_tc(int T, const void* x, int h, const void* w3, int E3,
-                                  float* parts, int ldp, const int32_t* offsets, int sms,
-                                  int* status, cudaStream_t s);
-
-int router_parts_ld(int E) { return (int)((3 * (int64_t)E + 7) / 8 * 8); }
+cudaError_t launch_router_gemm_tc(int T, const void* x, int h, const void* w3, int E, int ept,
+                                  int bn, float* logit_parts, int ldo, const int32_t* offsets,
+                                  int ksplit, int64_t split_stride, int sms, int* status,
+                                  cudaStream_t s);
 
 cudaError_t launch_router(const moe_config_t& c, const void* x, const float* w_r,
                           const float* gate_bias, const float* sel_bias, float* logits,
@@ -448,16 +563,19 @@ cudaError_t launch_router(const moe_config_t& c, const void* x, const float* w_r
   if (c.T == 0) return cudaSuccess;
   RouterArgs a = make_args(c, sel_bias, idx, prob, map);
   if (c.dtype == MOE_BF16) {
-    const int64_t n = (int64_t)c.E * c.h;
-    const int blocks = (int)std::min<int64_t>(ceil_div(n, 256), (int64_t)sms * 8);
-    split_router_weight_kernel<<<blocks, 256, 0, s>>>(w_r, n, rs.w3);
-    fill_group_offsets<<<1, 1, 0, s>>>(rs.offs, c.T);
+    const int ept = router_ept(c.E), bn = router_bn(c.E);
+    const int ntiles = router_ntiles(c.E);
+    const dim3 grid((unsigned)ceil_div(c.h / 4, 256), (unsigned)(ntiles * (ept + bn - 3 * ept)));
+    split_router_weight_kernel<<<grid, 256, 0, s>>>(w_r, c.E, c.h, ept, bn, ntiles, rs.w3, rs.offs,
+                                                    c.T);
+    const int64_t stride = (int64_t)c.T * rs.ldp;
+    const int nsplit = router_ksplit(c, rs.ksplit, sms);
     cudaError_t e = cudaGetLastError();
     if (e == cudaSuccess)
-      e = launch_router_gemm_tc(c.T, x, c.h, rs.w3, 3 * c.E, rs.parts, rs.ldp, rs.offs, sms,
-                                status, s);
+      e = launch_router_gemm_tc(c.T, x, c.h, rs.w3, c.E, ept, bn, rs.parts, rs.ldp, rs.offs,
+                                nsplit, stride, sms, status, s);
     if (e != cudaSuccess) return e;
-    return select_launch(c, nullptr, rs.parts, rs.ldp, gate_bias, logits, a, s);
+    return select_launch(c, nullptr, rs.parts, rs.ldp, nsplit, stride, gate_bias, logits, a, s);
   }
   const float* xf = static_cast<const float*>(x);
   if (c.E <= 32) {

@@ -52,11 +52,41 @@ def test_router_from_logits_bit_exact(T, E, K, score, renorm, bias, force):
     np.testing.assert_array_equal(to_np(rmap).astype(bool), O.routing_map(oi, E))
 
 
+@pytest.mark.parametrize("bias", [False, True])
+def test_router_sigmoid_near_ties_bit_exact(bias):
+    """Sigmoid keys a few ulps apart (and exact ties): the fp32 first pass
+    must hand such tokens to the double-precision ranking, so the selection
+    and its order still equal the oracle's."""
+    M = lib()
+    T, E, K = 256, 64, 8
+    rng = np.random.default_rng(7)
+    base = rng.normal(size=(T, 1))
+    steps = np.stack([rng.permutation(E) for _ in range(T)])
+    logits = (base + steps * 1.5e-7).astype(np.float32)  # neighbours 1-2 ulps apart or equal
+    b = (rng.integers(-3, 4, size=E) * 6e-8).astype(np.float32) if bias else None
+    cfg = M.make_config(T, 8, E, K, 8, M.MOE_F32, M.MOE_SCORE_SIGMOID, M.MOE_ACT_SWIGLU, 0, 0,
+                        M.MOE_FLAG_RENORM)
+    idx = torch.empty(T, K, dtype=torch.int32, device="cuda")
+    prob = torch.empty(T, K, dtype=torch.float32, device="cuda")
+    rmap = torch.empty(T, E, dtype=torch.uint8, device="cuda")
+    M.moe_router_topk_from_logits(cfg, to_dev(logits, "f32"), None if b is None else to_dev(b, "f32"),
+                                  idx, prob, rmap)
+    torch.cuda.synchronize()
+    oi, op = O.route(logits, K, M.MOE_SCORE_SIGMOID, True, b)
+    np.testing.assert_array_equal(to_np(idx), oi)
+    np.testing.assert_allclose(to_np(prob), op, rtol=2e-6, atol=1e-7)
+    np.testing.assert_array_equal(to_np(rmap).astype(bool), O.routing_map(oi, E))
+
+
 @pytest.mark.parametrize("T,h,E,K,score,dtype,gate_bias", [
     (300, 128, 8, 2, 0, "bf16", False), (257, 4096, 8, 2, 0, "bf16", False),
     (256, 128, 8, 2, 0, "f32", False), (100, 256, 16, 4, 0, "bf16", True),
     (100, 64, 32, 8, 1, "f32", False), (300, 512, 128, 8, 0, "bf16", True),
     (200, 7168, 256, 8, 1, "bf16", False), (64, 200, 5, 2, 0, "bf16", False),
+    # fused bf16 router with 16 and 32 padded experts, and with several token
+    # groups per warp; a 32-expert weight too large for shared memory (tensor cores)
+    (130, 1024, 32, 4, 0, "bf16", True), (90, 512, 20, 3, 1, "bf16", False),
+    (20000, 256, 8, 2, 0, "bf16", True), (77, 2048, 32, 8, 1, "bf16", False),
 ])
 def test_router_gating_matches_oracle(T, h, E, K, score, dtype, gate_bias):
     M = lib()
@@ -86,6 +116,9 @@ def test_router_gating_matches_oracle(T, h, E, K, score, dtype, gate_bias):
 @pytest.mark.parametrize("T,E,K,skew", [
     (1, 1, 1, False), (3, 2, 2, False), (127, 8, 2, False), (1000, 8, 2, True),
     (1000, 128, 8, True), (2049, 256, 8, False), (4096, 64, 8, False), (33, 4, 4, False),
+    # more tokens than the one-launch dispatch has warps (several tokens per
+    # warp in the row scatter), and more chunks than warps
+    (40000, 16, 4, True), (320000, 8, 2, False),
 ])
 def test_permute_maps_bit_exact(T, E, K, skew):
     M = lib()
