@@ -23,11 +23,13 @@ Sources (page title, then section / equation):
 * "emerging-techniques-moe-training" skill page, "Basic MoE Architecture"
   (MoELayer.forward: softmax -> topk -> divide by the top-k sum -> masked
   per-expert loop with output[mask] += score * expert(x[mask])), "Top-1
-  Routing (Switch Transformer)" (argmax), and "Mixtral 8x7B Architecture"
-  (index_add_ combine).
+  Routing (Switch Transformer)" (argmax), "Mixtral 8x7B Architecture"
+  (index_add_ combine), and "Load Balancing" (the auxiliary loss and the
+  router z-loss).
 * "Mixture-of-Experts from Architecture to Large-Scale Training", "Keep the
   Dense reference baseline" (one expert with top-1 routing is the dense FFN;
-  the router weight then gets no gradient) and "Calculation of activated
+  the router weight then gets no gradient; its load-balance loss is exactly
+  1) and "Calculation of activated
   parameters and total parameters" (a bias-free SwiGLU expert holds three
   h x F matrices).
 
@@ -47,6 +49,10 @@ Readings where the pages are silent (each also listed in the design doc):
 * GELU is the exact erf form; SwiGLU is silu(gate) * up with the gate in the
   first F rows of W1.
 * The shared expert has the routed experts' width, weight 1, and is not routed.
+* Auxiliary loss: the slot fractions count the (token, slot) pairs of the
+  selection (the page's bincount over all expert indices), the gate
+  probabilities are the full softmax of the logits whatever the scoring
+  function, and the fractions carry no gradient.
 
 Parity pins for every function here live in tests/test_oracle_*.py.  The
 backward has no printed values on the pages: it is pinned by central finite
@@ -443,8 +449,10 @@ def router_grad_logits(logits, idx, probs, dprob, score, renorm=True):
 
 def layer_bwd(x, w_r, w1, w2, dy, K, score, act, *, b1=None, b2=None, sel_bias=None,
               gate_bias=None, renorm=True, force_balance=False, w1_shared=None, w2_shared=None,
-              logits_dtype=np.float32, routing=None, weight_grads=True):
-    """Gradients of sum(dy * y) for the layer: returns a dict with dx [T,h],
+              logits_dtype=np.float32, routing=None, weight_grads=True, aux_coeff=0.0,
+              z_coeff=0.0):
+    """Gradients of sum(dy * y) + aux_coeff * aux + z_coeff * z (the two
+    load-balancing losses below) for the layer: returns a dict with dx [T,h],
     dw_r [E,h], dw1, dw2 (and db1, db2 when biased), dw1_shared, dw2_shared,
     dprob [T,K] and dlogits [T,E].  Experts with no tokens get zero gradient.
     The selection bias gets none (it only selects); the gate bias gets
@@ -514,6 +522,10 @@ def layer_bwd(x, w_r, w1, w2, dy, K, score, act, *, b1=None, b2=None, sel_bias=N
         dw1_s = dH.T @ x64 if weight_grads else None
         dx += dH @ w1s
     dl = router_grad_logits(logits, idx, probs, dprob, score, renorm)
+    if aux_coeff:
+        dl = dl + aux_coeff * aux_loss_grad(logits, idx)
+    if z_coeff:
+        dl = dl + z_coeff * z_loss_grad(logits)
     dw_r = dl.T @ x64
     dx += dl @ np.asarray(w_r, np.float64)
     return dict(dx=dx, dw_r=dw_r, db_r=dl.sum(axis=0), dw1=dw1, dw2=dw2, db1=db1, db2=db2,
@@ -551,6 +563,72 @@ def grouped_mlp_bwd(x_perm, offsets, prob_perm, w1, w2, dy_perm):
         dw1[e] = dH.T @ x_perm[r]
         dx[r] = dH @ w1e
     return dict(dx_perm=dx, dw1=dw1, dw2=dw2, dprob_perm=dprob)
+
+
+# ---------------------------------------------------------------------------
+# Load-balancing losses.  Skill page "emerging-techniques-moe-training",
+# "Load Balancing": "Auxiliary Loss" (the fraction of routed slots per expert
+# times the expert's mean gate probability, summed and scaled by the number of
+# experts) and "Router Z-Loss" (mean squared log-sum-exp of the gate logits);
+# the review page's training configuration sets the aux-loss coefficient to
+# 1e-3.  The gate probabilities of the auxiliary loss are the full softmax of
+# the gate logits whatever the scoring function (the page's code applies
+# softmax to the logits).  The slot fractions are counts of a discrete
+# selection: they carry no gradient.
+# ---------------------------------------------------------------------------
+
+def softmax_full(logits):
+    """Row-wise softmax over all E experts, float64."""
+    l = np.asarray(logits, np.float64)
+    m = l.max(axis=1, keepdims=True)
+    e = np.exp(l - m)
+    return e / e.sum(axis=1, keepdims=True)
+
+
+def logsumexp_rows(logits):
+    """log sum_e exp(l_te) per token, float64 (max-shifted)."""
+    l = np.asarray(logits, np.float64)
+    m = l.max(axis=1)
+    return m + np.log(np.exp(l - m[:, None]).sum(axis=1))
+
+
+def slot_fractions(idx, E):
+    """f_e = (number of (t, k) slots routed to e) / (T * K)."""
+    idx = np.asarray(idx, np.int64)
+    return np.bincount(idx.ravel(), minlength=E).astype(np.float64) / idx.size
+
+
+def aux_loss(logits, idx):
+    """aux = E * sum_e f_e P_e with f the slot fractions of the selection idx
+    and P_e = mean over tokens of softmax(l_t)_e."""
+    l = np.asarray(logits, np.float64)
+    E = l.shape[1]
+    f = slot_fractions(idx, E)
+    P = softmax_full(l).mean(axis=0)
+    return float(E * (f * P).sum())
+
+
+def z_loss(logits):
+    """z = mean over tokens of (log sum_e exp l_te)^2."""
+    return float((logsumexp_rows(logits) ** 2).mean())
+
+
+def aux_loss_grad(logits, idx):
+    """d aux / d l [T, E] with f held fixed: with s_t = softmax(l_t),
+    (E / T) s_tj (f_j - sum_e f_e s_te)."""
+    l = np.asarray(logits, np.float64)
+    T, E = l.shape
+    f = slot_fractions(idx, E)
+    s = softmax_full(l)
+    g = s @ f
+    return (E / T) * s * (f[None, :] - g[:, None])
+
+
+def z_loss_grad(logits):
+    """d z / d l [T, E] = (2 / T) lse_t softmax(l_t)_j."""
+    l = np.asarray(logits, np.float64)
+    T = l.shape[0]
+    return (2.0 / T) * logsumexp_rows(l)[:, None] * softmax_full(l)
 
 
 # ---------------------------------------------------------------------------
