@@ -247,6 +247,26 @@ moe_status_t moe_router_bwd(const moe_config_t* cfg, const void* x, const float*
                             float* dl_topk, float* dw_r, float* db_r, float* dx_router, void* ws,
                             size_t ws_bytes, moe_stream_t stream);
 
+/* Load-balancing losses of the router (skill page "emerging-techniques-moe-
+ * training", "Load Balancing": "Auxiliary Loss" and "Router Z-Loss"; the
+ * review page's training configuration weights the auxiliary loss by 1e-3):
+ *   f_e = (slots of topk_idx routed to e) / (T*K)   (no gradient: a count)
+ *   P_e = (1/T) sum_t softmax(l_t)_e                 (full softmax, any scoring)
+ *   losses[0] = aux = E * sum_e f_e P_e
+ *   losses[1] = z   = (1/T) sum_t (logsumexp_e l_te)^2
+ * and, when dlogits is given, adds the weighted gradients in place:
+ *   dlogits[t,j] += aux_coeff * (E/T) s_tj (f_j - sum_e f_e s_te)
+ *                 + z_coeff * (2/T) lse_t s_tj          (s_t = softmax(l_t))
+ *   logits [T,E] f32; topk_idx [T,K] i32 (ids outside [0,E) are reported as
+ *   MOE_ERR_DEVICE_BOUNDS and not counted); losses: 2 f32 (device, out);
+ *   dlogits [T,E] f32 (in/out) or NULL; ws: moe_workspace_size(cfg) bytes.
+ *   Sums in fp64 and in a fixed order: bitwise reproducible.  T = 0 writes
+ *   zero losses. */
+moe_status_t moe_router_aux_loss(const moe_config_t* cfg, const float* logits,
+                                 const int32_t* topk_idx, float aux_coeff, float z_coeff,
+                                 float* losses, float* dlogits, void* ws, size_t ws_bytes,
+                                 moe_stream_t stream);
+
 /* The whole backward layer pass after moe_layer_fwd with MOE_FLAG_SAVE_FOR_BWD
  * on the same workspace and inputs: dy [T,h] -> dx [T,h] (routed experts +
  * shared expert + router), dw_r [E,h] f32, db_r [E] f32 or NULL (gradient of

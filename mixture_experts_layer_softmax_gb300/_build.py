@@ -26,7 +26,8 @@ NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "--expt-relaxed-constexpr
 
 LIBS = {
     "libmoe_gb300.so": ["api.cu", "router.cu", "permute.cu", "combine.cu", "gemm_simt.cu",
-                        "gemm_tc.cu", "gemm_tc2.cu", "gemm_tc_bwd.cu", "bwd.cu", "permute_noalloc.cu"],
+                        "gemm_tc.cu", "gemm_tc2.cu", "gemm_tc_bwd.cu", "bwd.cu", "permute_noalloc.cu",
+                        "aux_loss.cu"],
     "libmoe_synth.so": ["synth.cu"],
 }
 

@@ -25,6 +25,8 @@ cudaError_t launch_expert_gemm_tc(const moe_config_t&, int, int, const void*, co
                                   const float*, const void*, const void*, void*, void*, int, int*,
                                   cudaStream_t);
 cudaError_t launch_bounded_wait_probe(int64_t, int*, cudaStream_t);
+cudaError_t launch_aux_loss(const moe_config_t&, const float*, const int32_t*, float, float, float*,
+                            float*, double*, double*, int32_t*, float*, int*, cudaStream_t);
 cudaError_t launch_tc_dgrad(bool, int, const void*, int, const void*, int, int, const int32_t*,
                             const float*, const void*, void*, float*, int, int*, cudaStream_t);
 cudaError_t launch_tc_wgrad(int, const void*, int, const void*, int, int, const int32_t*, void*,
@@ -467,6 +469,25 @@ moe_status_t moe_router_bwd(const moe_config_t* cfg, const void* x, const float*
     e = launch_bwd_combine(*cfg, nullptr, nullptr, nullptr, dl_topk, topk_idx, w_r, nullptr,
                            dx_router, d->sms, d->status, s);
   return cuda_status(e);
+}
+
+moe_status_t moe_router_aux_loss(const moe_config_t* cfg, const float* logits,
+                                 const int32_t* topk_idx, float aux_coeff, float z_coeff,
+                                 float* losses, float* dlogits, void* ws, size_t ws_bytes,
+                                 moe_stream_t stream) {
+  moe_status_t st = check_config(cfg);
+  if (st != MOE_OK) return st;
+  if (!losses || (cfg->T > 0 && (!logits || !topk_idx))) return MOE_ERR_INVALID_ARG;
+  if (!(aux_coeff == aux_coeff) || !(z_coeff == z_coeff)) return MOE_ERR_INVALID_ARG;  // NaN
+  if ((st = check_ws(cfg, ws, ws_bytes)) != MOE_OK) return st;
+  if (cfg->flags & MOE_FLAG_VALIDATE_ONLY) return MOE_OK;
+  const DeviceInfo* d = device_info();
+  if (!d) return MOE_ERR_CUDA;
+  const Workspace w = workspace_layout(*cfg);
+  return cuda_status(launch_aux_loss(*cfg, logits, topk_idx, aux_coeff, z_coeff, losses, dlogits,
+                                     at<double>(ws, w.aux_part_p), at<double>(ws, w.aux_part_z),
+                                     at<int32_t>(ws, w.aux_part_cnt), at<float>(ws, w.aux_f),
+                                     d->status, static_cast<cudaStream_t>(stream)));
 }
 
 moe_status_t moe_layer_bwd(const moe_config_t* cfg, const void* x, const float* w_r,

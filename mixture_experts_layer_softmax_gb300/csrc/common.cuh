@@ -124,12 +124,19 @@ inline int router_ksplit(const moe_config_t& c, int smax, int sms) {
   return best;
 }
 
+// Blocks of the load-balancing-loss partial sums: about 64 tokens each, at
+// most 512 (their partial rows live in the workspace).
+inline int aux_loss_blocks(int T) {
+  const int64_t nb = ((int64_t)T + 63) / 64;
+  return (int)(nb < 512 ? (nb > 0 ? nb : 1) : 512);
+}
+
 // ---- workspace layout ----------------------------------------------------
 // One layout per config, shared by every entry point, so the backward can find
 // what a SAVE_FOR_BWD forward left behind.
 struct Workspace {
   size_t router_w3, router_parts, router_off, logits, topk_idx, topk_prob, hist, chunk_base,
-      counts, offsets, dst_row, src_token, perm_prob, x_perm, act_save, a, y_perm, shared_off, shared_h, shared_a, shared_y,
+      counts, offsets, dst_row, src_token, perm_prob, aux_part_p, aux_part_z, aux_part_cnt, aux_f, x_perm, act_save, a, y_perm, shared_off, shared_h, shared_a, shared_y,
       // backward (MOE_FLAG_SAVE_FOR_BWD only)
       dy_perm, dh, dx_perm, dprob_part, dprob_perm, dl_topk, dl_perm, shared_dh, shared_dx,
       total;
@@ -166,6 +173,11 @@ inline Workspace workspace_layout(const moe_config_t& c) {
   w.dst_row = take(P * 4);
   w.src_token = take(P * 4);
   w.perm_prob = take(P * 4);
+  const size_t NB = (size_t)aux_loss_blocks(c.T);
+  w.aux_part_p = take(NB * E * 8);
+  w.aux_part_z = take(NB * 8);
+  w.aux_part_cnt = take(NB * E * 4);
+  w.aux_f = take(E * 4);
   w.x_perm = take(P * h * eb);
   w.act_save = take(save ? P * R1 * eb : 0);
   w.a = take(P * F * eb);

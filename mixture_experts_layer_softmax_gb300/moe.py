@@ -63,6 +63,8 @@ _SIG = {
     "moe_grouped_mlp_bwd": (ctypes.c_int, [_CFG] + [_P] * 13 + [ctypes.c_size_t, _P]),
     "moe_router_bwd": (ctypes.c_int, [_CFG] + [_P] * 14 + [ctypes.c_size_t, _P]),
     "moe_layer_bwd": (ctypes.c_int, [_CFG] + [_P] * 15 + [ctypes.c_size_t, _P]),
+    "moe_router_aux_loss": (ctypes.c_int, [_CFG, _P, _P, ctypes.c_float, ctypes.c_float, _P, _P,
+                                           _P, ctypes.c_size_t, _P]),
     "moe_get_error": (ctypes.c_int, [_P]),
     "moe_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "moe_version": (ctypes.c_char_p, []),
@@ -228,6 +230,14 @@ def moe_layer_bwd(cfg, x, w_r, w1, w2, w1_shared, w2_shared, dy, dx, dw_r, db_r,
         ctypes.byref(cfg), _ptr(x), _ptr(w_r), _ptr(w1), _ptr(w2), _ptr(w1_shared),
         _ptr(w2_shared), _ptr(dy), _ptr(dx), _ptr(dw_r), _ptr(db_r), _ptr(dw1), _ptr(dw2),
         _ptr(dw1_shared), _ptr(dw2_shared), wp, wb, _stream(stream)))
+
+
+def moe_router_aux_loss(cfg, logits, topk_idx, aux_coeff, z_coeff, losses, dlogits=None, ws=None,
+                        stream=None):
+    wp, wb = _ws(ws)
+    _check("moe_router_aux_loss", _lib.moe_router_aux_loss(
+        ctypes.byref(cfg), _ptr(logits), _ptr(topk_idx), float(aux_coeff), float(z_coeff),
+        _ptr(losses), _ptr(dlogits), wp, wb, _stream(stream)))
 
 
 def moe_get_error(stream=None) -> int:
