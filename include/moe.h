@@ -95,6 +95,12 @@ typedef struct {
   int32_t has_bias; /* experts carry b1, b2 (GELU only)         */
   int32_t n_shared; /* 0 or 1 always-on shared expert           */
   uint32_t flags;   /* MOE_FLAG_*                               */
+  /* Weights of the router's load-balancing losses (see moe_router_aux_loss)
+   * in the training backward: with either nonzero, moe_layer_fwd also
+   * computes both losses (read them with moe_layer_losses) and moe_layer_bwd
+   * adds their gradient to the router's.  Must be finite; 0 = off. */
+  float aux_loss_coeff;
+  float z_loss_coeff;
 } moe_config_t;
 
 /* Bytes of workspace every call below needs for `cfg` (the same figure for
@@ -266,6 +272,14 @@ moe_status_t moe_router_aux_loss(const moe_config_t* cfg, const float* logits,
                                  const int32_t* topk_idx, float aux_coeff, float z_coeff,
                                  float* losses, float* dlogits, void* ws, size_t ws_bytes,
                                  moe_stream_t stream);
+
+/* The two load-balancing losses of the last moe_layer_fwd on this workspace
+ * (losses[0] = auxiliary loss, losses[1] = z-loss; 2 f32, device, out),
+ * copied on the stream.  Only a forward whose config has a nonzero
+ * aux_loss_coeff or z_loss_coeff computes them: otherwise
+ * MOE_ERR_INVALID_ARG. */
+moe_status_t moe_layer_losses(const moe_config_t* cfg, float* losses, void* ws, size_t ws_bytes,
+                              moe_stream_t stream);
 
 /* The whole backward layer pass after moe_layer_fwd with MOE_FLAG_SAVE_FOR_BWD
  * on the same workspace and inputs: dy [T,h] -> dx [T,h] (routed experts +

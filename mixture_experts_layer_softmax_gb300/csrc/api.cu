@@ -1,6 +1,7 @@
 // The C ABI (include/moe.h): argument validation, workspace carving and the
 // order of the layer's steps.  Host code here only validates and enqueues; it
 // never reads device memory or synchronises (except moe_get_error).
+#include <cmath>
 #include <mutex>
 
 #include "common.cuh"
@@ -37,8 +38,10 @@ cudaError_t launch_router_bwd(const moe_config_t&, const float*, const int32_t*,
 cudaError_t launch_router_wgrad(const moe_config_t&, const void*, const int32_t*, const int32_t*,
                                 const float*, float*, float*, cudaStream_t);
 cudaError_t launch_bwd_combine(const moe_config_t&, const void*, const int32_t*, const void*,
-                               const float*, const int32_t*, const float*, void*, float*, int,
-                               int*, cudaStream_t);
+                               const float*, const int32_t*, const float*, const float*, void*,
+                               float*, int, int*, cudaStream_t);
+cudaError_t launch_router_dense_bwd(const moe_config_t&, const float*, const void*, const float*,
+                                    float*, float*, float*, cudaStream_t);
 }  // namespace moe
 
 using namespace moe;
@@ -94,6 +97,8 @@ moe_status_t check_config(const moe_config_t* c) {
                          MOE_FLAG_GEMM_2CTA;
   if (c->flags & ~known) return MOE_ERR_INVALID_ARG;
   if ((c->flags & MOE_FLAG_GEMM_1CTA) && (c->flags & MOE_FLAG_GEMM_2CTA)) return MOE_ERR_INVALID_ARG;
+  if (!std::isfinite(c->aux_loss_coeff) || !std::isfinite(c->z_loss_coeff))
+    return MOE_ERR_INVALID_ARG;
   if (c->E > 256 || c->K > 16) return MOE_ERR_UNSUPPORTED;
   if (c->act == MOE_ACT_SWIGLU && c->has_bias) return MOE_ERR_UNSUPPORTED;
   const int vec = c->dtype == MOE_BF16 ? 8 : 4;
@@ -370,6 +375,10 @@ moe_status_t moe_layer_fwd(const moe_config_t* cfg, const void* x, const float* 
   // Route
   cudaError_t e = launch_router(c, x, w_r, gate_bias, sel_bias, at<float>(ws, w.logits), idx,
                                 prob, nullptr, router_scratch(c, ws), d->sms, d->status, s);
+  if (e == cudaSuccess && (c.aux_loss_coeff != 0.f || c.z_loss_coeff != 0.f))
+    e = launch_aux_loss(c, at<float>(ws, w.logits), idx, 0.f, 0.f, at<float>(ws, w.aux_losses),
+                        nullptr, at<double>(ws, w.aux_part_p), at<double>(ws, w.aux_part_z),
+                        at<int32_t>(ws, w.aux_part_cnt), at<float>(ws, w.aux_f), d->status, s);
   // Dispatch
   if (e == cudaSuccess)
     e = launch_permute_maps(c, idx, prob, at<int32_t>(ws, w.hist), at<int32_t>(ws, w.chunk_base),
@@ -467,7 +476,7 @@ moe_status_t moe_router_bwd(const moe_config_t* cfg, const void* x, const float*
     e = launch_router_wgrad(*cfg, x, src_token, offsets, dl_perm, dw_r, db_r, s);
   if (e == cudaSuccess && dx_router)
     e = launch_bwd_combine(*cfg, nullptr, nullptr, nullptr, dl_topk, topk_idx, w_r, nullptr,
-                           dx_router, d->sms, d->status, s);
+                           nullptr, dx_router, d->sms, d->status, s);
   return cuda_status(e);
 }
 
@@ -488,6 +497,22 @@ moe_status_t moe_router_aux_loss(const moe_config_t* cfg, const float* logits,
                                      at<double>(ws, w.aux_part_p), at<double>(ws, w.aux_part_z),
                                      at<int32_t>(ws, w.aux_part_cnt), at<float>(ws, w.aux_f),
                                      d->status, static_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_layer_losses(const moe_config_t* cfg, float* losses, void* ws, size_t ws_bytes,
+                              moe_stream_t stream) {
+  moe_status_t st = check_config(cfg);
+  if (st != MOE_OK) return st;
+  if (!losses || (cfg->aux_loss_coeff == 0.f && cfg->z_loss_coeff == 0.f))
+    return MOE_ERR_INVALID_ARG;
+  if ((st = check_ws(cfg, ws, ws_bytes)) != MOE_OK) return st;
+  if (cfg->flags & MOE_FLAG_VALIDATE_ONLY) return MOE_OK;
+  if (cfg->T == 0)
+    return cuda_status(cudaMemsetAsync(losses, 0, 2 * sizeof(float),
+                                       static_cast<cudaStream_t>(stream)));
+  return cuda_status(cudaMemcpyAsync(losses, at<float>(ws, workspace_layout(*cfg).aux_losses),
+                                     2 * sizeof(float), cudaMemcpyDeviceToDevice,
+                                     static_cast<cudaStream_t>(stream)));
 }
 
 moe_status_t moe_layer_bwd(const moe_config_t* cfg, const void* x, const float* w_r,
@@ -551,11 +576,27 @@ moe_status_t moe_layer_bwd(const moe_config_t* cfg, const void* x, const float* 
   if (e == cudaSuccess)
     e = launch_router_wgrad(c, x, at<int32_t>(ws, w.src_token), offsets, at<float>(ws, w.dl_perm),
                             dw_r, db_r, s);
+  // the load-balancing losses: their logit gradient is dense, pushed through
+  // the gating layer by dense products (dW_r += dl^T x, db_r += sum dl,
+  // dx_add = dl W_r)
+  const float* dx_add = nullptr;
+  if (c.aux_loss_coeff != 0.f || c.z_loss_coeff != 0.f) {
+    float* dl_lb = at<float>(ws, w.aux_dl);
+    if (e == cudaSuccess) e = cudaMemsetAsync(dl_lb, 0, sizeof(float) * c.T * c.E, s);
+    if (e == cudaSuccess)
+      e = launch_aux_loss(c, at<float>(ws, w.logits), idx, c.aux_loss_coeff, c.z_loss_coeff,
+                          at<float>(ws, w.aux_losses), dl_lb, at<double>(ws, w.aux_part_p),
+                          at<double>(ws, w.aux_part_z), at<int32_t>(ws, w.aux_part_cnt),
+                          at<float>(ws, w.aux_f), d->status, s);
+    if (e == cudaSuccess)
+      e = launch_router_dense_bwd(c, dl_lb, x, w_r, dw_r, db_r, at<float>(ws, w.aux_dx), s);
+    dx_add = at<float>(ws, w.aux_dx);
+  }
   // dx = routed + shared + router contributions
   if (e == cudaSuccess)
     e = launch_bwd_combine(c, at<void>(ws, w.dx_perm), dst_row,
-                           c.n_shared ? at<void>(ws, w.shared_dx) : nullptr, dl_topk, idx, w_r, dx,
-                           nullptr, d->sms, d->status, s);
+                           c.n_shared ? at<void>(ws, w.shared_dx) : nullptr, dl_topk, idx, w_r,
+                           dx_add, dx, nullptr, d->sms, d->status, s);
   return cuda_status(e);
 }
 

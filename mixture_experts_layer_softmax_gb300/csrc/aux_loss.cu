@@ -217,3 +217,102 @@ cudaError_t launch_aux_loss(const moe_config_t& c, const float* logits, const in
 }
 
 }  // namespace moe
+
+namespace moe {
+
+// ---- dense router backward (for a logit gradient that is nonzero everywhere,
+// like the two losses' gradients): C[m, n] (+)= sum_k A(k, m) B(k, n) in fp32,
+// with A(k, m) = a[k * sak + m * sam] (fp32) and B(k, n) = b[k * ldb + n]
+// (bf16 or fp32 rows).  64 x 128 tiles, 16-deep k chunks staged in shared
+// memory, 256 threads with 4 x 8 outputs each, each output summed in k order
+// by one thread (reproducible).  Used for dW_r += dl^T x (a = dl [T, E]:
+// sak = E, sam = 1) and dx_add = dl W_r (a = dl: sak = 1, sam = E).
+template <typename TB>
+__global__ void __launch_bounds__(256) dense_tn_gemm_kernel(
+    const float* __restrict__ a, int64_t sak, int64_t sam, const TB* __restrict__ b, int64_t ldb,
+    int M, int N, int Kd, float* __restrict__ c, int64_t ldc, bool accumulate,
+    float* __restrict__ colsum) {
+  constexpr int BM = 64, BN = 128, BK = 16;
+  __shared__ float As[BK][BM];
+  __shared__ float Bs[BK][BN + 4];
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;  // 16 x 16 threads
+  const int m0 = blockIdx.y * BM, n0 = blockIdx.x * BN;
+  float acc[4][8] = {};
+  float csum = 0.f;  // block column 0 only: sum over k of A(k, m) for m = m0 + threadIdx.x
+  for (int k0 = 0; k0 < Kd; k0 += BK) {
+    // A tile: 16 x 64 (4 per thread)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int li = threadIdx.x + i * 256;
+      const int kk = li / BM, mm = li % BM;
+      const int k = k0 + kk, m = m0 + mm;
+      As[kk][mm] = (k < Kd && m < M) ? __ldg(a + (int64_t)k * sak + (int64_t)m * sam) : 0.f;
+    }
+    // B tile: 16 x 128 (8 per thread)
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int li = threadIdx.x + i * 256;
+      const int kk = li / BN, nn = li % BN;
+      const int k = k0 + kk, n = n0 + nn;
+      float v = 0.f;
+      if (k < Kd && n < N) v = to_f32(b[(int64_t)k * ldb + n]);
+      Bs[kk][nn] = v;
+    }
+    __syncthreads();
+    if (colsum && blockIdx.x == 0 && threadIdx.x < BM) {
+#pragma unroll
+      for (int kk = 0; kk < BK; ++kk) csum += As[kk][threadIdx.x];
+    }
+#pragma unroll
+    for (int kk = 0; kk < BK; ++kk) {
+      float av[4], bv[8];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) av[i] = As[kk][ty * 4 + i];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) bv[j] = Bs[kk][tx * 8 + j];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int m = m0 + ty * 4 + i;
+    if (m >= M) continue;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int n = n0 + tx * 8 + j;
+      if (n >= N) continue;
+      float* o = c + (int64_t)m * ldc + n;
+      *o = accumulate ? *o + acc[i][j] : acc[i][j];
+    }
+  }
+  if (colsum && blockIdx.x == 0 && threadIdx.x < BM && m0 + threadIdx.x < M)
+    colsum[m0 + threadIdx.x] += csum;
+}
+
+// dW_r [E,h] += dl^T x, db_r [E] += sum_t dl (when given), dx_add [T,h] = dl W_r
+// (when given), for a dense logit gradient dl [T, E] (fp32).
+cudaError_t launch_router_dense_bwd(const moe_config_t& c, const float* dl, const void* x,
+                                    const float* w_r, float* dw_r, float* db_r, float* dx_add,
+                                    cudaStream_t s) {
+  if (c.T == 0) return cudaSuccess;
+  const dim3 gw((unsigned)ceil_div(c.h, 128), (unsigned)ceil_div(c.E, 64));
+  if (c.dtype == MOE_BF16)
+    dense_tn_gemm_kernel<__nv_bfloat16><<<gw, 256, 0, s>>>(
+        dl, c.E, 1, static_cast<const __nv_bfloat16*>(x), c.h, c.E, c.h, c.T, dw_r, c.h, true,
+        db_r);
+  else
+    dense_tn_gemm_kernel<float><<<gw, 256, 0, s>>>(dl, c.E, 1, static_cast<const float*>(x), c.h,
+                                                   c.E, c.h, c.T, dw_r, c.h, true, db_r);
+  if (dx_add) {
+    const dim3 gx((unsigned)ceil_div(c.h, 128), (unsigned)ceil_div(c.T, 64));
+    dense_tn_gemm_kernel<float><<<gx, 256, 0, s>>>(dl, 1, c.E, w_r, c.h, c.T, c.h, c.E, dx_add,
+                                                   c.h, false, nullptr);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace moe

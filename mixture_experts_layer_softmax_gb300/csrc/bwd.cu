@@ -9,6 +9,7 @@
 //   sigmoid, renormalised:  dl_k = s_k (1 - s_k) (dprob_k - sum_j p_j dprob_j) / sum_sel s
 //   dW_r[e] = sum over e's rows r of dl_r x_r,  db_r[e] = sum dl_r  (dl is zero off the selection)
 //   dx[t]   = sum_k dx_perm[dst_row[t,k]] + dx_shared[t] + sum_k dl[t,k] W_r[e_k]
+//             (+ dx_add[t]: the dense router term of the load-balancing losses)
 // Every sum runs in a fixed order: the results are bitwise reproducible.
 #include "common.cuh"
 
@@ -108,8 +109,9 @@ template <typename T, int KMAX>
 __global__ void __launch_bounds__(128) bwd_combine_kernel(
     const T* __restrict__ dx_perm, const int32_t* __restrict__ dst_row,
     const T* __restrict__ dx_shared, const float* __restrict__ dl_topk,
-    const int32_t* __restrict__ idx, const float* __restrict__ w_r, int ntok, int K, int E, int h,
-    T* __restrict__ dx, float* __restrict__ dx_f32, int* status) {
+    const int32_t* __restrict__ idx, const float* __restrict__ w_r,
+    const float* __restrict__ dx_add, int ntok, int K, int E, int h, T* __restrict__ dx,
+    float* __restrict__ dx_f32, int* status) {
   constexpr int V = 8;
   __shared__ int64_t s_src[KMAX];
   __shared__ int64_t s_w[KMAX];
@@ -182,6 +184,12 @@ __global__ void __launch_bounds__(128) bwd_combine_kernel(
           acc[6] = fmaf(d, b.z, acc[6]); acc[7] = fmaf(d, b.w, acc[7]);
         }
     }
+    if (dx_add) {
+      const float4 a = __ldg(reinterpret_cast<const float4*>(dx_add + t * h + c));
+      const float4 b = __ldg(reinterpret_cast<const float4*>(dx_add + t * h + c + 4));
+      acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
+      acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
+    }
     if (dx) {
       if constexpr (sizeof(T) == 2) {
         Vec<T> o;
@@ -234,14 +242,15 @@ template <typename T>
 static cudaError_t bwd_combine_t(const moe_config_t& c, const void* dx_perm,
                                  const int32_t* dst_row, const void* dx_shared,
                                  const float* dl_topk, const int32_t* idx, const float* w_r,
-                                 void* dx, float* dx_f32, int* status, cudaStream_t s) {
+                                 const float* dx_add, void* dx, float* dx_f32, int* status,
+                                 cudaStream_t s) {
   const unsigned grid = (unsigned)c.T;
   const T* dp = static_cast<const T*>(dx_perm);
   const T* ds = static_cast<const T*>(dx_shared);
   T* o = static_cast<T*>(dx);
 #define MOE_BWD_COMBINE(KM)                                                                    \
-  bwd_combine_kernel<T, KM><<<grid, 128, 0, s>>>(dp, dst_row, ds, dl_topk, idx, w_r, c.T, c.K, \
-                                                 c.E, c.h, o, dx_f32, status)
+  bwd_combine_kernel<T, KM><<<grid, 128, 0, s>>>(dp, dst_row, ds, dl_topk, idx, w_r, dx_add,    \
+                                                 c.T, c.K, c.E, c.h, o, dx_f32, status)
   if (c.K <= 2) MOE_BWD_COMBINE(2);
   else if (c.K <= 4) MOE_BWD_COMBINE(4);
   else if (c.K <= 8) MOE_BWD_COMBINE(8);
@@ -252,15 +261,15 @@ static cudaError_t bwd_combine_t(const moe_config_t& c, const void* dx_perm,
 
 cudaError_t launch_bwd_combine(const moe_config_t& c, const void* dx_perm, const int32_t* dst_row,
                                const void* dx_shared, const float* dl_topk, const int32_t* idx,
-                               const float* w_r, void* dx, float* dx_f32, int sms, int* status,
-                               cudaStream_t s) {
+                               const float* w_r, const float* dx_add, void* dx, float* dx_f32,
+                               int sms, int* status, cudaStream_t s) {
   (void)sms;
   if (c.T == 0) return cudaSuccess;
   if (c.dtype == MOE_BF16)
-    return bwd_combine_t<__nv_bfloat16>(c, dx_perm, dst_row, dx_shared, dl_topk, idx, w_r, dx,
-                                        dx_f32, status, s);
-  return bwd_combine_t<float>(c, dx_perm, dst_row, dx_shared, dl_topk, idx, w_r, dx, dx_f32,
-                              status, s);
+    return bwd_combine_t<__nv_bfloat16>(c, dx_perm, dst_row, dx_shared, dl_topk, idx, w_r, dx_add,
+                                        dx, dx_f32, status, s);
+  return bwd_combine_t<float>(c, dx_perm, dst_row, dx_shared, dl_topk, idx, w_r, dx_add, dx,
+                              dx_f32, status, s);
 }
 
 }  // namespace moe

@@ -136,7 +136,8 @@ inline int aux_loss_blocks(int T) {
 // what a SAVE_FOR_BWD forward left behind.
 struct Workspace {
   size_t router_w3, router_parts, router_off, logits, topk_idx, topk_prob, hist, chunk_base,
-      counts, offsets, dst_row, src_token, perm_prob, aux_part_p, aux_part_z, aux_part_cnt, aux_f, x_perm, act_save, a, y_perm, shared_off, shared_h, shared_a, shared_y,
+      counts, offsets, dst_row, src_token, perm_prob, aux_part_p, aux_part_z, aux_part_cnt, aux_f,
+      aux_losses, aux_dl, aux_dx, x_perm, act_save, a, y_perm, shared_off, shared_h, shared_a, shared_y,
       // backward (MOE_FLAG_SAVE_FOR_BWD only)
       dy_perm, dh, dx_perm, dprob_part, dprob_perm, dl_topk, dl_perm, shared_dh, shared_dx,
       total;
@@ -178,6 +179,10 @@ inline Workspace workspace_layout(const moe_config_t& c) {
   w.aux_part_z = take(NB * 8);
   w.aux_part_cnt = take(NB * E * 4);
   w.aux_f = take(E * 4);
+  const bool lb = c.aux_loss_coeff != 0.f || c.z_loss_coeff != 0.f;
+  w.aux_losses = take(2 * 4);
+  w.aux_dl = take(lb && save ? T * E * 4 : 0);
+  w.aux_dx = take(lb && save ? T * h * 4 : 0);
   w.x_perm = take(P * h * eb);
   w.act_save = take(save ? P * R1 * eb : 0);
   w.a = take(P * F * eb);

@@ -36,7 +36,8 @@ class moe_config_t(ctypes.Structure):
     _fields_ = [("T", ctypes.c_int32), ("h", ctypes.c_int32), ("E", ctypes.c_int32),
                 ("K", ctypes.c_int32), ("F", ctypes.c_int32), ("dtype", ctypes.c_int32),
                 ("score", ctypes.c_int32), ("act", ctypes.c_int32), ("has_bias", ctypes.c_int32),
-                ("n_shared", ctypes.c_int32), ("flags", ctypes.c_uint32)]
+                ("n_shared", ctypes.c_int32), ("flags", ctypes.c_uint32),
+                ("aux_loss_coeff", ctypes.c_float), ("z_loss_coeff", ctypes.c_float)]
 
 
 class MoeError(RuntimeError):
@@ -63,6 +64,7 @@ _SIG = {
     "moe_grouped_mlp_bwd": (ctypes.c_int, [_CFG] + [_P] * 13 + [ctypes.c_size_t, _P]),
     "moe_router_bwd": (ctypes.c_int, [_CFG] + [_P] * 14 + [ctypes.c_size_t, _P]),
     "moe_layer_bwd": (ctypes.c_int, [_CFG] + [_P] * 15 + [ctypes.c_size_t, _P]),
+    "moe_layer_losses": (ctypes.c_int, [_CFG, _P, _P, ctypes.c_size_t, _P]),
     "moe_router_aux_loss": (ctypes.c_int, [_CFG, _P, _P, ctypes.c_float, ctypes.c_float, _P, _P,
                                            _P, ctypes.c_size_t, _P]),
     "moe_get_error": (ctypes.c_int, [_P]),
@@ -113,16 +115,19 @@ def _ws(ws):
 
 
 def make_config(T, h, E, K, F, dtype=MOE_BF16, score=MOE_SCORE_SOFTMAX, act=MOE_ACT_SWIGLU,
-                has_bias=0, n_shared=0, flags=MOE_FLAG_RENORM) -> moe_config_t:
+                has_bias=0, n_shared=0, flags=MOE_FLAG_RENORM, aux_loss_coeff=0.0,
+                z_loss_coeff=0.0) -> moe_config_t:
     return moe_config_t(int(T), int(h), int(E), int(K), int(F), int(dtype), int(score), int(act),
-                        int(has_bias), int(n_shared), int(flags))
+                        int(has_bias), int(n_shared), int(flags), float(aux_loss_coeff),
+                        float(z_loss_coeff))
 
 
-def config_for(w, flags_extra=0) -> moe_config_t:
+def config_for(w, flags_extra=0, aux_loss_coeff=0.0, z_loss_coeff=0.0) -> moe_config_t:
     """moe_config_t of a workloads.Workload."""
     flags = (MOE_FLAG_RENORM if w.renorm else 0) | (MOE_FLAG_FORCE_BALANCE if w.force_balance else 0)
     return make_config(w.T, w.h, w.E, w.K, w.F, MOE_BF16 if w.dtype == "bf16" else MOE_F32,
-                       w.score, w.act, int(w.has_bias), w.n_shared, flags | flags_extra)
+                       w.score, w.act, int(w.has_bias), w.n_shared, flags | flags_extra,
+                       aux_loss_coeff, z_loss_coeff)
 
 
 # ---- entry points -------------------------------------------------------------
@@ -238,6 +243,12 @@ def moe_router_aux_loss(cfg, logits, topk_idx, aux_coeff, z_coeff, losses, dlogi
     _check("moe_router_aux_loss", _lib.moe_router_aux_loss(
         ctypes.byref(cfg), _ptr(logits), _ptr(topk_idx), float(aux_coeff), float(z_coeff),
         _ptr(losses), _ptr(dlogits), wp, wb, _stream(stream)))
+
+
+def moe_layer_losses(cfg, losses, ws, stream=None):
+    wp, wb = _ws(ws)
+    _check("moe_layer_losses", _lib.moe_layer_losses(ctypes.byref(cfg), _ptr(losses), wp, wb,
+                                                     _stream(stream)))
 
 
 def moe_get_error(stream=None) -> int:

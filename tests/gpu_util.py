@@ -92,9 +92,9 @@ class Layer:
             return np.full(w.T, np.inf)
         return O.selection_margin(logits, w.K, w.score, self.h.get("sel_bias"))
 
-    def run_fwd(self, M, flags_extra=0, ws=None):
+    def run_fwd(self, M, flags_extra=0, ws=None, cfg=None):
         w = self.w
-        cfg = M.config_for(w, flags_extra)
+        cfg = cfg if cfg is not None else M.config_for(w, flags_extra)
         if ws is None:
             ws = torch.empty(M.moe_workspace_size(cfg), dtype=torch.uint8, device="cuda")
         y = torch.empty(w.T, w.h, dtype=torch.bfloat16 if w.dtype == "bf16" else torch.float32,

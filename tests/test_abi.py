@@ -52,6 +52,7 @@ def _cfg(M, **kw):
     (dict(K=9), 1), (dict(T=-1), 1), (dict(h=0), 1), (dict(dtype=7), 1), (dict(flags=1 << 20), 1),
     (dict(E=300, K=2), 2), (dict(K=17, E=64), 2), (dict(h=100), 2), (dict(F=20), 2),
     (dict(act=1, has_bias=1), 2), (dict(n_shared=2), 1),
+    (dict(aux_loss_coeff=float("nan")), 1), (dict(z_loss_coeff=float("inf")), 1),
 ])
 def test_config_rejections(M, kw, status):
     cfg = _cfg(M, **kw)

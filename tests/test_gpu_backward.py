@@ -73,11 +73,11 @@ def _bwd_workloads():
     ]
 
 
-def _run_layer_bwd(M, L):
+def _run_layer_bwd(M, L, ca=0.0, cz=0.0):
     w = L.w
-    cfg = M.config_for(w, M.MOE_FLAG_SAVE_FOR_BWD)
+    cfg = M.config_for(w, M.MOE_FLAG_SAVE_FOR_BWD, ca, cz)
     ws = torch.empty(M.moe_workspace_size(cfg), dtype=torch.uint8, device="cuda")
-    y, idx, prob, _ = L.run_fwd(M, flags_extra=M.MOE_FLAG_SAVE_FOR_BWD, ws=ws)
+    y, idx, prob, _ = L.run_fwd(M, ws=ws, cfg=cfg)
     bf = dict(dtype=torch.bfloat16, device="cuda")
     g = L.get
     out = dict(dx=torch.full((w.T, w.h), float("nan"), **bf),
@@ -93,6 +93,10 @@ def _run_layer_bwd(M, L):
                     out.get("dw1_shared"), out.get("dw2_shared"), ws)
     torch.cuda.synchronize()
     assert M.moe_get_error() == M.MOE_OK
+    if ca or cz:
+        out["losses"] = torch.full((2,), float("nan"), device="cuda")
+        M.moe_layer_losses(cfg, out["losses"], ws)
+        torch.cuda.synchronize()
     return idx, out
 
 
@@ -158,3 +162,37 @@ def test_router_backward_matches_oracle(score):
                       (dxr, dl_ref @ w_r.astype(np.float64))):
         ok, err, bound = tol_ok(to_np(got), want, "f32")
         assert ok, (err, bound)
+
+
+@pytest.mark.parametrize("w", _bwd_workloads()[:3], ids=lambda w: w.name)
+def test_layer_backward_with_load_balancing_losses(w):
+    """With both loss weights set (scaled with T so their dense logit gradient
+    is comparable to the routed one), dx, dW_r and db_r match the oracle's
+    gradient of sum(dy * y) + a * aux + c * z, the losses match at 1e-4, and
+    the change the weights make to dW_r and db_r matches the oracle's at fp32
+    accuracy."""
+    M = lib()
+    L = Layer(w)
+    ca, cz = 10.0 * w.T, 1.0 * w.T
+    idx0, out0 = _run_layer_bwd(M, L)
+    idx, out = _run_layer_bwd(M, L, ca, cz)
+    h = L.h
+    kw = dict(sel_bias=h.get("sel_bias"), gate_bias=h.get("gate_bias"), renorm=w.renorm,
+              force_balance=w.force_balance, w1_shared=h.get("w1_shared"),
+              w2_shared=h.get("w2_shared"))
+    ref = O.layer_bwd(h["x"], h["w_r"], h["w1"], h["w2"], h["dy"], w.K, w.score, w.act,
+                      aux_coeff=ca, z_coeff=cz, **kw)
+    np.testing.assert_array_equal(to_np(idx), ref["idx"])
+    for name in ("dx", "dw_r", "db_r"):
+        ok, err, bound = tol_ok(to_np(out[name]), ref[name], "bf16")
+        assert ok, (name, err, bound)
+    losses = to_np(out["losses"])
+    aux, z = O.aux_loss(ref["logits"], ref["idx"]), O.z_loss(ref["logits"])
+    assert abs(losses[0] - aux) <= 1e-4 * aux and abs(losses[1] - z) <= 1e-4 * z, (losses, aux, z)
+    dl = ca * O.aux_loss_grad(ref["logits"], ref["idx"]) + cz * O.z_loss_grad(ref["logits"])
+    x64 = h["x"].astype(np.float64)
+    for name, want in (("dw_r", dl.T @ x64), ("db_r", dl.sum(axis=0))):
+        got = to_np(out[name]).astype(np.float64) - to_np(out0[name]).astype(np.float64)
+        slack = 2.0 ** -23 * float(np.abs(to_np(out[name])).max())
+        ok, err, bound = tol_ok(got, want, "f32")
+        assert err <= bound + slack, (name, err, bound, slack)
