@@ -25,7 +25,7 @@ Sources (page title, then section / equation):
   per-expert loop with output[mask] += score * expert(x[mask])), "Top-1
   Routing (Switch Transformer)" (argmax), "Mixtral 8x7B Architecture"
   (index_add_ combine), and "Load Balancing" (the auxiliary loss and the
-  router z-loss).
+  router z-loss), "Capacity Factor Tuning" (expert capacity and dropping).
 * "Mixture-of-Experts from Architecture to Large-Scale Training", "Keep the
   Dense reference baseline" (one expert with top-1 routing is the dense FFN;
   the router weight then gets no gradient; its load-balance loss is exactly
@@ -49,6 +49,12 @@ Readings where the pages are silent (each also listed in the design doc):
 * GELU is the exact erf form; SwiGLU is silu(gate) * up with the gate in the
   first F rows of W1.
 * The shared expert has the routed experts' width, weight 1, and is not routed.
+* Expert capacity: counted in (token, slot) pairs, floor(cf * T * K / E) (the
+  skill page's int(tokens / experts * capacity_factor) with top-K slots); each
+  expert keeps its first C slots in ascending token order and drops the rest;
+  the kept weights are not renormalised, and a dropped slot still takes part
+  in the router's normalisation (its weight gets a gradient through the kept
+  ones).
 * Auxiliary loss: the slot fractions count the (token, slot) pairs of the
   selection (the page's bincount over all expert indices), the gate
   probabilities are the full softmax of the logits whatever the scoring
@@ -213,30 +219,61 @@ def order_margin(logits, K, score, sel_bias=None):
 # Dispatch
 # ---------------------------------------------------------------------------
 
-def dispatch_maps(idx, E):
+def dispatch_maps(idx, E, keep=None):
     """Expert-contiguous permutation of the T*K (token, slot) pairs.
 
     counts[e]  = number of pairs routed to expert e
     offsets    = exclusive prefix sum of counts (E+1 entries)
     dst_row[t,k] = offsets[e] + #{t' < t : e selected by t'}   (e = idx[t,k])
     src_token[r], src_slot[r]: the inverse map.
+    With keep (capacity_keep), only the kept pairs are counted and placed;
+    dropped pairs get dst_row = -1.
     Built the plainest way: expert by expert, tokens ascending.
     """
     idx = np.asarray(idx, np.int64)
     T, K = idx.shape
-    counts = np.array([np.count_nonzero(idx == e) for e in range(E)], dtype=np.int64)
+    if keep is None:
+        keep = np.ones((T, K), bool)
+    keep = np.asarray(keep, bool)
+    counts = np.array([np.count_nonzero((idx == e) & keep) for e in range(E)], dtype=np.int64)
     offsets = np.zeros(E + 1, dtype=np.int64)
     offsets[1:] = np.cumsum(counts)
     dst_row = np.full((T, K), -1, dtype=np.int64)
     src_token = np.full(T * K, -1, dtype=np.int64)
     src_slot = np.full(T * K, -1, dtype=np.int64)
     for e in range(E):
-        t_list, k_list = np.nonzero(idx == e)  # row-major: ascending token
+        t_list, k_list = np.nonzero((idx == e) & keep)  # row-major: ascending token
         rows = offsets[e] + np.arange(t_list.size)
         dst_row[t_list, k_list] = rows
         src_token[rows] = t_list
         src_slot[rows] = k_list
     return counts, offsets, dst_row, src_token, src_slot
+
+
+def expert_capacity(T, K, E, capacity_factor, min_capacity=0):
+    """Slots an expert may take: floor(capacity_factor * T * K / E), at least
+    min_capacity (skill page, "Capacity Factor Tuning": expert_capacity =
+    int(tokens / num_experts * capacity_factor), counted in (token, slot)
+    pairs for top-K routing; the DeepSpeed config there also names
+    min_capacity)."""
+    return max(int(min_capacity), int(math.floor(capacity_factor * T * K / E)))
+
+
+def capacity_keep(idx, E, capacity):
+    """keep[t, k]: whether slot (t, k) is within its expert's capacity -- the
+    expert keeps its first `capacity` slots in ascending token order and drops
+    the rest ("drop_tokens": tokens exceeding capacity are dropped).  Built the
+    plainest way: walk the tokens in order with one counter per expert."""
+    idx = np.asarray(idx, np.int64)
+    T, K = idx.shape
+    seen = np.zeros(E, np.int64)
+    keep = np.zeros((T, K), bool)
+    for t in range(T):
+        for k in range(K):
+            e = idx[t, k]
+            keep[t, k] = seen[e] < capacity
+            seen[e] += 1
+    return keep
 
 
 def permute_rows(x, src_token):
@@ -324,9 +361,11 @@ def _bias_row(b, e):
 
 def layer_fwd(x, w_r, w1, w2, K, score, act, *, b1=None, b2=None, sel_bias=None,
               gate_bias=None, renorm=True, force_balance=False, w1_shared=None, w2_shared=None,
-              logits_dtype=np.float32, tokens=None, routing=None):
+              logits_dtype=np.float32, tokens=None, routing=None, capacity=None):
     """The MoE layer output y[t] = sum_k p[t,k] E_{idx[t,k]}(x_t) + S(x_t),
-    float64 (review §1.1 MoE(x); §2.1 the four stages).
+    float64 (review §1.1 MoE(x); §2.1 the four stages).  With a capacity,
+    the sum runs over the kept slots only (capacity_keep); the kept weights
+    are not renormalised.
 
     Expert outputs are computed expert by expert over the permuted rows
     (Dispatch, then one FFN per expert, then Combine).  ``tokens`` restricts
@@ -342,7 +381,8 @@ def layer_fwd(x, w_r, w1, w2, K, score, act, *, b1=None, b2=None, sel_bias=None,
         idx, probs = route(logits, K, score, renorm, sel_bias, force_balance)
     else:
         logits, idx, probs = routing
-    counts, offsets, dst_row, src_token, src_slot = dispatch_maps(idx, E)
+    keep = None if capacity is None else capacity_keep(idx, E, capacity)
+    counts, offsets, dst_row, src_token, src_slot = dispatch_maps(idx, E, keep)
     if tokens is None:
         tokens = np.arange(T)
     tokens = np.asarray(tokens, np.int64)
@@ -362,24 +402,35 @@ def layer_fwd(x, w_r, w1, w2, K, score, act, *, b1=None, b2=None, sel_bias=None,
         y[tokens] += expert_ffn(x[tokens], w1_shared, w2_shared, act)
     return dict(logits=logits, idx=idx, probs=probs, counts=counts, offsets=offsets,
                 dst_row=dst_row, src_token=src_token, src_slot=src_slot,
-                y=y[tokens], tokens=tokens)
+                y=y[tokens], tokens=tokens, keep=keep)
 
 
 def layer_fwd_masked_dense(x, w_r, w1, w2, K, score, act, *, b1=None, b2=None,
                            sel_bias=None, gate_bias=None, renorm=True, force_balance=False,
-                           w1_shared=None, w2_shared=None, logits_dtype=np.float32):
+                           w1_shared=None, w2_shared=None, logits_dtype=np.float32,
+                           capacity=None):
     """Second formulation, no permutation: loop over the K slots and over the
     experts with a boolean mask and accumulate score * expert(x[mask]) (the
-    skill page's MoELayer.forward loop).  For small cases only."""
+    skill page's MoELayer.forward loop).  A capacity is applied the other way
+    round from capacity_keep: a slot's position inside its expert is the
+    running count of the token-major routing mask (a cumulative sum), and the
+    slot is kept when that position is below the capacity.  For small cases
+    only."""
     x = np.asarray(x)
     T, h = x.shape
     E = np.asarray(w_r).shape[0]
     logits = gating_logits(x, w_r, gate_bias, logits_dtype)
     idx, probs = route(logits, K, score, renorm, sel_bias, force_balance)
+    kept = np.ones((T, K), bool)
+    if capacity is not None:
+        onehot = np.zeros((T * K, E), np.int64)
+        onehot[np.arange(T * K), np.asarray(idx, np.int64).reshape(-1)] = 1
+        position = (np.cumsum(onehot, axis=0) - onehot)[np.arange(T * K), idx.reshape(-1)]
+        kept = (position < capacity).reshape(T, K)
     y = np.zeros((T, h), np.float64)
     for k in range(K):
         for e in range(E):
-            mask = idx[:, k] == e
+            mask = (idx[:, k] == e) & kept[:, k]
             if not mask.any():
                 continue
             out = expert_ffn(x[mask], w1[e], w2[e], act, _bias_row(b1, e), _bias_row(b2, e))
@@ -450,7 +501,7 @@ def router_grad_logits(logits, idx, probs, dprob, score, renorm=True):
 def layer_bwd(x, w_r, w1, w2, dy, K, score, act, *, b1=None, b2=None, sel_bias=None,
               gate_bias=None, renorm=True, force_balance=False, w1_shared=None, w2_shared=None,
               logits_dtype=np.float32, routing=None, weight_grads=True, aux_coeff=0.0,
-              z_coeff=0.0):
+              z_coeff=0.0, capacity=None):
     """Gradients of sum(dy * y) + aux_coeff * aux + z_coeff * z (the two
     load-balancing losses below) for the layer: returns a dict with dx [T,h],
     dw_r [E,h], dw1, dw2 (and db1, db2 when biased), dw1_shared, dw2_shared,
@@ -467,7 +518,8 @@ def layer_bwd(x, w_r, w1, w2, dy, K, score, act, *, b1=None, b2=None, sel_bias=N
         idx, probs = route(logits, K, score, renorm, sel_bias, force_balance)
     else:
         logits, idx, probs = routing
-    counts, offsets, dst_row, src_token, src_slot = dispatch_maps(idx, E)
+    keep = None if capacity is None else capacity_keep(idx, E, capacity)
+    counts, offsets, dst_row, src_token, src_slot = dispatch_maps(idx, E, keep)
     dx = np.zeros((T, h), np.float64)
     dprob = np.zeros(idx.shape, np.float64)
     dw1 = dw2 = None
