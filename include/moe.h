@@ -101,7 +101,21 @@ typedef struct {
    * adds their gradient to the router's.  Must be finite; 0 = off. */
   float aux_loss_coeff;
   float z_loss_coeff;
+  /* Expert capacity in (token, slot) pairs (skill page "emerging-techniques-
+   * moe-training", "Capacity Factor Tuning"; see moe_expert_capacity): each
+   * expert keeps its first `capacity` slots in ascending token order and
+   * drops the rest (their dst_row is -1; they add nothing to y; the kept
+   * weights are not renormalised).  0 = dropless. */
+  int32_t capacity;
 } moe_config_t;
+
+/* floor(capacity_factor * T * K / E), at least min_capacity: the capacity of
+ * the skill page's formula, int(tokens / experts * capacity_factor), counted
+ * in top-K slots.  Host-only arithmetic; -1 if an argument is out of range
+ * (T < 0, K < 1, E < 1, capacity_factor not finite and > 0) or the result
+ * does not fit an int32. */
+int32_t moe_expert_capacity(int32_t T, int32_t K, int32_t E, float capacity_factor,
+                            int32_t min_capacity);
 
 /* Bytes of workspace every call below needs for `cfg` (the same figure for
  * all of them; it grows with MOE_FLAG_SAVE_FOR_BWD).  0 if cfg is invalid. */
@@ -245,7 +259,8 @@ moe_status_t moe_grouped_mlp_bwd(const moe_config_t* cfg, const void* dy_perm, c
  * optionally dx_router[t] = sum_k dl_k W_r[e_k] (fp32 [T,h]).
  *   x [T,h]; logits [T,E]; topk_idx/topk_prob [T,K]; offsets, dst_row, src_token
  *   from moe_permute; outputs dl_topk [T,K], dw_r [E,h], db_r [E] or NULL,
- *   dx_router or NULL (then w_r may be NULL). */
+ *   dx_router or NULL (then w_r may be NULL).  Dropless configs only
+ *   (capacity 0, else MOE_ERR_UNSUPPORTED: moe_layer_bwd covers capacity). */
 moe_status_t moe_router_bwd(const moe_config_t* cfg, const void* x, const float* logits,
                             const int32_t* topk_idx, const float* topk_prob,
                             const int32_t* offsets, const int32_t* dst_row,

@@ -40,8 +40,12 @@ cudaError_t launch_router_wgrad(const moe_config_t&, const void*, const int32_t*
 cudaError_t launch_bwd_combine(const moe_config_t&, const void*, const int32_t*, const void*,
                                const float*, const int32_t*, const float*, const float*, void*,
                                float*, int, int*, cudaStream_t);
-cudaError_t launch_router_dense_bwd(const moe_config_t&, const float*, const void*, const float*,
-                                    float*, float*, float*, cudaStream_t);
+cudaError_t launch_scatter_topk_grad(const moe_config_t&, const float*, const int32_t*, float*,
+                                     cudaStream_t);
+cudaError_t launch_dense_router_wgrad(const moe_config_t&, const float*, const void*, float*,
+                                      float*, cudaStream_t);
+cudaError_t launch_dense_router_dx(const moe_config_t&, const float*, const float*, float*,
+                                   cudaStream_t);
 }  // namespace moe
 
 using namespace moe;
@@ -99,6 +103,7 @@ moe_status_t check_config(const moe_config_t* c) {
   if ((c->flags & MOE_FLAG_GEMM_1CTA) && (c->flags & MOE_FLAG_GEMM_2CTA)) return MOE_ERR_INVALID_ARG;
   if (!std::isfinite(c->aux_loss_coeff) || !std::isfinite(c->z_loss_coeff))
     return MOE_ERR_INVALID_ARG;
+  if (c->capacity < 0) return MOE_ERR_INVALID_ARG;
   if (c->E > 256 || c->K > 16) return MOE_ERR_UNSUPPORTED;
   if (c->act == MOE_ACT_SWIGLU && c->has_bias) return MOE_ERR_UNSUPPORTED;
   const int vec = c->dtype == MOE_BF16 ? 8 : 4;
@@ -208,6 +213,16 @@ int* device_status_word() {
 }  // namespace moe
 
 extern "C" {
+
+int32_t moe_expert_capacity(int32_t T, int32_t K, int32_t E, float capacity_factor,
+                            int32_t min_capacity) {
+  if (T < 0 || K < 1 || E < 1 || !std::isfinite(capacity_factor) || capacity_factor <= 0.f)
+    return -1;
+  const double c = std::floor((double)capacity_factor * (double)T * (double)K / (double)E);
+  const double m = c > (double)min_capacity ? c : (double)min_capacity;
+  if (m > 2147483647.0) return -1;
+  return (int32_t)m;
+}
 
 size_t moe_workspace_size(const moe_config_t* cfg) {
   if (check_config(cfg) != MOE_OK) return 0;
@@ -455,6 +470,9 @@ moe_status_t moe_router_bwd(const moe_config_t* cfg, const void* x, const float*
                             size_t ws_bytes, moe_stream_t stream) {
   moe_status_t st = check_config(cfg);
   if (st != MOE_OK) return st;
+  // with an expert capacity, dropped slots get a router gradient but have no
+  // permuted row for the segmented dW_r sum: moe_layer_bwd handles them
+  if (cfg->capacity > 0) return MOE_ERR_UNSUPPORTED;
   if ((st = check_bwd_support(*cfg)) != MOE_OK) return st;
   if (cfg->T > 0 && (!x || !logits || !topk_idx || !topk_prob || !offsets || !dst_row ||
                      !src_token || !dprob_perm || !dl_topk || !dw_r))
@@ -573,24 +591,33 @@ moe_status_t moe_layer_bwd(const moe_config_t* cfg, const void* x, const float* 
     e = launch_router_bwd(c, at<float>(ws, w.logits), idx, at<float>(ws, w.topk_prob), dst_row,
                           at<float>(ws, w.dprob_perm), dl_topk, at<float>(ws, w.dl_perm),
                           d->status, s);
-  if (e == cudaSuccess)
-    e = launch_router_wgrad(c, x, at<int32_t>(ws, w.src_token), offsets, at<float>(ws, w.dl_perm),
-                            dw_r, db_r, s);
-  // the load-balancing losses: their logit gradient is dense, pushed through
-  // the gating layer by dense products (dW_r += dl^T x, db_r += sum dl,
-  // dx_add = dl W_r)
+  // Router weight gradient.  Dropless without load-balancing losses: a
+  // segmented sum over each expert's permuted rows.  Otherwise the logit
+  // gradient is dense or reaches dropped slots that have no permuted row, so
+  // it is gathered into a dense [T, E] matrix and pushed through the gating
+  // layer by dense products: the losses' part first goes to dx (dx_add = dl
+  // W_r; the routed part reaches dx through the combine below), then the
+  // routed slots are added and dW_r = dl^T x, db_r = sum_t dl.
+  const bool lb = c.aux_loss_coeff != 0.f || c.z_loss_coeff != 0.f;
   const float* dx_add = nullptr;
-  if (c.aux_loss_coeff != 0.f || c.z_loss_coeff != 0.f) {
-    float* dl_lb = at<float>(ws, w.aux_dl);
-    if (e == cudaSuccess) e = cudaMemsetAsync(dl_lb, 0, sizeof(float) * c.T * c.E, s);
+  if (!lb && c.capacity == 0) {
     if (e == cudaSuccess)
-      e = launch_aux_loss(c, at<float>(ws, w.logits), idx, c.aux_loss_coeff, c.z_loss_coeff,
-                          at<float>(ws, w.aux_losses), dl_lb, at<double>(ws, w.aux_part_p),
-                          at<double>(ws, w.aux_part_z), at<int32_t>(ws, w.aux_part_cnt),
-                          at<float>(ws, w.aux_f), d->status, s);
-    if (e == cudaSuccess)
-      e = launch_router_dense_bwd(c, dl_lb, x, w_r, dw_r, db_r, at<float>(ws, w.aux_dx), s);
-    dx_add = at<float>(ws, w.aux_dx);
+      e = launch_router_wgrad(c, x, at<int32_t>(ws, w.src_token), offsets,
+                              at<float>(ws, w.dl_perm), dw_r, db_r, s);
+  } else {
+    float* dl_dense = at<float>(ws, w.aux_dl);
+    if (e == cudaSuccess) e = cudaMemsetAsync(dl_dense, 0, sizeof(float) * c.T * c.E, s);
+    if (lb) {
+      if (e == cudaSuccess)
+        e = launch_aux_loss(c, at<float>(ws, w.logits), idx, c.aux_loss_coeff, c.z_loss_coeff,
+                            at<float>(ws, w.aux_losses), dl_dense, at<double>(ws, w.aux_part_p),
+                            at<double>(ws, w.aux_part_z), at<int32_t>(ws, w.aux_part_cnt),
+                            at<float>(ws, w.aux_f), d->status, s);
+      if (e == cudaSuccess) e = launch_dense_router_dx(c, dl_dense, w_r, at<float>(ws, w.aux_dx), s);
+      dx_add = at<float>(ws, w.aux_dx);
+    }
+    if (e == cudaSuccess) e = launch_scatter_topk_grad(c, dl_topk, idx, dl_dense, s);
+    if (e == cudaSuccess) e = launch_dense_router_wgrad(c, dl_dense, x, dw_r, db_r, s);
   }
   // dx = routed + shared + router contributions
   if (e == cudaSuccess)

@@ -225,8 +225,9 @@ namespace moe {
 // with A(k, m) = a[k * sak + m * sam] (fp32) and B(k, n) = b[k * ldb + n]
 // (bf16 or fp32 rows).  64 x 128 tiles, 16-deep k chunks staged in shared
 // memory, 256 threads with 4 x 8 outputs each, each output summed in k order
-// by one thread (reproducible).  Used for dW_r += dl^T x (a = dl [T, E]:
-// sak = E, sam = 1) and dx_add = dl W_r (a = dl: sak = 1, sam = E).
+// by one thread (reproducible).  Used for dW_r = dl^T x (a = dl [T, E]:
+// sak = E, sam = 1; colsum = db_r, the sums over k of A(k, m)) and
+// dx_add = dl W_r (a = dl: sak = 1, sam = E).
 template <typename TB>
 __global__ void __launch_bounds__(256) dense_tn_gemm_kernel(
     const float* __restrict__ a, int64_t sak, int64_t sam, const TB* __restrict__ b, int64_t ldb,
@@ -289,29 +290,55 @@ __global__ void __launch_bounds__(256) dense_tn_gemm_kernel(
       *o = accumulate ? *o + acc[i][j] : acc[i][j];
     }
   }
-  if (colsum && blockIdx.x == 0 && threadIdx.x < BM && m0 + threadIdx.x < M)
-    colsum[m0 + threadIdx.x] += csum;
+  if (colsum && blockIdx.x == 0 && threadIdx.x < BM && m0 + threadIdx.x < M) {
+    float* o = colsum + m0 + threadIdx.x;
+    *o = accumulate ? *o + csum : csum;
+  }
 }
 
-// dW_r [E,h] += dl^T x, db_r [E] += sum_t dl (when given), dx_add [T,h] = dl W_r
-// (when given), for a dense logit gradient dl [T, E] (fp32).
-cudaError_t launch_router_dense_bwd(const moe_config_t& c, const float* dl, const void* x,
-                                    const float* w_r, float* dw_r, float* db_r, float* dx_add,
-                                    cudaStream_t s) {
+// Adds the routed slots' logit gradient dl_topk [T, K] into the dense [T, E]
+// one (the K experts of a token are distinct: one thread per element).
+__global__ void scatter_topk_grad_kernel(const float* __restrict__ dl_topk,
+                                         const int32_t* __restrict__ idx, int T, int K, int E,
+                                         float* __restrict__ dl) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= (int64_t)T * K) return;
+  const int e = __ldg(idx + i);
+  if (e >= 0 && e < E) dl[(i / K) * E + e] += __ldg(dl_topk + i);
+}
+
+cudaError_t launch_scatter_topk_grad(const moe_config_t& c, const float* dl_topk,
+                                     const int32_t* idx, float* dl, cudaStream_t s) {
+  const int64_t n = (int64_t)c.T * c.K;
+  if (n == 0) return cudaSuccess;
+  scatter_topk_grad_kernel<<<(unsigned)ceil_div(n, 256), 256, 0, s>>>(dl_topk, idx, c.T, c.K, c.E,
+                                                                      dl);
+  return cudaGetLastError();
+}
+
+// dW_r [E,h] = dl^T x and db_r [E] = sum_t dl (when given) for a dense logit
+// gradient dl [T, E] (fp32); both written, not accumulated.
+cudaError_t launch_dense_router_wgrad(const moe_config_t& c, const float* dl, const void* x,
+                                      float* dw_r, float* db_r, cudaStream_t s) {
   if (c.T == 0) return cudaSuccess;
   const dim3 gw((unsigned)ceil_div(c.h, 128), (unsigned)ceil_div(c.E, 64));
   if (c.dtype == MOE_BF16)
     dense_tn_gemm_kernel<__nv_bfloat16><<<gw, 256, 0, s>>>(
-        dl, c.E, 1, static_cast<const __nv_bfloat16*>(x), c.h, c.E, c.h, c.T, dw_r, c.h, true,
+        dl, c.E, 1, static_cast<const __nv_bfloat16*>(x), c.h, c.E, c.h, c.T, dw_r, c.h, false,
         db_r);
   else
     dense_tn_gemm_kernel<float><<<gw, 256, 0, s>>>(dl, c.E, 1, static_cast<const float*>(x), c.h,
-                                                   c.E, c.h, c.T, dw_r, c.h, true, db_r);
-  if (dx_add) {
-    const dim3 gx((unsigned)ceil_div(c.h, 128), (unsigned)ceil_div(c.T, 64));
-    dense_tn_gemm_kernel<float><<<gx, 256, 0, s>>>(dl, 1, c.E, w_r, c.h, c.T, c.h, c.E, dx_add,
-                                                   c.h, false, nullptr);
-  }
+                                                   c.E, c.h, c.T, dw_r, c.h, false, db_r);
+  return cudaGetLastError();
+}
+
+// dx_add [T,h] = dl W_r (written).
+cudaError_t launch_dense_router_dx(const moe_config_t& c, const float* dl, const float* w_r,
+                                   float* dx_add, cudaStream_t s) {
+  if (c.T == 0) return cudaSuccess;
+  const dim3 gx((unsigned)ceil_div(c.h, 128), (unsigned)ceil_div(c.T, 64));
+  dense_tn_gemm_kernel<float><<<gx, 256, 0, s>>>(dl, 1, c.E, w_r, c.h, c.T, c.h, c.E, dx_add, c.h,
+                                                 false, nullptr);
   return cudaGetLastError();
 }
 

@@ -34,17 +34,21 @@ __global__ void __launch_bounds__(256) router_bwd_kernel(
   const int lane = threadIdx.x & 31;
   const int64_t t = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
   if (t >= T) return;
-  const bool act = lane < K;
+  // a slot dropped by the expert capacity (dst_row -1) has no expert output,
+  // so dprob = 0, but its weight still enters the normalisation of the kept
+  // ones and gets a gradient through them
+  bool act = lane < K;
   int r = -1, e = 0;
   float dp = 0.f, p = 0.f, s = 0.f;
   if (act) {
     r = __ldg(dst_row + t * K + lane);
     e = __ldg(idx + t * K + lane);
-    if (r < 0 || r >= P || e < 0 || e >= E) {
+    if (r < -1 || r >= P || e < 0 || e >= E) {
       report(status, MOE_ERR_DEVICE_BOUNDS);
+      act = false;
       r = -1;
     } else {
-      dp = __ldg(dprob_perm + r);
+      dp = r >= 0 ? __ldg(dprob_perm + r) : 0.f;
       p = __ldg(prob + t * K + lane);
       s = sigmoid_f(__ldg(logits + t * E + e));
     }
@@ -55,10 +59,14 @@ __global__ void __launch_bounds__(256) router_bwd_kernel(
     pdp += __shfl_xor_sync(0xffffffffu, pdp, off);
     ssum += __shfl_xor_sync(0xffffffffu, ssum, off);
   }
-  if (!act || r < 0) return;
+  if (lane >= K) return;
+  if (!act) {  // an invalid slot: no gradient
+    dl_topk[t * K + lane] = 0.f;
+    return;
+  }
   const float dl = score == MOE_SCORE_SOFTMAX ? p * (dp - pdp) : s * (1.f - s) * (dp - pdp) / ssum;
   dl_topk[t * K + lane] = dl;
-  dl_perm[r] = dl;
+  if (r >= 0) dl_perm[r] = dl;
 }
 
 // dW_r[e, c..c+8) = sum over expert e's rows of dl_perm[r] * x[src_token[r], c..c+8)
@@ -125,7 +133,10 @@ __global__ void __launch_bounds__(128) bwd_combine_kernel(
     if (k < K) {
       if (dx_perm) {
         const int r = __ldg(dst_row + t * K + k);
-        if (r >= 0 && r < P) src = (int64_t)r * h; else report(status, MOE_ERR_DEVICE_BOUNDS);
+        if (r >= 0 && r < P)
+          src = (int64_t)r * h;
+        else if (r != -1)  // -1: a dropped slot, no expert output to differentiate
+          report(status, MOE_ERR_DEVICE_BOUNDS);
       }
       if (dl_topk) {
         const int e = __ldg(idx + t * K + k);

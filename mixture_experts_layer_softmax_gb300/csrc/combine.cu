@@ -35,7 +35,7 @@ __global__ void __launch_bounds__(128) combine_kernel(const T* __restrict__ y_pe
       if (r >= 0 && r < P) {
         off = (int64_t)r * h;
         wk = w ? __ldg(w + t * K + k) : 1.f;
-      } else {
+      } else if (r != -1) {  // -1: a dropped slot (capacity) or an id reported by dispatch
         report(status, MOE_ERR_DEVICE_BOUNDS);
       }
     }

@@ -181,7 +181,7 @@ inline Workspace workspace_layout(const moe_config_t& c) {
   w.aux_f = take(E * 4);
   const bool lb = c.aux_loss_coeff != 0.f || c.z_loss_coeff != 0.f;
   w.aux_losses = take(2 * 4);
-  w.aux_dl = take(lb && save ? T * E * 4 : 0);
+  w.aux_dl = take((lb || c.capacity > 0) && save ? T * E * 4 : 0);  // dense router gradient
   w.aux_dx = take(lb && save ? T * h * 4 : 0);
   w.x_perm = take(P * h * eb);
   w.act_save = take(save ? P * R1 * eb : 0);

@@ -14,6 +14,10 @@
 //                    dst_row = offsets[e] + base[c][e] + rank inside the chunk
 //                    (ranks from ballots over the lanes' expert ids);
 //                    src_token, perm_prob are the inverse maps.
+//   With an expert capacity C (skill page "emerging-techniques-moe-training",
+//   "Capacity Factor Tuning"), counts[e] = min(slots, C) and a pair whose
+//   position base + rank inside its expert is >= C is dropped (dst_row = -1):
+//   every expert keeps its first C slots in ascending token order.
 //   4. scatter_rows: each token's row is read once and written to its K
 //                    destinations with 16-byte vectors.
 #include "common.cuh"
@@ -43,8 +47,9 @@ MOE_D void hist_chunk(int c, int lane, int32_t* my, const int32_t* __restrict__ 
   __syncwarp();
 }
 
-// Exclusive scan of hist[:, e] over the chunks into base[:, e]; counts[e].
-MOE_D void scan_expert(int e, int lane, const int32_t* __restrict__ hist, int NC, int E,
+// Exclusive scan of hist[:, e] over the chunks into base[:, e]; counts[e] =
+// the slots expert e keeps (all of them, or at most `cap` when cap > 0).
+MOE_D void scan_expert(int e, int lane, const int32_t* __restrict__ hist, int NC, int E, int cap,
                        int32_t* __restrict__ base, int32_t* __restrict__ counts) {
   int running = 0;
   for (int c0 = 0; c0 < NC; c0 += 32) {
@@ -59,7 +64,7 @@ MOE_D void scan_expert(int e, int lane, const int32_t* __restrict__ hist, int NC
     if (c < NC) base[(int64_t)c * E + e] = running + incl - v;
     running += __shfl_sync(0xffffffffu, incl, 31);
   }
-  if (lane == 0) counts[e] = running;
+  if (lane == 0) counts[e] = (cap > 0 && running > cap) ? cap : running;
 }
 
 // Whole block (256 threads): s_off[0..E] = exclusive scan of counts[0..E)
@@ -86,13 +91,15 @@ MOE_D void block_offsets(const int32_t* __restrict__ counts, int E, int32_t* s_o
   if (blockIdx.x == 0 && offsets_out && E == 256 && e == 0) offsets_out[256] = s_off[256];
 }
 
-// Destination rows of chunk c's pairs: dst_row = offsets[e] + base[c][e] +
-// rank of the pair among the chunk's earlier tokens routed to e (from ballots
-// over the lanes' expert-id bits, E <= 256); src_token and perm_prob are the
-// inverse maps.  Expert ids outside [0, E) get dst_row = -1 (reported by the
-// histogram step).
+// Destination rows of chunk c's pairs: the pair's position among expert e's
+// slots is base[c][e] + its rank among the chunk's earlier tokens routed to e
+// (from ballots over the lanes' expert-id bits, E <= 256); dst_row =
+// offsets[e] + position, or -1 when cap > 0 and position >= cap (dropped:
+// beyond the expert's capacity).  src_token and perm_prob are the inverse
+// maps of the kept pairs.  Expert ids outside [0, E) get dst_row = -1
+// (reported by the histogram step).
 MOE_D void ranks_chunk(int c, int lane, const int32_t* __restrict__ idx,
-                       const float* __restrict__ prob, int T, int K, int E,
+                       const float* __restrict__ prob, int T, int K, int E, int cap,
                        const int32_t* __restrict__ base, const int32_t* s_off, int32_t* __restrict__ dst_row,
                        int32_t* __restrict__ src_token, float* __restrict__ perm_prob) {
   const int64_t t = (int64_t)c * kChunk + lane;
@@ -125,7 +132,12 @@ MOE_D void ranks_chunk(int c, int lane, const int32_t* __restrict__ idx,
         dst_row[t * K + k] = -1;
         continue;
       }
-      const int r = s_off[e] + __ldg(base + (int64_t)c * E + e) + rank[k];
+      const int pos = __ldg(base + (int64_t)c * E + e) + rank[k];
+      if (cap > 0 && pos >= cap) {
+        dst_row[t * K + k] = -1;
+        continue;
+      }
+      const int r = s_off[e] + pos;
       dst_row[t * K + k] = r;
       src_token[r] = (int32_t)t;
       if (perm_prob) perm_prob[r] = prob ? __ldg(prob + t * K + k) : 1.f;
@@ -189,18 +201,19 @@ __global__ void __launch_bounds__(256) chunk_hist_kernel(const int32_t* __restri
 
 // Warp per expert: exclusive scan of hist[:, e] over the chunks.
 __global__ void __launch_bounds__(256) chunk_scan_kernel(const int32_t* __restrict__ hist, int NC,
-                                                         int E, int32_t* __restrict__ base,
+                                                         int E, int cap,
+                                                         int32_t* __restrict__ base,
                                                          int32_t* __restrict__ counts) {
   const int lane = threadIdx.x & 31;
   const int e = blockIdx.x * 8 + (threadIdx.x >> 5);
-  if (e < E) scan_expert(e, lane, hist, NC, E, base, counts);
+  if (e < E) scan_expert(e, lane, hist, NC, E, cap, base, counts);
 }
 
 // Block: exclusive scan of counts into shared offsets, then one warp per chunk
 // computes every pair's destination row.
 __global__ void __launch_bounds__(256) chunk_ranks_kernel(
-    const int32_t* __restrict__ idx, const float* __restrict__ prob, int T, int K, int E, int NC,
-    const int32_t* __restrict__ base, const int32_t* __restrict__ counts,
+    const int32_t* __restrict__ idx, const float* __restrict__ prob, int T, int K, int E, int cap,
+    int NC, const int32_t* __restrict__ base, const int32_t* __restrict__ counts,
     int32_t* __restrict__ offsets_out, int32_t* __restrict__ dst_row,
     int32_t* __restrict__ src_token, float* __restrict__ perm_prob) {
   __shared__ int32_t s_off[257];
@@ -208,7 +221,7 @@ __global__ void __launch_bounds__(256) chunk_ranks_kernel(
   block_offsets(counts, E, s_off, s_warp, offsets_out);
   const int c = blockIdx.x * 8 + (threadIdx.x >> 5);
   if (c < NC)
-    ranks_chunk(c, threadIdx.x & 31, idx, prob, T, K, E, base, s_off, dst_row, src_token,
+    ranks_chunk(c, threadIdx.x & 31, idx, prob, T, K, E, cap, base, s_off, dst_row, src_token,
                 perm_prob);
 }
 
@@ -239,9 +252,10 @@ cudaError_t launch_permute_maps(const moe_config_t& c, const int32_t* idx, const
   const int blocks = (int)ceil_div(NC, 8);
   chunk_hist_kernel<<<blocks, 256, 8 * c.E * sizeof(int32_t), s>>>(idx, c.T, c.K, c.E, NC, hist,
                                                                   status);
-  chunk_scan_kernel<<<(unsigned)ceil_div(c.E, 8), 256, 0, s>>>(hist, NC, c.E, base, counts);
-  chunk_ranks_kernel<<<blocks, 256, 0, s>>>(idx, prob, c.T, c.K, c.E, NC, base, counts, offsets,
-                                            dst_row, src_token, perm_prob);
+  chunk_scan_kernel<<<(unsigned)ceil_div(c.E, 8), 256, 0, s>>>(hist, NC, c.E, c.capacity, base,
+                                                                counts);
+  chunk_ranks_kernel<<<blocks, 256, 0, s>>>(idx, prob, c.T, c.K, c.E, c.capacity, NC, base, counts,
+                                            offsets, dst_row, src_token, perm_prob);
   return cudaGetLastError();
 }
 

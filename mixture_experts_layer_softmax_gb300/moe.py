@@ -37,7 +37,8 @@ class moe_config_t(ctypes.Structure):
                 ("K", ctypes.c_int32), ("F", ctypes.c_int32), ("dtype", ctypes.c_int32),
                 ("score", ctypes.c_int32), ("act", ctypes.c_int32), ("has_bias", ctypes.c_int32),
                 ("n_shared", ctypes.c_int32), ("flags", ctypes.c_uint32),
-                ("aux_loss_coeff", ctypes.c_float), ("z_loss_coeff", ctypes.c_float)]
+                ("aux_loss_coeff", ctypes.c_float), ("z_loss_coeff", ctypes.c_float),
+                ("capacity", ctypes.c_int32)]
 
 
 class MoeError(RuntimeError):
@@ -65,6 +66,8 @@ _SIG = {
     "moe_router_bwd": (ctypes.c_int, [_CFG] + [_P] * 14 + [ctypes.c_size_t, _P]),
     "moe_layer_bwd": (ctypes.c_int, [_CFG] + [_P] * 15 + [ctypes.c_size_t, _P]),
     "moe_layer_losses": (ctypes.c_int, [_CFG, _P, _P, ctypes.c_size_t, _P]),
+    "moe_expert_capacity": (ctypes.c_int32, [ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                             ctypes.c_float, ctypes.c_int32]),
     "moe_router_aux_loss": (ctypes.c_int, [_CFG, _P, _P, ctypes.c_float, ctypes.c_float, _P, _P,
                                            _P, ctypes.c_size_t, _P]),
     "moe_get_error": (ctypes.c_int, [_P]),
@@ -116,18 +119,18 @@ def _ws(ws):
 
 def make_config(T, h, E, K, F, dtype=MOE_BF16, score=MOE_SCORE_SOFTMAX, act=MOE_ACT_SWIGLU,
                 has_bias=0, n_shared=0, flags=MOE_FLAG_RENORM, aux_loss_coeff=0.0,
-                z_loss_coeff=0.0) -> moe_config_t:
+                z_loss_coeff=0.0, capacity=0) -> moe_config_t:
     return moe_config_t(int(T), int(h), int(E), int(K), int(F), int(dtype), int(score), int(act),
                         int(has_bias), int(n_shared), int(flags), float(aux_loss_coeff),
-                        float(z_loss_coeff))
+                        float(z_loss_coeff), int(capacity))
 
 
-def config_for(w, flags_extra=0, aux_loss_coeff=0.0, z_loss_coeff=0.0) -> moe_config_t:
+def config_for(w, flags_extra=0, aux_loss_coeff=0.0, z_loss_coeff=0.0, capacity=0) -> moe_config_t:
     """moe_config_t of a workloads.Workload."""
     flags = (MOE_FLAG_RENORM if w.renorm else 0) | (MOE_FLAG_FORCE_BALANCE if w.force_balance else 0)
     return make_config(w.T, w.h, w.E, w.K, w.F, MOE_BF16 if w.dtype == "bf16" else MOE_F32,
                        w.score, w.act, int(w.has_bias), w.n_shared, flags | flags_extra,
-                       aux_loss_coeff, z_loss_coeff)
+                       aux_loss_coeff, z_loss_coeff, capacity)
 
 
 # ---- entry points -------------------------------------------------------------
@@ -137,6 +140,11 @@ def moe_status_string(status) -> str:
 
 def moe_version() -> str:
     return _lib.moe_version().decode()
+
+
+def moe_expert_capacity(T, K, E, capacity_factor, min_capacity=0) -> int:
+    return int(_lib.moe_expert_capacity(int(T), int(K), int(E), float(capacity_factor),
+                                        int(min_capacity)))
 
 
 def moe_workspace_size(cfg) -> int:
