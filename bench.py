@@ -385,16 +385,12 @@ def run_ours(args, w):
             M.moe_unpermute_combine(cfg, y_perm, dst_row, None, y_s if w.n_shared else None, y)
             mark(6)
 
-    # kernels of this library per step: route (the fused router is one kernel;
-    # the tensor-core router splits W_r, runs the gating GEMM and selects),
-    # the one-launch dispatch, FC1 and FC2, the shared expert's two GEMMs (+ its
-    # offsets in moe_layer_fwd), combine
-    if w.dtype == "bf16":
-        pad = 8 if E <= 8 else (16 if E <= 16 else 32)
-        route_k = 1 if (E <= 32 and pad * h * 4 <= 192 * 1024) else 3
-    else:
-        route_k = 1 if E <= 32 else 2
-    launches_per_step = route_k + 1 + 2 + ((3 if train else 2) if w.n_shared else 0) + 1
+    # kernels of this library per step: route (bf16: split W_r, the gating
+    # GEMM, selection; fp32: one fused kernel for E <= 32, else GEMM and
+    # selection), dispatch (histogram, scan, ranks, row scatter), FC1 and FC2,
+    # the shared expert's two GEMMs (+ its offsets in moe_layer_fwd), combine
+    route_k = 3 if w.dtype == "bf16" else (1 if E <= 32 else 2)
+    launches_per_step = route_k + 4 + 2 + ((3 if train else 2) if w.n_shared else 0) + 1
     if train:  # backward: scatter, 4 GEMMs (+4 shared), dprob, router, router wgrad, combine
         launches_per_step += 1 + 4 + (4 if w.n_shared else 0) + 4
     # Eager stage timing: a GPU-side sleep after the L2 flush lets the host
