@@ -48,6 +48,9 @@ def parse():
     p.add_argument("--workload", default=None, help="workload name (default: the Mixtral-shaped layer)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--gather", action="store_true",
+                   help="time the forward with the gather-fused FC1 (no x_perm) instead of the "
+                        "x_perm scatter")
     p.add_argument("--no-graph", action="store_true",
                    help="time eager launches only (default: the step is also captured in a CUDA "
                         "graph and the graph replays give the headline time)")
@@ -338,6 +341,10 @@ def run_ours(args, w):
 
     stages = ["route", "dispatch", "fc1", "fc2", "shared", "combine"]
     train = w.backward
+    # --gather: dispatch builds only the maps and FC1 gathers the token rows
+    # (moe_expert_fc1_gather); by default the rows are scattered into x_perm
+    # once, as moe_layer_fwd does
+    gather = w.dtype == "bf16" and args.gather
     if train:
         # training step: the whole forward (saving for backward) then the whole
         # backward, each one C-ABI call, on the same workspace
@@ -371,10 +378,17 @@ def run_ours(args, w):
             mark(0)
             M.moe_router_topk(cfg, x, w_r, gate_bias, sel_bias, None, idx, prob, None, ws)
             mark(1)
-            M.moe_permute(cfg, x, idx, prob, x_perm, counts, offsets, dst_row, src_token,
-                          perm_prob, ws)
+            if gather:  # maps only: FC1 gathers the token rows itself
+                M.moe_permute(cfg, None, idx, prob, None, counts, offsets, dst_row, src_token,
+                              perm_prob, ws)
+            else:
+                M.moe_permute(cfg, x, idx, prob, x_perm, counts, offsets, dst_row, src_token,
+                              perm_prob, ws)
             mark(2)
-            M.moe_expert_fc1(cfg, x_perm, offsets, perm_prob, w1, b1, None, a)
+            if gather:
+                M.moe_expert_fc1_gather(cfg, x, src_token, offsets, perm_prob, w1, b1, None, a)
+            else:
+                M.moe_expert_fc1(cfg, x_perm, offsets, perm_prob, w1, b1, None, a)
             mark(3)
             M.moe_expert_fc2(cfg, a, offsets, perm_prob, w2, b2, y_perm)
             mark(4)
@@ -390,7 +404,8 @@ def run_ours(args, w):
     # selection), dispatch (histogram, scan, ranks, row scatter), FC1 and FC2,
     # the shared expert's two GEMMs (+ its offsets in moe_layer_fwd), combine
     route_k = 3 if w.dtype == "bf16" else (1 if E <= 32 else 2)
-    launches_per_step = route_k + 4 + 2 + ((3 if train else 2) if w.n_shared else 0) + 1
+    dispatch_k = 3 if (gather and not train) else 4
+    launches_per_step = route_k + dispatch_k + 2 + ((3 if train else 2) if w.n_shared else 0) + 1
     if train:  # backward: scatter, 4 GEMMs (+4 shared), dprob, router, router wgrad, combine
         launches_per_step += 1 + 4 + (4 if w.n_shared else 0) + 4
     # Eager stage timing: a GPU-side sleep after the L2 flush lets the host
@@ -432,6 +447,21 @@ def run_ours(args, w):
     if st != M.MOE_OK:
         raise RuntimeError(f"device status after the timed steps: {M.moe_status_string(st)}")
 
+    # the standalone permute (maps + x_perm row scatter), as the training path
+    # and moe_permute callers run it, timed on its own
+    permute_ms = None
+    if not train:
+        pev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+        for i in range(args.steps):
+            flush_buf.fill_(1)
+            hold()
+            pev[i][0].record(stream)
+            M.moe_permute(cfg, x, idx, prob, x_perm, counts, offsets, dst_row, src_token,
+                          perm_prob, ws)
+            pev[i][1].record(stream)
+        torch.cuda.synchronize()
+        permute_ms = statistics.mean(a.elapsed_time(b) for a, b in pev)
     per_step = [e[0].elapsed_time(e[n_ev - 1]) for e in evs]
     stage_ms = {s: statistics.mean(e[i].elapsed_time(e[i + 1]) for e in evs) for i, s in enumerate(stages)}
     ms_eager = ms = statistics.mean(per_step)
@@ -554,6 +584,8 @@ def run_ours(args, w):
         "gpu_launches": launches_per_step * args.steps, "clocks": clocks, "e2e": e2e,
         "wall_s_timed": t_wall, "ms_per_step_eager": ms_eager, "cuda_graph": graph_ms is not None,
         "gemm_tiling": args.tiling,
+        "forward_path": ("dispatch maps, token rows gathered inside FC1 (no x_perm)"
+                         if (gather and not train) else "dispatch maps + x_perm row scatter"),
     }
     if train:
         fwd_fl = w.flops_fwd()
@@ -570,7 +602,7 @@ def run_ours(args, w):
         gemm_tf = (fc1_flops + fc2_flops) / ((stage_ms["fc1"] + stage_ms["fc2"]) / 1000.0) / 1e12
         perm_bytes = T * h * esz + P * h * esz
         comb_bytes = P * h * esz + T * h * esz + (T * h * esz if w.n_shared else 0)
-        perm_gbs = perm_bytes / (stage_ms["dispatch"] / 1000.0) / 1e9
+        perm_gbs = perm_bytes / (permute_ms / 1000.0) / 1e9
         comb_gbs = comb_bytes / (stage_ms["combine"] / 1000.0) / 1e9
         pair = args.tiling == "2cta" or (args.tiling == "auto" and P >= 512 * E)
         fc1_kernel = ("grouped_gemm_tc2_kernel<FC1> (CTA pairs)" if pair
@@ -583,6 +615,10 @@ def run_ours(args, w):
         line["grouped_gemm_pct_bf16_peak"] = 100.0 * gemm_tf / peak_tf
         line["grouped_gemm_tflops"] = gemm_tf
         line["permute_pct_hbm"] = 100.0 * perm_gbs / pk["hbm_gbs"]
+        line["permute_ms"] = permute_ms
+        line["permute_how"] = ("moe_permute with the row scatter (maps + x_perm), timed alone; the "
+                               "forward above " + ("gathers the rows inside FC1 instead"
+                                                   if gather else "uses it"))
         line["combine_pct_hbm"] = 100.0 * comb_gbs / pk["hbm_gbs"]
         line["route_ms"] = stage_ms["route"]
         # the router reads every token row once (its weight stays in L2/shared memory)

@@ -205,6 +205,22 @@ moe_status_t moe_expert_fc2(const moe_config_t* cfg, const void* a, const int32_
                             const float* perm_prob, const void* w2, const void* b2,
                             void* y_perm, moe_stream_t stream);
 
+/* FC1 with the dispatch gather fused in (review §4.3.1 "permutation fusion";
+ * §2.1 Dispatch then Expert computation): GEMM row r reads the token row
+ * x[src_token[r]] directly instead of x_perm[r], so the permuted copy of x is
+ * never written.  Same outputs and rules as moe_expert_fc1 otherwise.
+ *   x [T,h] bf16; src_token [T*K] i32 and offsets [E+1] from moe_permute
+ *   (called with x = NULL: maps only); perm_prob, w1, b1, act_save, a as in
+ *   moe_expert_fc1.  Tensor-core (bf16) configurations only, else
+ *   MOE_ERR_UNSUPPORTED.  The rows are fetched by TMA tile::gather4 loads;
+ *   since FC1 reads each row block once per N tile, this is slower on GB300
+ *   than moe_permute's one-pass scatter followed by moe_expert_fc1 (which
+ *   moe_layer_fwd uses), but it needs no x_perm buffer. */
+moe_status_t moe_expert_fc1_gather(const moe_config_t* cfg, const void* x,
+                                   const int32_t* src_token, const int32_t* offsets,
+                                   const float* perm_prob, const void* w1, const void* b1,
+                                   void* act_save, void* a, moe_stream_t stream);
+
 /* Combine (review §2.1 "Combine"; the skill page's index_add_):
  *   y[t] = sum_{k=0}^{K-1} w[t,k] * y_perm[dst_row[t,k]]  (+ shared_y[t])
  * with w = topk_prob, or 1 when topk_prob is NULL (probabilities already

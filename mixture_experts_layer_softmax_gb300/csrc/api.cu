@@ -24,7 +24,7 @@ cudaError_t launch_expert_gemm_simt(const moe_config_t&, int, int, const void*, 
                                     cudaStream_t);
 cudaError_t launch_expert_gemm_tc(const moe_config_t&, int, int, const void*, const int32_t*,
                                   const float*, const void*, const void*, void*, void*, int, int*,
-                                  cudaStream_t);
+                                  cudaStream_t, const int32_t*);
 cudaError_t launch_bounded_wait_probe(int64_t, int*, cudaStream_t);
 cudaError_t launch_aux_loss(const moe_config_t&, const float*, const int32_t*, float, float, float*,
                             float*, double*, double*, int32_t*, float*, int*, cudaStream_t);
@@ -149,21 +149,26 @@ bool use_tensor_cores(const moe_config_t& c) {
   return c.dtype == MOE_BF16 && !(c.flags & MOE_FLAG_GEMM_SIMT);
 }
 
+// src_token (tensor cores, FC1 only): A is the token rows x and GEMM row r
+// reads x[src_token[r]] (the gather-fused FC1) instead of a permuted buffer.
 cudaError_t run_expert_gemm(const moe_config_t& c, int fc, int rows, const void* A,
                             const int32_t* offsets, const float* prob, const void* w,
                             const void* bias, void* act_save, void* out, const DeviceInfo* d,
-                            cudaStream_t s) {
+                            cudaStream_t s, const int32_t* src_token = nullptr) {
   if (use_tensor_cores(c))
     return launch_expert_gemm_tc(c, fc, rows, A, offsets, prob, w, bias, act_save, out, d->sms,
-                                 d->status, s);
+                                 d->status, s, src_token);
+  if (src_token) return cudaErrorInvalidValue;
   return launch_expert_gemm_simt(c, fc, rows, A, offsets, prob, w, bias, act_save, out, s);
 }
 
 cudaError_t run_grouped_mlp(const moe_config_t& c, int rows, const void* x_perm,
                             const int32_t* offsets, const float* prob, const void* w1,
                             const void* b1, const void* w2, const void* b2, void* act_save,
-                            void* a, void* y_perm, const DeviceInfo* d, cudaStream_t s) {
-  cudaError_t e = run_expert_gemm(c, 1, rows, x_perm, offsets, prob, w1, b1, act_save, a, d, s);
+                            void* a, void* y_perm, const DeviceInfo* d, cudaStream_t s,
+                            const int32_t* src_token = nullptr) {
+  cudaError_t e =
+      run_expert_gemm(c, 1, rows, x_perm, offsets, prob, w1, b1, act_save, a, d, s, src_token);
   if (e != cudaSuccess) return e;
   return run_expert_gemm(c, 2, rows, a, offsets, prob, w2, b2, nullptr, y_perm, d, s);
 }
@@ -329,6 +334,24 @@ moe_status_t moe_expert_fc1(const moe_config_t* cfg, const void* x_perm, const i
                                      static_cast<cudaStream_t>(stream)));
 }
 
+moe_status_t moe_expert_fc1_gather(const moe_config_t* cfg, const void* x,
+                                   const int32_t* src_token, const int32_t* offsets,
+                                   const float* perm_prob, const void* w1, const void* b1,
+                                   void* act_save, void* a, moe_stream_t stream) {
+  moe_status_t st = check_config(cfg);
+  if (st != MOE_OK) return st;
+  if (!use_tensor_cores(*cfg)) return MOE_ERR_UNSUPPORTED;
+  if (!x || !src_token || !offsets || !w1 || !a) return MOE_ERR_INVALID_ARG;
+  if (cfg->has_bias && !b1) return MOE_ERR_INVALID_ARG;
+  if (!al16(x) || !al16(w1) || !al16(a) || !al16(act_save)) return MOE_ERR_INVALID_ARG;
+  if (cfg->flags & MOE_FLAG_VALIDATE_ONLY) return MOE_OK;
+  const DeviceInfo* d = device_info();
+  if (!d) return MOE_ERR_CUDA;
+  return cuda_status(run_expert_gemm(*cfg, 1, cfg->T * cfg->K, x, offsets, perm_prob, w1,
+                                     cfg->has_bias ? b1 : nullptr, act_save, a, d,
+                                     static_cast<cudaStream_t>(stream), src_token));
+}
+
 moe_status_t moe_expert_fc2(const moe_config_t* cfg, const void* a, const int32_t* offsets,
                             const float* perm_prob, const void* w2, const void* b2,
                             void* y_perm, moe_stream_t stream) {
@@ -394,7 +417,10 @@ moe_status_t moe_layer_fwd(const moe_config_t* cfg, const void* x, const float* 
     e = launch_aux_loss(c, at<float>(ws, w.logits), idx, 0.f, 0.f, at<float>(ws, w.aux_losses),
                         nullptr, at<double>(ws, w.aux_part_p), at<double>(ws, w.aux_part_z),
                         at<int32_t>(ws, w.aux_part_cnt), at<float>(ws, w.aux_f), d->status, s);
-  // Dispatch
+  // Dispatch: the maps, then the rows scattered once into x_perm.  (FC1 could
+  // gather its rows from x instead -- moe_expert_fc1_gather -- but it re-reads
+  // each row block once per N tile, and a gathered re-read costs the TMA
+  // engine far more than a tiled one: the one-pass scatter is faster.)
   if (e == cudaSuccess)
     e = launch_permute_maps(c, idx, prob, at<int32_t>(ws, w.hist), at<int32_t>(ws, w.chunk_base),
                             at<int32_t>(ws, w.counts), offsets, dst_row,

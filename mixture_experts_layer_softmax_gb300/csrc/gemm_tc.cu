@@ -61,6 +61,8 @@ enum TcMode { kTcSwiGLU = 0, kTcGelu = 1, kTcFc2 = 2, kTcF32 = 3 };
 
 struct TcParams {
   const int32_t* offsets;        // [E+1]
+  const __nv_bfloat16* xg;       // gather mode: token rows [*, Kd]
+  const int32_t* src_token;      // gather mode: token of each permuted row
   const float* prob;             // [P] or null
   const __nv_bfloat16* bias;     // GELU FC1: b1 [E][N]; FC2: b2 [E][N]; or null
   __nv_bfloat16* out;            // [P, N]
@@ -119,7 +121,13 @@ MOE_D void store8(__nv_bfloat16* dst, const float* v) {
   *reinterpret_cast<uint4*>(dst) = u;
 }
 
-template <int MODE, int BNT>
+// GATHER (FC1 only): the A rows are the token rows x[src_token[r]], fetched
+// by the TMA engine with tile::gather4 loads (four token rows each; the x map's
+// box is one row high): the producer warp's 32 lanes each fetch 4 of the
+// tile's 128 rows per stage into the same 128-byte-swizzled layout, completing
+// on the stage barrier like the tiled loads.  Rows past the expert's end load
+// token row 0 (their outputs are never stored).
+template <int MODE, int BNT, bool GATHER = false>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                            const __grid_constant__ CUtensorMap tmB, const TcParams p) {
@@ -193,7 +201,56 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc::WaitCtl wc{p.status, &ctl.abort, p.wait_limit_ns, 0};
   tc::WaitCtl wdrain{p.status, nullptr, 1000000000ull, 0};
 
-  if (warp == 0) {
+  if (warp == 0 && GATHER) {
+    // ================= gathering TMA producer (whole warp) =================
+    int stage = 0;
+    uint32_t phase = 0, issued = 0, issued_par = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+      int e, mb, nb;
+      decode_tile(ctl, E, nblk, tile / S, e, mb, nb);
+      const int m_e = ctl.off[e + 1] - ctl.off[e];
+      int b_row0, b_row1 = 0;
+      if (MODE == kTcSwiGLU) {
+        b_row0 = e * p.Nb + nb * (BN / 2);
+        b_row1 = e * p.Nb + p.N + nb * (BN / 2);
+      } else {
+        b_row0 = e * p.Nb + nb * BN;
+      }
+      int rr[4];  // this lane's 4 rows (4 lane .. 4 lane + 3) of the tile's 128
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int lr = mb * BM + 4 * lane + j;
+        rr[j] = lr < m_e ? __ldg(p.src_token + ctl.off[e] + lr) : 0;
+      }
+      for (int kb = 0; kb < KB; ++kb) {
+        int w_ok = lane == 0 ? (int)tc::mbar_wait(tc::smem_u32(&ctl.empty[stage]), phase ^ 1, wc) : 0;
+        if (!__shfl_sync(0xffffffffu, w_ok, 0)) { ok = false; break; }
+        const uint32_t fb = tc::smem_u32(&ctl.full[stage]);
+        if (lane == 0) {
+          tc::mbar_arrive_expect_tx(fb, STAGE_BYTES);
+          const uint32_t b_dst = tc::smem_u32(sB + stage * B_BYTES);
+          if (MODE == kTcSwiGLU) {
+            tc::tma_load_2d(b_dst, &tmB, kb * BK, b_row0, fb);
+            tc::tma_load_2d(b_dst + B_BYTES / 2, &tmB, kb * BK, b_row1, fb);
+          } else {
+            tc::tma_load_2d(b_dst, &tmB, kb * BK, b_row0, fb);
+          }
+        }
+        tc::tma_gather4(tc::smem_u32(sA + stage * A_BYTES) + lane * 512, &tmA, kb * BK, rr[0], rr[1],
+                        rr[2], rr[3], fb);
+        issued |= 1u << stage;
+        issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
+        if (++stage == STAGES) { stage = 0; phase ^= 1; }
+      }
+    }
+    // copies still in flight must land before the block exits
+    if (lane == 0)
+      for (int s = 0; s < STAGES; ++s)
+        if ((issued >> s) & 1u)
+          tc::mbar_wait(tc::smem_u32(&ctl.full[s]), (issued_par >> s) & 1u, wdrain);
+    __syncwarp();
+  } else if (warp == 0) {
     // ================= TMA producer =================
     if (lane == 0) {
       int stage = 0;
@@ -415,33 +472,42 @@ bool encode_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, u
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int MODE, int BNT = 256>
+template <int MODE, int BNT = 256, bool GATHER = false>
 cudaError_t launch_mode(const CUtensorMap& a, const CUtensorMap& b, const TcParams& p, int grid,
                         cudaStream_t s) {
   constexpr size_t bytes = smem_bytes<BNT>();
-  cudaError_t e = cudaFuncSetAttribute(grouped_gemm_tc_kernel<MODE, BNT>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  auto kern = grouped_gemm_tc_kernel<MODE, BNT, GATHER>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
   if (e != cudaSuccess) return e;
-  grouped_gemm_tc_kernel<MODE, BNT><<<grid, kThreads, bytes, s>>>(a, b, p);
+  kern<<<grid, kThreads, bytes, s>>>(a, b, p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 // One grouped GEMM: out[r, :] = epilogue(A[r, :] B_e^T) for the rows r of each
-// expert e.  A [P, Kd]; B [E * Nb, Kd] (bf16, row-major).
+// expert e.  A [P, Kd]; B [E * Nb, Kd] (bf16, row-major).  With src_token (FC1
+// only), row r of the GEMM is token row A[src_token[r]] (A = x, [T, Kd]).
 cudaError_t launch_grouped_gemm_tc(int mode, int P, const void* A, int Kd, const void* B, int Nb,
                                    int E, int N, const int32_t* offsets, const float* prob,
                                    int prob_here, const void* bias, void* out, void* act_save,
-                                   int sms, int* status, cudaStream_t s) {
+                                   int sms, int* status, cudaStream_t s,
+                                   const int32_t* src_token, int T) {
   if (P == 0) return cudaSuccess;
+  const bool gather = src_token != nullptr;
+  if (gather && mode != kTcSwiGLU && mode != kTcGelu) return cudaErrorInvalidValue;
   CUtensorMap ma, mb;
-  if (!encode_2d(&ma, A, (uint64_t)P, (uint64_t)Kd, BM)) return cudaErrorInvalidValue;
   constexpr int BN = 256;
   const uint32_t brows = mode == kTcSwiGLU ? BN / 2 : BN;
   if (!encode_2d(&mb, B, (uint64_t)E * Nb, (uint64_t)Kd, brows)) return cudaErrorInvalidValue;
+  // gather: the token rows x [T, Kd], fetched four rows at a time (box one row high)
+  if (!encode_2d(&ma, A, (uint64_t)(gather ? T : P), (uint64_t)Kd, gather ? 1 : BM))
+    return cudaErrorInvalidValue;
   TcParams p;
   p.offsets = offsets; p.prob = prob;
+  p.xg = static_cast<const __nv_bfloat16*>(A);
+  p.src_token = src_token;
   p.bias = static_cast<const __nv_bfloat16*>(bias);
   p.out = static_cast<__nv_bfloat16*>(out);
   p.act_save = static_cast<__nv_bfloat16*>(act_save);
@@ -454,8 +520,12 @@ cudaError_t launch_grouped_gemm_tc(int mode, int P, const void* A, int Kd, const
   const int64_t tiles_max = (ceil_div(P, BM) + E) * (int64_t)nblk;
   const int grid = (int)(tiles_max < sms ? tiles_max : sms);
   switch (mode) {
-    case kTcSwiGLU: return launch_mode<kTcSwiGLU>(ma, mb, p, grid, s);
-    case kTcGelu: return launch_mode<kTcGelu>(ma, mb, p, grid, s);
+    case kTcSwiGLU:
+      return gather ? launch_mode<kTcSwiGLU, 256, true>(ma, mb, p, grid, s)
+                    : launch_mode<kTcSwiGLU>(ma, mb, p, grid, s);
+    case kTcGelu:
+      return gather ? launch_mode<kTcGelu, 256, true>(ma, mb, p, grid, s)
+                    : launch_mode<kTcGelu>(ma, mb, p, grid, s);
     case kTcF32: return launch_mode<kTcF32>(ma, mb, p, grid, s);
     default: return launch_mode<kTcFc2>(ma, mb, p, grid, s);
   }
@@ -464,14 +534,16 @@ cudaError_t launch_grouped_gemm_tc(int mode, int P, const void* A, int Kd, const
 cudaError_t launch_grouped_gemm_tc2(int mode, int P, const void* A, int Kd, const void* B, int Nb,
                                     int E, int N, const int32_t* offsets, const float* prob,
                                     int prob_here, const void* bias, void* out, void* act_save,
-                                    int sms, int* status, cudaStream_t s);
+                                    int sms, int* status, cudaStream_t s,
+                                    const int32_t* src_token, int T);
 
 // One of the two expert GEMMs (fc = 1: x_perm -> a, fc = 2: a -> y_perm), on
-// CTA pairs when the experts are large enough to fill 256-row tiles.
+// CTA pairs when the experts are large enough to fill 256-row tiles.  With
+// src_token, FC1 gathers its rows from the token rows A = x instead.
 cudaError_t launch_expert_gemm_tc(const moe_config_t& c, int fc, int P, const void* A,
                                   const int32_t* offsets, const float* prob, const void* w,
                                   const void* bias, void* act_save, void* out, int sms,
-                                  int* status, cudaStream_t s) {
+                                  int* status, cudaStream_t s, const int32_t* src_token) {
   const bool swiglu = c.act == MOE_ACT_SWIGLU;
   const bool prob_after = c.has_bias != 0;
   const bool pair = (c.flags & MOE_FLAG_GEMM_2CTA) ||
@@ -479,9 +551,9 @@ cudaError_t launch_expert_gemm_tc(const moe_config_t& c, int fc, int P, const vo
   auto run = pair ? launch_grouped_gemm_tc2 : launch_grouped_gemm_tc;
   if (fc == 1)
     return run(swiglu ? kTcSwiGLU : kTcGelu, P, A, c.h, w, swiglu ? 2 * c.F : c.F, c.E, c.F,
-               offsets, prob, !prob_after, bias, out, act_save, sms, status, s);
+               offsets, prob, !prob_after, bias, out, act_save, sms, status, s, src_token, c.T);
   return run(kTcFc2, P, A, c.F, w, c.h, c.E, c.h, offsets, prob, prob_after, bias, out, nullptr,
-             sms, status, s);
+             sms, status, s, nullptr, c.T);
 }
 
 // Router gating on the tensor cores.  w3 holds the exactly split router

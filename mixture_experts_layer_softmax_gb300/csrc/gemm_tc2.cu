@@ -41,6 +41,8 @@ enum Tc2Mode { kSwiGLU = 0, kGelu = 1, kFc2 = 2 };
 
 struct Tc2Params {
   const int32_t* offsets;
+  const __nv_bfloat16* xg;     // gather mode: token rows [*, Kd]
+  const int32_t* src_token;    // gather mode: token of each permuted row
   const float* prob;
   const __nv_bfloat16* bias;
   __nv_bfloat16* out;
@@ -145,7 +147,24 @@ MOE_D void store8(__nv_bfloat16* dst, const float* v) {
   *reinterpret_cast<uint4*>(dst) = u;
 }
 
-template <int MODE>
+// GATHER: the A rows are not a permuted buffer's consecutive rows but the
+// token rows x[src_token[r]], fetched by the TMA engine with tile::gather4
+// loads (four token rows per load, the x map's box one row high): the
+// producer warp's 32 lanes each fetch 4 of the CTA's 128 rows per stage into
+// the same 128-byte-swizzled layout, completing on the same stage barrier as
+// the tiled loads.  Rows past the expert's end load token row 0 (their
+// outputs are never stored).
+MOE_D void tma_gather4_pair(uint32_t dst, const CUtensorMap* map, int32_t c0, int4 rows,
+                            uint32_t bar_cluster) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile::gather4"
+      ".mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(rows.x), "r"(rows.y), "r"(rows.z),
+      "r"(rows.w), "r"(bar_cluster)
+      : "memory");
+}
+
+template <int MODE, bool GATHER>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     grouped_gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmA,
                             const __grid_constant__ CUtensorMap tmB, const Tc2Params p) {
@@ -210,7 +229,48 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   tc::WaitCtl wc{p.status, &ctl.abort, p.wait_limit_ns, 0};
   tc::WaitCtl wdrain{p.status, nullptr, 1000000000ull, 0};
 
-  if (warp == 0) {
+  if (warp == 0 && GATHER) {
+    // ================= gathering TMA producer (whole warp, both CTAs) =======
+    int stage = 0;
+    uint32_t phase = 0, issued = 0, issued_par = 0;
+    bool ok = true;
+    for (int tile = cid; tile < total && ok; tile += ncl) {
+      int e, mb, nb;
+      decode_tile(ctl, E, nblk, tile, e, mb, nb);
+      const int lrow0 = mb * BMC + (int)rank * BM;  // first A row of this CTA, inside the expert
+      const int m_e = ctl.off[e + 1] - ctl.off[e];
+      const int b_row = MODE == kSwiGLU ? e * p.Nb + (int)rank * p.N + nb * BNL
+                                        : e * p.Nb + nb * BN + (int)rank * BNL;
+      // this lane's 4 rows (4 lane .. 4 lane + 3) of the CTA's 128
+      int rr[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int lr = lrow0 + 4 * lane + j;
+        rr[j] = lr < m_e ? __ldg(p.src_token + ctl.off[e] + lr) : 0;
+      }
+      const int4 rows = make_int4(rr[0], rr[1], rr[2], rr[3]);
+      for (int kb = 0; kb < KB; ++kb) {
+        int w_ok = lane == 0 ? (int)tc::mbar_wait(tc::smem_u32(&ctl.empty[stage]), phase ^ 1, wc) : 0;
+        if (!__shfl_sync(0xffffffffu, w_ok, 0)) { ok = false; break; }
+        const uint32_t full_local = tc::smem_u32(&ctl.full[stage]);
+        const uint32_t full_even = mapa(full_local, 0);
+        if (lane == 0) {
+          if (even) tc::mbar_arrive_expect_tx(full_local, 2 * STAGE_BYTES);
+          tma_load_2d_pair(tc::smem_u32(sB + stage * B_BYTES), &tmB, kb * BK, b_row, full_even);
+        }
+        tma_gather4_pair(tc::smem_u32(sA + stage * A_BYTES) + lane * 512, &tmA, kb * BK, rows,
+                         full_even);
+        issued |= 1u << stage;
+        issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
+        if (++stage == STAGES) { stage = 0; phase ^= 1; }
+      }
+    }
+    if (lane == 0)
+      for (int s = 0; s < STAGES; ++s)
+        if ((issued >> s) & 1u)
+          tc::mbar_wait(tc::smem_u32(&ctl.empty[s]), (issued_par >> s) & 1u, wdrain);
+    __syncwarp();
+  } else if (warp == 0) {
     // ================= TMA producer (both CTAs) =================
     if (lane == 0) {
       int stage = 0;
@@ -396,11 +456,12 @@ bool encode(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int MODE>
+template <int MODE, bool GATHER>
 cudaError_t launch_mode2(const CUtensorMap& a, const CUtensorMap& b, const Tc2Params& p,
                          int64_t tiles, int sms, cudaStream_t s) {
-  cudaError_t e = cudaFuncSetAttribute(grouped_gemm_tc2_kernel<MODE>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+  auto kern = grouped_gemm_tc2_kernel<MODE, GATHER>;
+  cudaError_t e =
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
   if (e != cudaSuccess) return e;
   // as many pairs as can be resident at once (a pair needs two SMs of one
   // cluster-capable group), capped by the tile count
@@ -410,29 +471,36 @@ cudaError_t launch_mode2(const CUtensorMap& a, const CUtensorMap& b, const Tc2Pa
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = s;
-  if (cudaOccupancyMaxActiveClusters(&max_clusters, grouped_gemm_tc2_kernel<MODE>, &cfg) !=
-          cudaSuccess ||
+  if (cudaOccupancyMaxActiveClusters(&max_clusters, kern, &cfg) != cudaSuccess ||
       max_clusters < 1)
     max_clusters = sms / 2;
   const int64_t pairs = tiles < max_clusters ? tiles : max_clusters;
-  grouped_gemm_tc2_kernel<MODE><<<(unsigned)(2 * pairs), kThreads, kSmemBytes, s>>>(a, b, p);
+  kern<<<(unsigned)(2 * pairs), kThreads, kSmemBytes, s>>>(a, b, p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 // Pair-tile version of launch_grouped_gemm_tc (same modes: 0 SwiGLU FC1,
-// 1 GELU FC1, 2 FC2; same arguments).
+// 1 GELU FC1, 2 FC2; same arguments).  With src_token (FC1 only), A is not a
+// permuted buffer: row r of the GEMM is token row A[src_token[r]] (A = x, [T, Kd]).
 cudaError_t launch_grouped_gemm_tc2(int mode, int P, const void* A, int Kd, const void* B, int Nb,
                                     int E, int N, const int32_t* offsets, const float* prob,
                                     int prob_here, const void* bias, void* out, void* act_save,
-                                    int sms, int* status, cudaStream_t s) {
+                                    int sms, int* status, cudaStream_t s,
+                                    const int32_t* src_token, int T) {
   if (P == 0) return cudaSuccess;
+  const bool gather = src_token != nullptr;
+  if (gather && mode == kFc2) return cudaErrorInvalidValue;
   CUtensorMap ma, mb;
-  if (!encode(&ma, A, (uint64_t)P, (uint64_t)Kd, BM)) return cudaErrorInvalidValue;
   if (!encode(&mb, B, (uint64_t)E * Nb, (uint64_t)Kd, BNL)) return cudaErrorInvalidValue;
+  // gather: the token rows x [T, Kd], fetched four rows at a time (box one row high)
+  if (!encode(&ma, A, (uint64_t)(gather ? T : P), (uint64_t)Kd, gather ? 1 : BM))
+    return cudaErrorInvalidValue;
   Tc2Params p;
   p.offsets = offsets; p.prob = prob;
+  p.xg = static_cast<const __nv_bfloat16*>(A);
+  p.src_token = src_token;
   p.bias = static_cast<const __nv_bfloat16*>(bias);
   p.out = static_cast<__nv_bfloat16*>(out);
   p.act_save = static_cast<__nv_bfloat16*>(act_save);
@@ -442,9 +510,13 @@ cudaError_t launch_grouped_gemm_tc2(int mode, int P, const void* A, int Kd, cons
   const int nblk = mode == kSwiGLU ? (N + BNL - 1) / BNL : (N + BN - 1) / BN;
   const int64_t tiles = (ceil_div(P, BMC) + E) * (int64_t)nblk;
   switch (mode) {
-    case kSwiGLU: return launch_mode2<kSwiGLU>(ma, mb, p, tiles, sms, s);
-    case kGelu: return launch_mode2<kGelu>(ma, mb, p, tiles, sms, s);
-    default: return launch_mode2<kFc2>(ma, mb, p, tiles, sms, s);
+    case kSwiGLU:
+      return gather ? launch_mode2<kSwiGLU, true>(ma, mb, p, tiles, sms, s)
+                    : launch_mode2<kSwiGLU, false>(ma, mb, p, tiles, sms, s);
+    case kGelu:
+      return gather ? launch_mode2<kGelu, true>(ma, mb, p, tiles, sms, s)
+                    : launch_mode2<kGelu, false>(ma, mb, p, tiles, sms, s);
+    default: return launch_mode2<kFc2, false>(ma, mb, p, tiles, sms, s);
   }
 }
 

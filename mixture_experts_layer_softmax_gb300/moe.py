@@ -59,6 +59,7 @@ _SIG = {
                                            ctypes.c_size_t, _P]),
     "moe_expert_fc1": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P, _P, _P]),
     "moe_expert_fc2": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P, _P]),
+    "moe_expert_fc1_gather": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "moe_unpermute_combine": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P]),
     "moe_layer_fwd": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                      ctypes.c_size_t, _P]),
@@ -195,6 +196,13 @@ def moe_expert_fc1(cfg, x_perm, offsets, perm_prob, w1, b1, act_save, a, stream=
     _check("moe_expert_fc1", _lib.moe_expert_fc1(
         ctypes.byref(cfg), _ptr(x_perm), _ptr(offsets), _ptr(perm_prob), _ptr(w1), _ptr(b1),
         _ptr(act_save), _ptr(a), _stream(stream)))
+
+
+def moe_expert_fc1_gather(cfg, x, src_token, offsets, perm_prob, w1, b1, act_save, a,
+                          stream=None):
+    _check("moe_expert_fc1_gather", _lib.moe_expert_fc1_gather(
+        ctypes.byref(cfg), _ptr(x), _ptr(src_token), _ptr(offsets), _ptr(perm_prob), _ptr(w1),
+        _ptr(b1), _ptr(act_save), _ptr(a), _stream(stream)))
 
 
 def moe_expert_fc2(cfg, a, offsets, perm_prob, w2, b2, y_perm, stream=None):
