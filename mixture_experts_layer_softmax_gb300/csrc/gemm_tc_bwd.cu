@@ -21,24 +21,39 @@
 // end are zeroed in shared memory first.
 //
 // Kernel structure as the forward kernel: persistent, 1 CTA per SM, TMA warp,
-// MMA warp, 4 epilogue warps, 4-stage ring of 48 KB, TMEM 2 x 256 columns,
-// bounded waits.  MN-major tiles are {64 elements, 64 K-rows} TMA boxes with
-// 128-byte swizzle (8 KB each): LBO = 8 KB between 64-element atoms, SBO =
-// 1 KB between 8-row groups.
+// MMA warp, 4 epilogue warps, TMEM 2 x 256 columns, bounded waits.  The data
+// gradients use a 4-stage ring of 48 KB; the weight gradient 2 stages of
+// 96 KB (one 128-row block of the expert per stage) and streams its output
+// through 32 KB of staging with TMA stores.  MN-major tiles are {64 elements,
+// BK K-rows} TMA boxes with 128-byte swizzle: LBO = 64 x BK x 2 bytes between
+// 64-element atoms, SBO = 1 KB between 8-row groups.
 #include "tc_ptx.cuh"
 
 namespace moe {
 namespace {
 
-constexpr int BM = 128, BN = 256, BK = 64, MAX_STAGES = 4;
-constexpr int A_BYTES = BM * BK * 2;  // 16 KB
-constexpr int B_BYTES = BN * BK * 2;  // 32 KB
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int ATOM = 64 * 64 * 2;     // one MN-major {64, 64} box
+constexpr int BM = 128, BN = 256;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int kThreads = 192;
 
 enum BwdKind { kDgradSwiGLU = 0, kDgradPlain = 1, kWgrad = 2 };
+
+// Per-kind pipeline.  The data-gradient kernels reduce over thousands of K
+// values in 4 stages of 64.  The weight-gradient kernel reduces over one
+// expert's rows (about a hundred in a fine-grained layer) with its operands in
+// L2, where a stage's load rate grows with the size of its TMA boxes: it uses
+// 2 stages of 128 rows (96 KB, six {64 column, 128 row} boxes), one stage per
+// tile at that size.
+template <int KIND>
+struct BwdCfg {
+  static constexpr int BK = KIND == kWgrad ? 128 : 64;
+  static constexpr int STAGES = KIND == kWgrad ? 2 : 4;
+  static constexpr int A_BYTES = BM * BK * 2;
+  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int ATOM = 64 * BK * 2;  // one MN-major {64 columns, BK rows} box
+  static constexpr int NTS = KIND == kWgrad ? 1 : 257;  // tile_start entries needed
+};
 
 struct BwdParams {
   const int32_t* offsets;      // [E+1]
@@ -51,23 +66,26 @@ struct BwdParams {
   uint64_t wait_limit_ns;
 };
 
+template <int STAGES, int NTS>
 struct SmemCtl {
-  uint64_t full[MAX_STAGES], empty[MAX_STAGES], tmem_full[2], tmem_empty[2], drain;
+  uint64_t full[STAGES], empty[STAGES], tmem_full[2], tmem_empty[2], drain;
   uint32_t tmem_base;
   int abort;
-  int tile_start[257];
+  int total;
+  int tile_start[NTS];
   int off[257];
 };
 
 // The weight-gradient kernel writes its 128 x 256 output tile through shared
-// memory and TMA stores (64 KB of staging), so it keeps 3 stages instead of 4:
-// its reduction is only one expert's rows (a few 64-row blocks) anyway.
-constexpr int STAGING_BYTES = BM * BN * 2;
-template <int KIND> constexpr int stages_of() { return KIND == 2 ? 3 : 4; }
+// memory with TMA stores, 64 columns at a time: each epilogue warp has two
+// 4 KB slots ({64 column, 32 row} boxes) and refills one while the other's
+// store is still reading it (32 KB of staging).
+constexpr int STAGING_BYTES = 4 * 2 * 4096;
 template <int KIND>
 constexpr size_t smem_bytes() {
-  return 1024 + (size_t)stages_of<KIND>() * STAGE_BYTES + (KIND == 2 ? STAGING_BYTES : 0) +
-         sizeof(SmemCtl);
+  return 1024 + (size_t)BwdCfg<KIND>::STAGES * BwdCfg<KIND>::STAGE_BYTES +
+         (KIND == kWgrad ? STAGING_BYTES : 0) +
+         sizeof(SmemCtl<BwdCfg<KIND>::STAGES, BwdCfg<KIND>::NTS>);
 }
 
 MOE_D void tma_store_3d(const CUtensorMap* map, int32_t c0, int32_t c1, int32_t c2, uint32_t src) {
@@ -78,7 +96,7 @@ MOE_D void tma_store_3d(const CUtensorMap* map, int32_t c0, int32_t c1, int32_t 
       : "memory");
 }
 MOE_D void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-MOE_D void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+MOE_D void bulk_wait_read1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
 MOE_D void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 MOE_D void tma_load_3d(uint32_t dst, const CUtensorMap* map, int32_t c0, int32_t c1, int32_t c2,
@@ -109,10 +127,58 @@ MOE_D void load8(const __nv_bfloat16* src, float* v) {
   }
 }
 
+// Epilogue of one weight-gradient tile for one epilogue warp (TMEM lane
+// quarter q): its 32 rows x 256 columns, 64 columns at a time: TMEM -> bf16 ->
+// a swizzled {64 col, 32 row} box in one of the warp's two 4 KB shared-memory
+// slots (row `lane`, 16-B chunk c at c ^ (lane & 7)) -> one TMA store (rows
+// past M are clipped).  A slot is refilled once the store issued from it two
+// boxes earlier has read it, so the other slot's store stays in flight.  The
+// accumulator is released (tmem_empty) right after its last read.  have_rows
+// false: the expert has no rows and the tile is zeros.
+MOE_D void wgrad_store_tile(uint32_t tbase, bool have_rows, int e, int mb, int nb, int q,
+                            int lane, uint8_t* staging, const CUtensorMap* tmC,
+                            uint32_t tmem_empty_bar) {
+  uint8_t* slots = staging + q * 2 * 4096;
+#pragma unroll 1
+  for (int j = 0; j < BN / 64; ++j) {
+    uint8_t* box = slots + (j & 1) * 4096;
+    uint32_t r[64];
+    if (have_rows) {
+      tc::tmem_ld_32x32b_x64(tbase + j * 64, r);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 64; ++i) r[i] = 0u;
+    }
+    if (j == BN / 64 - 1) {  // every TMEM read of this tile is done: release it
+      tc::fence_before_sync();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(tmem_empty_bar);
+    }
+    if (lane == 0) bulk_wait_read1();  // the store from this slot (box j - 2) has read it
+    __syncwarp();
+#pragma unroll
+    for (int g = 0; g < 8; ++g) {
+      uint4 u;
+      u.x = pack2(__uint_as_float(r[g * 8 + 0]), __uint_as_float(r[g * 8 + 1]));
+      u.y = pack2(__uint_as_float(r[g * 8 + 2]), __uint_as_float(r[g * 8 + 3]));
+      u.z = pack2(__uint_as_float(r[g * 8 + 4]), __uint_as_float(r[g * 8 + 5]));
+      u.w = pack2(__uint_as_float(r[g * 8 + 6]), __uint_as_float(r[g * 8 + 7]));
+      *reinterpret_cast<uint4*>(box + lane * 128 + ((g ^ (lane & 7)) << 4)) = u;
+    }
+    tc::fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_3d(tmC, nb * BN + j * 64, mb * BM + q * 32, e, tc::smem_u32(box));
+      bulk_commit();
+    }
+  }
+}
+
 template <int KIND>
 struct Tiles {
   // dgrad: row tiles of each expert x N tiles; wgrad: M tiles x N tiles per expert
-  MOE_D static void decode(const SmemCtl& c, int E, int mt, int nt, int tile, int& e, int& mb,
+  template <typename Ctl>
+  MOE_D static void decode(const Ctl& c, int E, int mt, int nt, int tile, int& e, int& mb,
                            int& nb) {
     if (KIND == kWgrad) {
       const int tpe = mt * nt;
@@ -140,14 +206,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_tc_bwd_kernel(const __grid_constant__ CUtensorMap tmA,
                                const __grid_constant__ CUtensorMap tmB,
                                const __grid_constant__ CUtensorMap tmC, const BwdParams p) {
-  constexpr int STAGES = stages_of<KIND>();
+  constexpr int STAGES = BwdCfg<KIND>::STAGES;
+  constexpr int BK = BwdCfg<KIND>::BK;
+  constexpr int A_BYTES = BwdCfg<KIND>::A_BYTES;
+  constexpr int B_BYTES = BwdCfg<KIND>::B_BYTES;
+  constexpr int STAGE_BYTES = BwdCfg<KIND>::STAGE_BYTES;
+  constexpr int ATOM = BwdCfg<KIND>::ATOM;
+  using Ctl = SmemCtl<STAGES, BwdCfg<KIND>::NTS>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* sA = smem;
   uint8_t* sB = smem + STAGES * A_BYTES;
-  uint8_t* sC = smem + STAGES * STAGE_BYTES;  // wgrad output staging (64 KB)
-  SmemCtl& ctl = *reinterpret_cast<SmemCtl*>(sC + (KIND == kWgrad ? STAGING_BYTES : 0));
+  uint8_t* sC = smem + STAGES * STAGE_BYTES;  // wgrad output staging (32 KB)
+  Ctl& ctl = *reinterpret_cast<Ctl*>(sC + (KIND == kWgrad ? STAGING_BYTES : 0));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int E = p.E;
   const int nt = (p.N + BN - 1) / BN;
@@ -179,7 +251,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   if (warp == 2) {
     if (KIND == kWgrad) {
-      if (lane == 0) ctl.tile_start[E] = E * mt * nt;
+      if (lane == 0) ctl.total = E * mt * nt;
     } else {
       int running = 0;
       for (int e0 = 0; e0 < E; e0 += 32) {
@@ -194,14 +266,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (e < E) ctl.tile_start[e] = running + incl - v;
         running += __shfl_sync(0xffffffffu, incl, 31);
       }
-      if (lane == 0) ctl.tile_start[E] = running;
+      if (lane == 0) ctl.total = running;
     }
   }
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem_base = ctl.tmem_base;
-  const int total = ctl.tile_start[E];
+  const int total = ctl.total;
   tc::WaitCtl wc{p.status, &ctl.abort, p.wait_limit_ns, 0};
   tc::WaitCtl wdrain{p.status, nullptr, 1000000000ull, 0};
 
@@ -324,47 +396,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
       int e, mb, nb;
       Tiles<KIND>::decode(ctl, E, mt, nt, tile, e, mb, nb);
+      const int m_e = ctl.off[e + 1] - ctl.off[e];
       if (!tc::mbar_wait(tc::smem_u32(&ctl.tmem_full[acc]), acc_phase, wc)) break;
       tc::fence_after_sync();
-      const int m_e = ctl.off[e + 1] - ctl.off[e];
       const uint32_t tbase = tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(q * 32) << 16);
       if (KIND == kWgrad) {
-        // this warp's 32 rows x 256 columns go to 4 swizzled {64 col, 32 row}
-        // boxes in shared memory (row `lane`, 16-B chunk c at c ^ (lane & 7)),
-        // then one lane stores them with TMA (rows past M are clipped).
-        uint8_t* box0 = sC + q * 4 * 4096;
-        if (lane == 0) bulk_wait_read0();  // the previous tile's stores have read the staging
-        __syncwarp();
-#pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
-          uint32_t r[32];
-          if (m_e > 0) {
-            tc::tmem_ld_32x32b_x32(tbase + c * 32, r);
-          } else {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) r[i] = 0u;
-          }
-          uint8_t* row = box0 + (c >> 1) * 4096 + lane * 128;
-#pragma unroll
-          for (int g = 0; g < 4; ++g) {
-            const int chunk = (c & 1) * 4 + g;
-            uint4 u;
-            u.x = pack2(__uint_as_float(r[g * 8 + 0]), __uint_as_float(r[g * 8 + 1]));
-            u.y = pack2(__uint_as_float(r[g * 8 + 2]), __uint_as_float(r[g * 8 + 3]));
-            u.z = pack2(__uint_as_float(r[g * 8 + 4]), __uint_as_float(r[g * 8 + 5]));
-            u.w = pack2(__uint_as_float(r[g * 8 + 6]), __uint_as_float(r[g * 8 + 7]));
-            *reinterpret_cast<uint4*>(row + ((chunk ^ (lane & 7)) << 4)) = u;
-          }
-        }
-        tc::fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-#pragma unroll
-          for (int j = 0; j < 4; ++j)
-            tma_store_3d(&tmC, nb * BN + j * 64, mb * BM + q * 32, e,
-                         tc::smem_u32(box0 + j * 4096));
-          bulk_commit();
-        }
+        wgrad_store_tile(tbase, m_e > 0, e, mb, nb, q, lane, sC, &tmC,
+                         tc::smem_u32(&ctl.tmem_empty[acc]));
       } else {
         const int local_row = mb * BM + q * 32 + lane;
         const bool valid = local_row < m_e;
@@ -405,10 +443,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         if (KIND == kDgradSwiGLU && valid && p.dprob_part) p.dprob_part[row * nt + nb] = dpr;
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(tc::smem_u32(&ctl.tmem_empty[acc]));
       }
-      tc::fence_before_sync();
-      __syncwarp();
-      if (lane == 0) tc::mbar_arrive(tc::smem_u32(&ctl.tmem_empty[acc]));
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1;
     }
@@ -496,15 +534,16 @@ cudaError_t launch_tc_wgrad(int rows, const void* A, int M, const void* B, int N
                             cudaStream_t s) {
   CUtensorMap ma, mb;
   const uint64_t r = rows > 0 ? (uint64_t)rows : 1;  // a map needs a non-empty extent
-  if (!encode_map(&ma, A, 0, r, (uint64_t)M, 64)) return cudaErrorInvalidValue;
-  if (!encode_map(&mb, B, 0, r, (uint64_t)N, 64)) return cudaErrorInvalidValue;
+  constexpr uint32_t kbox = BwdCfg<kWgrad>::BK;
+  if (!encode_map(&ma, A, 0, r, (uint64_t)M, kbox)) return cudaErrorInvalidValue;
+  if (!encode_map(&mb, B, 0, r, (uint64_t)N, kbox)) return cudaErrorInvalidValue;
   BwdParams p{};
   p.offsets = offsets; p.out = static_cast<__nv_bfloat16*>(out);
   p.E = E; p.Kd = 0; p.M = M; p.N = N; p.status = status; p.wait_limit_ns = 2000000000ull;
-  const int64_t tiles = (int64_t)E * ceil_div(M, BM) * ceil_div(N, BN);
-  const int grid = (int)(tiles < sms ? tiles : sms);
   CUtensorMap mc;  // the output dW [E][M][N], stored in {64, 32, 1} boxes
   if (!encode_map(&mc, out, (uint64_t)E, (uint64_t)M, (uint64_t)N, 32)) return cudaErrorInvalidValue;
+  const int64_t tiles = (int64_t)E * ceil_div(M, BM) * ceil_div(N, BN);
+  const int grid = (int)(tiles < sms ? tiles : sms);
   return launch_kind<kWgrad>(ma, mb, mc, p, grid, s);
 }
 

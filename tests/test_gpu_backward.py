@@ -23,6 +23,8 @@ def _bits(t):
     (300, 200, 5, 2, 136, True),
     (400, 256, 64, 8, 128, False),
     (700, 128, 1, 1, 256, False),
+    # experts on both sides of the resident-panel limit (256 rows) in one call
+    (2000, 128, 8, 1, 64, False),
 ])
 def test_grouped_mlp_backward_matches_oracle(T, h, E, K, F, skew):
     M = lib()
