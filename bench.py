@@ -48,6 +48,8 @@ def parse():
     p.add_argument("--workload", default=None, help="workload name (default: the Mixtral-shaped layer)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-mxfp8", action="store_true",
+                   help="skip the MXFP8 expert-MLP measurement reported beside the bf16 line")
     p.add_argument("--gather", action="store_true",
                    help="time the forward with the gather-fused FC1 (no x_perm) instead of the "
                         "x_perm scatter")
@@ -281,6 +283,68 @@ def traffic_record(w):
     if not rec or rec.get("kernel_hash") != kernel_hash():
         return None
     return rec.get("fc1_bytes_per_launch")
+
+
+def time_mxfp8(M, torch, w, cfg, x_perm, offsets, perm_prob, w1, w2, flush_buf, hold, stream,
+               steps):
+    """The expert MLP in MXFP8 on the timed step's own dispatch (x_perm,
+    offsets, perm_prob as the last step left them): quantise x_perm, FC1 with
+    the SwiGLU epilogue writing a in MXFP8, FC2; the weights are quantised once
+    beforehand (timed on their own).  Device times with CUDA events, L2 flushed
+    before every iteration."""
+    T, h, E, K, F = w.T, w.h, w.E, w.K, w.F
+    P = T * K
+    dev = x_perm.device
+    u8 = dict(dtype=torch.uint8, device=dev)
+    R1 = 2 * F
+    w1q, w1sf = torch.empty(E * R1, h, **u8), torch.empty(M.moe_mxfp8_scale_bytes(E * R1, h, E), **u8)
+    w2q, w2sf = torch.empty(E * h, F, **u8), torch.empty(M.moe_mxfp8_scale_bytes(E * h, F, E), **u8)
+    xq, xsf = torch.empty(P, h, **u8), torch.empty(M.moe_mxfp8_scale_bytes(P, h, E), **u8)
+    aq, asf = torch.empty(P, F, **u8), torch.empty(M.moe_mxfp8_scale_bytes(P, F, E), **u8)
+    y_mx = torch.empty(P, h, dtype=torch.bfloat16, device=dev)
+
+    def ev():
+        return torch.cuda.Event(enable_timing=True)
+
+    wq0, wq1 = ev(), ev()
+    flush_buf.fill_(1)
+    wq0.record(stream)
+    M.moe_mxfp8_quantize(E * R1, h, E, None, w1, w1q, w1sf)
+    M.moe_mxfp8_quantize(E * h, F, E, None, w2, w2q, w2sf)
+    wq1.record(stream)
+
+    def run(marks=None):
+        def mark(i):
+            if marks is not None:
+                marks[i].record(stream)
+        mark(0)
+        M.moe_mxfp8_quantize(P, h, E, offsets, x_perm, xq, xsf)
+        mark(1)
+        M.moe_expert_fc1_mxfp8(cfg, xq, xsf, offsets, perm_prob, w1q, w1sf, None, aq, asf)
+        mark(2)
+        M.moe_expert_fc2_mxfp8(cfg, aq, asf, offsets, w2q, w2sf, y_mx)
+        mark(3)
+
+    for _ in range(3):
+        flush_buf.fill_(1)
+        run()
+    torch.cuda.synchronize()
+    marks = [[ev() for _ in range(4)] for _ in range(steps)]
+    for i in range(steps):
+        flush_buf.fill_(1)
+        hold()
+        run(marks[i])
+    torch.cuda.synchronize()
+    st = M.moe_get_error()
+    if st != M.MOE_OK:
+        raise RuntimeError(f"device status after the MXFP8 steps: {M.moe_status_string(st)}")
+    t = [statistics.mean(m[j].elapsed_time(m[j + 1]) for m in marks) for j in range(3)]
+    out = {"quantize_x_ms": t[0], "fc1_ms": t[1], "fc2_ms": t[2], "expert_mlp_ms": sum(t),
+           "weight_quantize_ms": wq0.elapsed_time(wq1),
+           "how": "moe_mxfp8_quantize(x_perm) + moe_expert_fc1_mxfp8 (SwiGLU, a written in "
+                  "MXFP8) + moe_expert_fc2_mxfp8 on the timed step's dispatch; weights "
+                  "quantised once (weight_quantize_ms); not part of the headline value"}
+    return out
 
 
 def run_ours(args, w):
@@ -566,6 +630,12 @@ def run_ours(args, w):
                "how": "moe_layer_fwd per step; tokens copied in from pinned host memory and the "
                       "output copied back every step, on a copy stream overlapped with compute"}
 
+    mx = None
+    if (not train and not args.no_mxfp8 and w.dtype == "bf16" and w.act == 1
+            and not w.has_bias and h % 128 == 0 and F % 128 == 0):
+        mx = time_mxfp8(M, torch, w, cfg, x_perm, offsets, perm_prob, w1, w2, flush_buf, hold,
+                        stream, args.steps)
+
     if rank != 0:
         if world > 1:
             torch.distributed.destroy_process_group()
@@ -623,6 +693,17 @@ def run_ours(args, w):
         line["route_ms"] = stage_ms["route"]
         # the router reads every token row once (its weight stays in L2/shared memory)
         line["route_pct_hbm"] = 100.0 * (T * h * esz) / (stage_ms["route"] / 1000.0) / 1e9 / pk["hbm_gbs"]
+        if mx is not None:
+            # FP8 tensor peak: the measured bf16 burst x the nominal fp8/bf16 ratio (4.5 / 2.25)
+            fp8_peak = 2.0 * peak_tf
+            mx["fc1_tflops"] = fc1_flops / (mx["fc1_ms"] / 1000.0) / 1e12
+            mx["fc2_tflops"] = fc2_flops / (mx["fc2_ms"] / 1000.0) / 1e12
+            mx["fp8_peak_tflops"] = fp8_peak
+            mx["fp8_peak_kind"] = f"{pk_kind} bf16 burst x 2 (nominal fp8/bf16 ratio)"
+            mx["fc1_frac_fp8_peak"] = mx["fc1_tflops"] / fp8_peak
+            mx["expert_gemms_speedup_vs_bf16"] = ((stage_ms["fc1"] + stage_ms["fc2"])
+                                                  / (mx["fc1_ms"] + mx["fc2_ms"]))
+            line["mxfp8"] = mx
     if not args.no_cpu_baseline:
         S = args.sample_tokens or auto_sample(w)
         samp = OracleSample(w, S)

@@ -221,6 +221,63 @@ moe_status_t moe_expert_fc1_gather(const moe_config_t* cfg, const void* x,
                                    const float* perm_prob, const void* w1, const void* b1,
                                    void* act_save, void* a, moe_stream_t stream);
 
+/* ---- MXFP8 expert GEMMs (review §5.3.3 "MXFP8 (Blackwell)") ----------------
+ * Activations and weights quantised in 1 x 32 blocks along the GEMM's K
+ * dimension, each block one E8M0 scale, elements FP8 E4M3 (OCP Microscaling
+ * v1.0: X = floor(log2 max|x|) - 8, element = x / 2^X rounded to nearest even,
+ * saturated to +-448); the GEMMs run as block-scaled tensor-core MMAs with
+ * fp32 accumulation.  Forward only, SwiGLU experts without biases.
+ *
+ * MXFP8 tensor format: codes [rows, K] uint8 (E4M3, row-major) and a scale
+ * buffer of moe_mxfp8_scale_bytes(rows, K, groups) bytes.  The rows form
+ * groups (experts); each group's rows are cut into 128-row tiles, numbered
+ * group after group; the scales of tile t and K columns kb*128..kb*128+127
+ * form one 512-byte atom at byte (t * K/128 + kb) * 512, where row i of the
+ * tile (i = 0..127), block j (j = 0..3) sits at byte 16 (i % 32) + 4 (i / 32)
+ * + j.  K must be a multiple of 128.  Scale bytes of rows past a group's end
+ * inside its last tile are unspecified.
+ *
+ * Errors: NULL or 16-byte-misaligned tensors -> MOE_ERR_INVALID_ARG; K or the
+ * config's h / F not multiples of 128, act not SwiGLU, has_bias, fp32 dtype ->
+ * MOE_ERR_UNSUPPORTED; bounded-wait timeouts on the device -> reported by
+ * moe_get_error. */
+
+/* Bytes of the scale buffer of an MXFP8 tensor of `rows` rows in `groups`
+ * groups with K columns (K a multiple of 128); 0 on bad arguments. */
+size_t moe_mxfp8_scale_bytes(int64_t rows, int32_t K, int32_t groups);
+
+/* Quantise x [rows, K] bf16 (device) to MXFP8: codes q [rows, K] and scales sf
+ * (device, caller-owned).  offsets [groups+1] (device): group g holds rows
+ * offsets[g] .. offsets[g+1]-1 (rows outside every group get codes but no
+ * scales); NULL: groups of rows/groups rows each (rows % groups == 0), as for
+ * expert weights [E][N][K].  Deterministic and exact: the decisions depend
+ * only on the bf16 values. */
+moe_status_t moe_mxfp8_quantize(int64_t rows, int32_t K, int32_t groups, const int32_t* offsets,
+                                const void* x, uint8_t* q, uint8_t* sf, moe_stream_t stream);
+
+/* MXFP8 FC1 with the SwiGLU epilogue: H = x_perm W1_e^T over the dequantised
+ * operands (fp32), a[r] = p_r silu(H[r, :F]) H[r, F:] (p_r = perm_prob[r], 1
+ * when NULL).  Outputs, any non-NULL subset:
+ *   a [P,F] bf16;  a_q [P,F] + a_sf = a quantised to MXFP8 from fp32 (blocks
+ *   along F, groups = the experts of `offsets`), FC2's left operand.
+ *   x_q [P,h] + x_sf: x_perm in MXFP8 (groups = experts, from offsets);
+ *   w1_q [E*2F, h] + w1_sf: W1 in MXFP8 (uniform groups of 2F rows).
+ * cfg gives T, K (P = T*K rows), h, E, F; offsets [E+1] as from moe_permute. */
+moe_status_t moe_expert_fc1_mxfp8(const moe_config_t* cfg, const uint8_t* x_q,
+                                  const uint8_t* x_sf, const int32_t* offsets,
+                                  const float* perm_prob, const uint8_t* w1_q,
+                                  const uint8_t* w1_sf, void* a, uint8_t* a_q, uint8_t* a_sf,
+                                  moe_stream_t stream);
+
+/* MXFP8 FC2: y_perm[r] = a[r] W2_e^T over the dequantised operands, bf16 out.
+ *   a_q [P,F] + a_sf (from moe_expert_fc1_mxfp8 or moe_mxfp8_quantize with the
+ *   experts' offsets); w2_q [E*h, F] + w2_sf (uniform groups of h rows);
+ *   y_perm [P,h] out. */
+moe_status_t moe_expert_fc2_mxfp8(const moe_config_t* cfg, const uint8_t* a_q,
+                                  const uint8_t* a_sf, const int32_t* offsets,
+                                  const uint8_t* w2_q, const uint8_t* w2_sf, void* y_perm,
+                                  moe_stream_t stream);
+
 /* Combine (review §2.1 "Combine"; the skill page's index_add_):
  *   y[t] = sum_{k=0}^{K-1} w[t,k] * y_perm[dst_row[t,k]]  (+ shared_y[t])
  * with w = topk_prob, or 1 when topk_prob is NULL (probabilities already

@@ -46,6 +46,13 @@ cudaError_t launch_dense_router_wgrad(const moe_config_t&, const float*, const v
                                       float*, cudaStream_t);
 cudaError_t launch_dense_router_dx(const moe_config_t&, const float*, const float*, float*,
                                    cudaStream_t);
+size_t mxfp8_scale_bytes(int64_t rows, int K, int groups);
+cudaError_t launch_mxfp8_quantize(int, int, int, const int32_t*, const void*, uint8_t*, uint8_t*,
+                                  int, cudaStream_t);
+cudaError_t launch_grouped_gemm_mxfp8(bool, int, const uint8_t*, const uint8_t*, int,
+                                      const uint8_t*, const uint8_t*, int, int, int,
+                                      const int32_t*, const float*, void*, uint8_t*, uint8_t*,
+                                      int, int*, cudaStream_t);
 }  // namespace moe
 
 using namespace moe;
@@ -366,6 +373,78 @@ moe_status_t moe_expert_fc2(const moe_config_t* cfg, const void* a, const int32_
   return cuda_status(run_expert_gemm(*cfg, 2, cfg->T * cfg->K, a, offsets, perm_prob, w2,
                                      cfg->has_bias ? b2 : nullptr, nullptr, y_perm, d,
                                      static_cast<cudaStream_t>(stream)));
+}
+
+size_t moe_mxfp8_scale_bytes(int64_t rows, int32_t K, int32_t groups) {
+  if (rows < 0 || K <= 0 || K % 128 || groups < 1) return 0;
+  return mxfp8_scale_bytes(rows, K, groups);
+}
+
+moe_status_t moe_mxfp8_quantize(int64_t rows, int32_t K, int32_t groups, const int32_t* offsets,
+                                const void* x, uint8_t* q, uint8_t* sf, moe_stream_t stream) {
+  if (rows < 0 || rows > INT32_MAX || K <= 0 || groups < 1 || groups > 256)
+    return MOE_ERR_INVALID_ARG;
+  if (K % 128) return MOE_ERR_UNSUPPORTED;
+  if (!offsets && rows % groups) return MOE_ERR_INVALID_ARG;
+  if (rows == 0) return MOE_OK;
+  if (!x || !q || !sf || !al16(x) || !al16(q) || !al16(sf)) return MOE_ERR_INVALID_ARG;
+  const DeviceInfo* d = device_info();
+  if (!d) return MOE_ERR_CUDA;
+  return cuda_status(launch_mxfp8_quantize((int)rows, K, groups, offsets, x, q, sf, d->sms,
+                                           static_cast<cudaStream_t>(stream)));
+}
+
+namespace {
+moe_status_t check_mxfp8(const moe_config_t* cfg) {
+  moe_status_t st = check_config(cfg);
+  if (st != MOE_OK) return st;
+  if (cfg->dtype != MOE_BF16 || cfg->act != MOE_ACT_SWIGLU || cfg->has_bias || cfg->h % 128 ||
+      cfg->F % 128)
+    return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+}  // namespace
+
+moe_status_t moe_expert_fc1_mxfp8(const moe_config_t* cfg, const uint8_t* x_q,
+                                  const uint8_t* x_sf, const int32_t* offsets,
+                                  const float* perm_prob, const uint8_t* w1_q,
+                                  const uint8_t* w1_sf, void* a, uint8_t* a_q, uint8_t* a_sf,
+                                  moe_stream_t stream) {
+  moe_status_t st = check_mxfp8(cfg);
+  if (st != MOE_OK) return st;
+  if (!x_q || !x_sf || !offsets || !w1_q || !w1_sf) return MOE_ERR_INVALID_ARG;
+  if (!a && !a_q) return MOE_ERR_INVALID_ARG;
+  if (!a_q != !a_sf) return MOE_ERR_INVALID_ARG;
+  if (!al16(x_q) || !al16(x_sf) || !al16(w1_q) || !al16(w1_sf) || !al16(a) || !al16(a_q) ||
+      !al16(a_sf))
+    return MOE_ERR_INVALID_ARG;
+  if (cfg->flags & MOE_FLAG_VALIDATE_ONLY) return MOE_OK;
+  const DeviceInfo* d = device_info();
+  if (!d) return MOE_ERR_CUDA;
+  const moe_config_t& c = *cfg;
+  return cuda_status(launch_grouped_gemm_mxfp8(true, c.T * c.K, x_q, x_sf, c.h, w1_q, w1_sf,
+                                               2 * c.F, c.E, c.F, offsets, perm_prob, a, a_q, a_sf,
+                                               d->sms, d->status,
+                                               static_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_expert_fc2_mxfp8(const moe_config_t* cfg, const uint8_t* a_q,
+                                  const uint8_t* a_sf, const int32_t* offsets,
+                                  const uint8_t* w2_q, const uint8_t* w2_sf, void* y_perm,
+                                  moe_stream_t stream) {
+  moe_status_t st = check_mxfp8(cfg);
+  if (st != MOE_OK) return st;
+  if (!a_q || !a_sf || !offsets || !w2_q || !w2_sf || !y_perm) return MOE_ERR_INVALID_ARG;
+  if (!al16(a_q) || !al16(a_sf) || !al16(w2_q) || !al16(w2_sf) || !al16(y_perm))
+    return MOE_ERR_INVALID_ARG;
+  if (cfg->flags & MOE_FLAG_VALIDATE_ONLY) return MOE_OK;
+  const DeviceInfo* d = device_info();
+  if (!d) return MOE_ERR_CUDA;
+  const moe_config_t& c = *cfg;
+  return cuda_status(launch_grouped_gemm_mxfp8(false, c.T * c.K, a_q, a_sf, c.F, w2_q, w2_sf, c.h,
+                                               c.E, c.h, offsets, nullptr, y_perm, nullptr,
+                                               nullptr, d->sms, d->status,
+                                               static_cast<cudaStream_t>(stream)));
 }
 
 moe_status_t moe_unpermute_combine(const moe_config_t* cfg, const void* y_perm,

@@ -172,6 +172,47 @@ MOE_D void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t id
       : "memory");
 }
 
+// ---- block-scaled MMA (kind::mxf8f6f4) ------------------------------------------
+// Instruction descriptor for E4M3 x E4M3 -> fp32 with E8M0 scales, both
+// operands K-major: B scale id in bits 4-5, A/B formats (E4M3 = 0) in 7-9 /
+// 10-12, N >> 3 in 17-22, scale format UE8M0 (1) in bit 23, M >> 4 in 24-28,
+// A scale id in 29-30.  The scale id picks the byte of each 32-bit TMEM scale
+// word (one 32-element K block per MMA of K = 32).
+MOE_HD constexpr uint32_t idesc_mxf8_e4m3(int M, int N, int sfa_id, int sfb_id) {
+  return ((uint32_t)sfb_id << 4) | ((uint32_t)(N >> 3) << 17) | (1u << 23) |
+         ((uint32_t)(M >> 4) << 24) | ((uint32_t)sfa_id << 29);
+}
+
+MOE_D void mma_mxf8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                    uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], "
+      "[%5], p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+// Shared-memory descriptor of one 512-byte scale atom as the source of a
+// tcgen05.cp 32x128b: 32 rows of 16 bytes, no swizzle, 8-row core-matrix
+// groups 128 bytes apart.
+MOE_D uint64_t desc_sf_atom(uint32_t addr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((addr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)(128u >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  return d;
+}
+
+// Copy 32 rows x 128 bits from shared memory into TMEM columns taddr ..
+// taddr + 3 of all four lane quarters (row r to lane r of each quarter).
+// Ordered before later tcgen05.mma of the same thread.
+MOE_D void tmem_cp_32x128b_warpx4(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
+               : "memory");
+}
+
 // Arrive on `bar` once every tcgen05.mma issued so far by this thread is done.
 MOE_D void mma_commit(uint32_t bar) {
   asm volatile(

@@ -60,6 +60,11 @@ _SIG = {
     "moe_expert_fc1": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P, _P, _P]),
     "moe_expert_fc2": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P, _P]),
     "moe_expert_fc1_gather": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "moe_mxfp8_scale_bytes": (ctypes.c_size_t, [ctypes.c_int64, ctypes.c_int32, ctypes.c_int32]),
+    "moe_mxfp8_quantize": (ctypes.c_int, [ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, _P, _P,
+                                          _P, _P, _P]),
+    "moe_expert_fc1_mxfp8": (ctypes.c_int, [_CFG] + [_P] * 10),
+    "moe_expert_fc2_mxfp8": (ctypes.c_int, [_CFG] + [_P] * 7),
     "moe_unpermute_combine": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P]),
     "moe_layer_fwd": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                      ctypes.c_size_t, _P]),
@@ -208,6 +213,29 @@ def moe_expert_fc1_gather(cfg, x, src_token, offsets, perm_prob, w1, b1, act_sav
 def moe_expert_fc2(cfg, a, offsets, perm_prob, w2, b2, y_perm, stream=None):
     _check("moe_expert_fc2", _lib.moe_expert_fc2(
         ctypes.byref(cfg), _ptr(a), _ptr(offsets), _ptr(perm_prob), _ptr(w2), _ptr(b2),
+        _ptr(y_perm), _stream(stream)))
+
+
+def moe_mxfp8_scale_bytes(rows, K, groups) -> int:
+    return int(_lib.moe_mxfp8_scale_bytes(int(rows), int(K), int(groups)))
+
+
+def moe_mxfp8_quantize(rows, K, groups, offsets, x, q, sf, stream=None):
+    _check("moe_mxfp8_quantize", _lib.moe_mxfp8_quantize(
+        int(rows), int(K), int(groups), _ptr(offsets), _ptr(x), _ptr(q), _ptr(sf),
+        _stream(stream)))
+
+
+def moe_expert_fc1_mxfp8(cfg, x_q, x_sf, offsets, perm_prob, w1_q, w1_sf, a, a_q, a_sf,
+                         stream=None):
+    _check("moe_expert_fc1_mxfp8", _lib.moe_expert_fc1_mxfp8(
+        ctypes.byref(cfg), _ptr(x_q), _ptr(x_sf), _ptr(offsets), _ptr(perm_prob), _ptr(w1_q),
+        _ptr(w1_sf), _ptr(a), _ptr(a_q), _ptr(a_sf), _stream(stream)))
+
+
+def moe_expert_fc2_mxfp8(cfg, a_q, a_sf, offsets, w2_q, w2_sf, y_perm, stream=None):
+    _check("moe_expert_fc2_mxfp8", _lib.moe_expert_fc2_mxfp8(
+        ctypes.byref(cfg), _ptr(a_q), _ptr(a_sf), _ptr(offsets), _ptr(w2_q), _ptr(w2_sf),
         _ptr(y_perm), _stream(stream)))
 
 

@@ -108,3 +108,31 @@ def test_other_entry_points_validate(M):
     assert M.raw("moe_grouped_mlp_fwd")(ctypes.byref(gelu_b), P, P, P, P, None, P, None, None, P,
                                         P, big, None) == 1
     assert M.raw("moe_test_bounded_wait")(0, None) == 1
+
+
+def test_mxfp8_argument_checks(M):
+    assert M.moe_mxfp8_scale_bytes(1000, 256, 4) == (8 + 4) * 2 * 512
+    assert M.moe_mxfp8_scale_bytes(4096 * 4, 7168, 256 // 256) == (128 + 1) * 56 * 512
+    assert M.moe_mxfp8_scale_bytes(10, 100, 1) == 0      # K not a multiple of 128
+    assert M.moe_mxfp8_scale_bytes(10, 128, 0) == 0
+    q = M.raw("moe_mxfp8_quantize")
+    P = 1 << 20  # fake aligned addresses: validation fails (or returns) first
+    assert q(10, 96, 1, None, P, P, P, None) == M.MOE_ERR_UNSUPPORTED
+    assert q(10, 128, 3, None, P, P, P, None) == M.MOE_ERR_INVALID_ARG  # 10 % 3 != 0
+    assert q(10, 128, 1, None, None, P, P, None) == M.MOE_ERR_INVALID_ARG
+    assert q(10, 128, 1, None, P + 8, P, P, None) == M.MOE_ERR_INVALID_ARG
+    assert q(0, 128, 1, None, None, None, None, None) == M.MOE_OK
+    assert q(10, 128, 300, P, P, P, P, None) == M.MOE_ERR_INVALID_ARG   # > 256 groups
+    f1 = M.raw("moe_expert_fc1_mxfp8")
+    f2 = M.raw("moe_expert_fc2_mxfp8")
+    ok = _cfg(M, flags=M.MOE_FLAG_RENORM | M.MOE_FLAG_VALIDATE_ONLY)
+    assert f1(ctypes.byref(ok), P, P, P, None, P, P, P, None, None, None) == M.MOE_OK
+    assert f1(ctypes.byref(ok), P, P, P, None, P, P, None, P, P, None) == M.MOE_OK
+    assert f1(ctypes.byref(ok), P, P, P, None, P, P, None, None, None, None) == M.MOE_ERR_INVALID_ARG
+    assert f1(ctypes.byref(ok), P, P, P, None, P, P, None, P, None, None) == M.MOE_ERR_INVALID_ARG
+    assert f2(ctypes.byref(ok), P, P, P, P, P, P, None) == M.MOE_OK
+    assert f2(ctypes.byref(ok), P, None, P, P, P, P, None) == M.MOE_ERR_INVALID_ARG
+    for kw in (dict(act=M.MOE_ACT_GELU), dict(F=192), dict(h=200), dict(dtype=M.MOE_F32, h=128)):
+        bad = _cfg(M, flags=M.MOE_FLAG_RENORM | M.MOE_FLAG_VALIDATE_ONLY, **kw)
+        assert f1(ctypes.byref(bad), P, P, P, None, P, P, P, None, None, None) == M.MOE_ERR_UNSUPPORTED
+        assert f2(ctypes.byref(bad), P, P, P, P, P, P, None) == M.MOE_ERR_UNSUPPORTED
