@@ -255,6 +255,21 @@ size_t moe_mxfp8_scale_bytes(int64_t rows, int32_t K, int32_t groups);
 moe_status_t moe_mxfp8_quantize(int64_t rows, int32_t K, int32_t groups, const int32_t* offsets,
                                 const void* x, uint8_t* q, uint8_t* sf, moe_stream_t stream);
 
+/* Dispatch with the MXFP8 quantisation fused in: the maps of moe_permute
+ * (counts, offsets, dst_row, src_token, perm_prob; same rules, capacity
+ * included) and, instead of x_perm, x_perm in MXFP8 -- x_q [P,h] codes and
+ * x_sf scales (moe_mxfp8_scale_bytes(T*K, h, E) bytes, groups = the experts of
+ * `offsets`).  Each token row is read and quantised once (blocks along h) and
+ * its codes and scales written to its K rows: the same bytes as
+ * moe_permute followed by moe_mxfp8_quantize(offsets), in one pass over x.
+ * bf16 configurations with h % 128 == 0, else MOE_ERR_UNSUPPORTED; ws as for
+ * moe_permute.  Rows of dropped slots are not written. */
+moe_status_t moe_permute_mxfp8(const moe_config_t* cfg, const void* x, const int32_t* topk_idx,
+                               const float* topk_prob, uint8_t* x_q, uint8_t* x_sf,
+                               int32_t* counts, int32_t* offsets, int32_t* dst_row,
+                               int32_t* src_token, float* perm_prob, void* ws, size_t ws_bytes,
+                               moe_stream_t stream);
+
 /* MXFP8 FC1 with the SwiGLU epilogue: H = x_perm W1_e^T over the dequantised
  * operands (fp32), a[r] = p_r silu(H[r, :F]) H[r, F:] (p_r = perm_prob[r], 1
  * when NULL).  Outputs, any non-NULL subset:

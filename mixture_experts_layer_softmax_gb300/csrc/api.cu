@@ -49,6 +49,9 @@ cudaError_t launch_dense_router_dx(const moe_config_t&, const float*, const floa
 size_t mxfp8_scale_bytes(int64_t rows, int K, int groups);
 cudaError_t launch_mxfp8_quantize(int, int, int, const int32_t*, const void*, uint8_t*, uint8_t*,
                                   int, cudaStream_t);
+cudaError_t launch_scatter_quantize(const moe_config_t&, const void*, const int32_t*,
+                                    const int32_t*, const int32_t*, uint8_t*, uint8_t*, int, int*,
+                                    cudaStream_t);
 cudaError_t launch_grouped_gemm_mxfp8(bool, int, const uint8_t*, const uint8_t*, int,
                                       const uint8_t*, const uint8_t*, int, int, int,
                                       const int32_t*, const float*, void*, uint8_t*, uint8_t*,
@@ -392,6 +395,33 @@ moe_status_t moe_mxfp8_quantize(int64_t rows, int32_t K, int32_t groups, const i
   if (!d) return MOE_ERR_CUDA;
   return cuda_status(launch_mxfp8_quantize((int)rows, K, groups, offsets, x, q, sf, d->sms,
                                            static_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_permute_mxfp8(const moe_config_t* cfg, const void* x, const int32_t* topk_idx,
+                               const float* topk_prob, uint8_t* x_q, uint8_t* x_sf,
+                               int32_t* counts, int32_t* offsets, int32_t* dst_row,
+                               int32_t* src_token, float* perm_prob, void* ws, size_t ws_bytes,
+                               moe_stream_t stream) {
+  moe_status_t st = check_config(cfg);
+  if (st != MOE_OK) return st;
+  if (cfg->dtype != MOE_BF16 || cfg->h % 128) return MOE_ERR_UNSUPPORTED;
+  if (!counts || !offsets) return MOE_ERR_INVALID_ARG;
+  if (cfg->T > 0 && (!x || !topk_idx || !dst_row || !src_token || !x_q || !x_sf))
+    return MOE_ERR_INVALID_ARG;
+  if (!al16(x) || !al16(x_q) || !al16(x_sf)) return MOE_ERR_INVALID_ARG;
+  if ((st = check_ws(cfg, ws, ws_bytes)) != MOE_OK) return st;
+  if (cfg->flags & MOE_FLAG_VALIDATE_ONLY) return MOE_OK;
+  const DeviceInfo* d = device_info();
+  if (!d) return MOE_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const Workspace w = workspace_layout(*cfg);
+  cudaError_t e = launch_permute_maps(*cfg, topk_idx, topk_prob, at<int32_t>(ws, w.hist),
+                                      at<int32_t>(ws, w.chunk_base), counts, offsets, dst_row,
+                                      src_token, perm_prob, d->status, s);
+  if (e == cudaSuccess)
+    e = launch_scatter_quantize(*cfg, x, topk_idx, dst_row, offsets, x_q, x_sf, d->sms,
+                                d->status, s);
+  return cuda_status(e);
 }
 
 namespace {

@@ -208,6 +208,106 @@ __global__ void __launch_bounds__(256)
   }
 }
 
+// ---- dispatch with the quantisation fused in ------------------------------------
+// One warp per token (grid-stride): the token row x[t] (bf16, h columns) is
+// read once, quantised to MXFP8 (lanes 4j..4j+3 share a 32-value block, lanes
+// 16c..16c+15 a 128-column chunk), and its codes and scale words are written
+// to each of its K destination rows dst_row[t, k] of the permuted operand
+// (the scale atom of row r of expert e: tile rtile[e] + (r - off[e]) / 128).
+// Dropped slots (dst_row -1) are skipped; other out-of-range rows or expert
+// ids are reported (MOE_ERR_DEVICE_BOUNDS) and skipped.
+template <int KMAX>
+__global__ void __launch_bounds__(256)
+    scatter_quantize_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ idx,
+                            const int32_t* __restrict__ dst_row,
+                            const int32_t* __restrict__ offsets, int T, int K, int E, int h,
+                            uint8_t* __restrict__ q, uint8_t* __restrict__ sf, int* status) {
+  __shared__ int s_off[257], s_rt[257];
+  for (int g = threadIdx.x; g <= E; g += blockDim.x) s_off[g] = __ldg(offsets + g);
+  __syncthreads();
+  if (threadIdx.x < 32) {  // rtile = exclusive scan of ceil(rows_e / 128)
+    const int lane = threadIdx.x;
+    int running = 0;
+    for (int g0 = 0; g0 < E; g0 += 32) {
+      const int g = g0 + lane;
+      const int v = g < E ? (s_off[g + 1] - s_off[g] + 127) / 128 : 0;
+      int incl = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+      }
+      if (g < E) s_rt[g] = running + incl - v;
+      running += __shfl_sync(0xffffffffu, incl, 31);
+    }
+  }
+  __syncthreads();
+  const int lane = threadIdx.x & 31;
+  const int KB = h / BK;
+  const int nvec = h / 8;  // 16-byte vectors per row
+  const int64_t P = (int64_t)T * K;
+  constexpr int kMaxVec = 4;
+  for (int64_t t = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5); t < T; t += (int64_t)gridDim.x * 8) {
+    int64_t row[KMAX], atom0[KMAX];
+#pragma unroll
+    for (int k = 0; k < KMAX; ++k) {
+      row[k] = -1;
+      if (k < K) {
+        const int r = __ldg(dst_row + t * K + k);
+        const int e = __ldg(idx + t * K + k);
+        if (r >= 0 && r < P && e >= 0 && e < E && r >= s_off[e] && r < s_off[e + 1]) {
+          const int lr = r - s_off[e];
+          row[k] = r;
+          atom0[k] = atom_word(s_rt[e] + lr / 128, KB, 0, lr & 127);
+        } else if (r != -1) {
+          report(status, MOE_ERR_DEVICE_BOUNDS);
+        }
+      }
+    }
+    const __nv_bfloat16* src = x + t * h;
+    for (int v0 = 0; v0 < nvec; v0 += 32 * kMaxVec) {
+      uint4 raw[kMaxVec];
+#pragma unroll
+      for (int i = 0; i < kMaxVec; ++i) {
+        const int v = v0 + i * 32 + lane;
+        raw[i] = make_uint4(0, 0, 0, 0);
+        if (v < nvec) raw[i] = __ldg(reinterpret_cast<const uint4*>(src) + v);
+      }
+#pragma unroll
+      for (int i = 0; i < kMaxVec; ++i) {
+        const int v = v0 + i * 32 + lane;
+        const __nv_bfloat16* xv = reinterpret_cast<const __nv_bfloat16*>(&raw[i]);
+        float f[8], amax = 0.f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          f[j] = __bfloat162float(xv[j]);
+          amax = fmaxf(amax, fabsf(f[j]));
+        }
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+        const uint32_t code = e8m0_code(amax);
+        const float inv = e8m0_inverse(code);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) f[j] *= inv;
+        const uint2 c8 = e4m3x8(f);
+        const uint32_t c1 = __shfl_down_sync(0xffffffffu, code, 4);
+        const uint32_t c2 = __shfl_down_sync(0xffffffffu, code, 8);
+        const uint32_t c3 = __shfl_down_sync(0xffffffffu, code, 12);
+        const uint32_t word = code | (c1 << 8) | (c2 << 16) | (c3 << 24);
+        if (v < nvec) {
+#pragma unroll
+          for (int k = 0; k < KMAX; ++k) {
+            if (row[k] < 0) continue;
+            *reinterpret_cast<uint2*>(q + row[k] * h + (int64_t)v * 8) = c8;
+            if ((lane & 15) == 0)
+              *reinterpret_cast<uint32_t*>(sf + atom0[k] + (int64_t)(v >> 4) * ATOM) = word;
+          }
+        }
+      }
+    }
+  }
+}
+
 // ---- GEMM -------------------------------------------------------------------------
 MOE_D void decode_tile(const MxCtl& c, int E, int nblk, int tile, int& e, int& mb, int& nb) {
   int lo = 0, hi = E - 1;  // largest e with tile_start[e] <= tile
@@ -541,6 +641,23 @@ cudaError_t launch_mxfp8_quantize(int rows, int K, int groups, const int32_t* of
   const int grid = (int)(blocks < 8LL * sms ? blocks : 8LL * sms);
   mxfp8_quantize_kernel<<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(x), rows, K, groups,
                                              offsets, offsets ? 0 : rows / groups, q, sf);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_scatter_quantize(const moe_config_t& c, const void* x, const int32_t* idx,
+                                    const int32_t* dst_row, const int32_t* offsets, uint8_t* q,
+                                    uint8_t* sf, int sms, int* status, cudaStream_t s) {
+  if (c.T == 0) return cudaSuccess;
+  const int64_t need = ceil_div(c.T, 8);
+  const int grid = (int)(need < 8LL * sms ? need : 8LL * sms);
+  const __nv_bfloat16* xs = static_cast<const __nv_bfloat16*>(x);
+#define MOE_SQ(KM) \
+  scatter_quantize_kernel<KM><<<grid, 256, 0, s>>>(xs, idx, dst_row, offsets, c.T, c.K, c.E, c.h, q, sf, status)
+  if (c.K <= 2) MOE_SQ(2);
+  else if (c.K <= 4) MOE_SQ(4);
+  else if (c.K <= 8) MOE_SQ(8);
+  else MOE_SQ(16);
+#undef MOE_SQ
   return cudaGetLastError();
 }
 

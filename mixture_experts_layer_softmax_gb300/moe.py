@@ -63,6 +63,7 @@ _SIG = {
     "moe_mxfp8_scale_bytes": (ctypes.c_size_t, [ctypes.c_int64, ctypes.c_int32, ctypes.c_int32]),
     "moe_mxfp8_quantize": (ctypes.c_int, [ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, _P, _P,
                                           _P, _P, _P]),
+    "moe_permute_mxfp8": (ctypes.c_int, [_CFG] + [_P] * 11 + [ctypes.c_size_t, _P]),
     "moe_expert_fc1_mxfp8": (ctypes.c_int, [_CFG] + [_P] * 10),
     "moe_expert_fc2_mxfp8": (ctypes.c_int, [_CFG] + [_P] * 7),
     "moe_unpermute_combine": (ctypes.c_int, [_CFG, _P, _P, _P, _P, _P, _P]),
@@ -223,6 +224,15 @@ def moe_mxfp8_scale_bytes(rows, K, groups) -> int:
 def moe_mxfp8_quantize(rows, K, groups, offsets, x, q, sf, stream=None):
     _check("moe_mxfp8_quantize", _lib.moe_mxfp8_quantize(
         int(rows), int(K), int(groups), _ptr(offsets), _ptr(x), _ptr(q), _ptr(sf),
+        _stream(stream)))
+
+
+def moe_permute_mxfp8(cfg, x, topk_idx, topk_prob, x_q, x_sf, counts, offsets, dst_row,
+                      src_token, perm_prob, ws, stream=None):
+    wp, wb = _ws(ws)
+    _check("moe_permute_mxfp8", _lib.moe_permute_mxfp8(
+        ctypes.byref(cfg), _ptr(x), _ptr(topk_idx), _ptr(topk_prob), _ptr(x_q), _ptr(x_sf),
+        _ptr(counts), _ptr(offsets), _ptr(dst_row), _ptr(src_token), _ptr(perm_prob), wp, wb,
         _stream(stream)))
 
 

@@ -320,3 +320,65 @@ def test_full_size_deepseek_v3_sampled():
         S = X.grouped_gemm(a_codes & 0x7F, a_scales, one, ow2q & 0x7F, ow2s, h)
         yg = to_np(y[rows]).astype(np.float64)
         assert np.all(np.abs(yg - y_ref) <= F * U * S + 2.0 ** -8 * np.abs(y_ref) + 1e-30)
+
+
+@pytest.mark.parametrize("T,E,K,h,cap", [
+    (1000, 8, 2, 256, 0), (333, 64, 8, 384, 0), (2048, 256, 8, 7168, 0), (700, 16, 4, 128, 150),
+    (0, 8, 2, 256, 0),
+])
+def test_permute_mxfp8_equals_permute_then_quantize(T, E, K, h, cap):
+    M = lib()
+    rng = np.random.default_rng(T + E + h)
+    logits = rng.standard_normal((T, E)).astype(np.float32)
+    logits[:, 0] += 1.0
+    from oracle import moe_oracle as O
+    idx, prob = O.route(logits, K, O.SCORE_SOFTMAX) if T else (np.zeros((0, K), np.int32),
+                                                                np.zeros((0, K), np.float32))
+    x = hard_rows(rng, T, h) if T else np.zeros((0, h), np.float32)
+    cfg = M.make_config(T, h, E, K, 128, M.MOE_BF16, 0, M.MOE_ACT_SWIGLU, 0, 0, M.MOE_FLAG_RENORM,
+                        capacity=cap)
+    ws = torch.empty(M.moe_workspace_size(cfg), dtype=torch.uint8, device="cuda")
+    P = T * K
+    i32 = dict(dtype=torch.int32, device="cuda")
+    xd = to_dev(x, "bf16")
+    idd = torch.from_numpy(np.ascontiguousarray(idx, np.int32)).cuda()
+    pdd = to_dev(prob, "f32")
+    sfb = M.moe_mxfp8_scale_bytes(P, h, E)
+    outs = {}
+    for fused in ((True,) if T == 0 else (True, False)):
+        counts, offsets = torch.empty(E, **i32), torch.empty(E + 1, **i32)
+        dst_row, src_token = torch.empty(T, K, **i32), torch.empty(max(P, 1), **i32)
+        perm_prob = torch.empty(max(P, 1), dtype=torch.float32, device="cuda")
+        q = torch.zeros(max(P, 1), h, dtype=torch.uint8, device="cuda")
+        sf = torch.zeros(max(sfb, 16), dtype=torch.uint8, device="cuda")
+        if fused:
+            M.moe_permute_mxfp8(cfg, xd, idd, pdd, q, sf, counts, offsets, dst_row, src_token,
+                                perm_prob, ws)
+        else:
+            x_perm = torch.zeros(max(P, 1), h, dtype=torch.bfloat16, device="cuda")
+            M.moe_permute(cfg, xd, idd, pdd, x_perm, counts, offsets, dst_row, src_token,
+                          perm_prob, ws)
+            M.moe_mxfp8_quantize(P, h, E, offsets, x_perm, q, sf)
+        torch.cuda.synchronize()
+        assert M.moe_get_error() == M.MOE_OK
+        outs[fused] = dict(q=q.cpu().numpy(), sf=sf, offsets=to_np(offsets),
+                           src=src_token.cpu().numpy(), dst=dst_row.cpu().numpy())
+    f = outs[True]
+    if T == 0:  # no rows: the maps are empty, nothing is written
+        assert not f["offsets"].any()
+        return
+    u = outs[False]
+    np.testing.assert_array_equal(f["offsets"], u["offsets"])
+    np.testing.assert_array_equal(f["dst"], u["dst"])
+    n = int(f["offsets"][-1])
+    if n == 0:
+        return
+    np.testing.assert_array_equal(f["q"][:n], u["q"][:n])
+    idx_s = scale_index(n, h, f["offsets"])
+    np.testing.assert_array_equal(gpu_scales(f["sf"], idx_s), gpu_scales(u["sf"], idx_s))
+    # and against the oracle: row r holds token src_token[r] quantised
+    oq, os_ = X.quantize(x[f["src"][:n]])
+    np.testing.assert_array_equal(f["q"][:n], oq)
+    np.testing.assert_array_equal(gpu_scales(f["sf"], idx_s), os_)
+    if cap:
+        assert (f["dst"] == -1).any()
