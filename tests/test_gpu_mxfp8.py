@@ -173,6 +173,7 @@ CASES = [
     dict(seed=2, T=500, K=4, E=16, h=384, F=256, skew=True, empty=(3, 7)),
     dict(seed=3, T=100, K=8, E=64, h=512, F=128, skew=True),     # many experts below one tile
     dict(seed=4, T=2048, K=1, E=2, h=1024, F=384),               # multi-tile experts
+    dict(seed=6, T=1024, K=2, E=4, h=2048, F=512),               # ~4 tiles per expert, long K
 ]
 
 
