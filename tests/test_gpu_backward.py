@@ -20,11 +20,10 @@ def _bits(t):
 
 @pytest.mark.parametrize("T,h,E,K,F,skew", [
     (600, 512, 8, 2, 768, False),
-    (300, 200, 5, 2, 136, True),
+    (300, 200, 5, 2, 136, True),     # M = 200 and 272: ragged weight-gradient tiles
     (400, 256, 64, 8, 128, False),
     (700, 128, 1, 1, 256, False),
-    # experts on both sides of the resident-panel limit (256 rows) in one call
-    (2000, 128, 8, 1, 64, False),
+    (2000, 128, 8, 1, 64, False),    # a single 64-wide FFN; experts of ~250 rows (two blocks)
 ])
 def test_grouped_mlp_backward_matches_oracle(T, h, E, K, F, skew):
     M = lib()
