@@ -9,7 +9,10 @@
 // bit-reproducible: inside an expert's segment rows are in ascending token
 // order.  Tokens are cut into chunks of 32 (one warp each):
 //   1. chunk_hist:   hist[c][e] = pairs of chunk c routed to e
-//   2. chunk_scan:   base[c][e] = sum_{c' < c} hist[c'][e]; counts[e] (warp per expert)
+//   2. chunk_scan:   base[c][e] = sum_{c' < c} hist[c'][e]; counts[e] (warp per expert);
+//                    for small batches (ceil(T/32) * E <= 8192) every block of
+//                    step 3 redoes this scan in shared memory instead (one
+//                    launch fewer)
 //   3. chunk_ranks:  offsets = exclusive scan of counts; for every pair
 //                    dst_row = offsets[e] + base[c][e] + rank inside the chunk
 //                    (ranks from ballots over the lanes' expert ids);
@@ -49,12 +52,12 @@ MOE_D void hist_chunk(int c, int lane, int32_t* my, const int32_t* __restrict__ 
 
 // Exclusive scan of hist[:, e] over the chunks into base[:, e]; counts[e] =
 // the slots expert e keeps (all of them, or at most `cap` when cap > 0).
-MOE_D void scan_expert(int e, int lane, const int32_t* __restrict__ hist, int NC, int E, int cap,
-                       int32_t* __restrict__ base, int32_t* __restrict__ counts) {
+MOE_D void scan_expert(int e, int lane, const int32_t* hist, int NC, int E, int cap,
+                       int32_t* base, int32_t* counts) {
   int running = 0;
   for (int c0 = 0; c0 < NC; c0 += 32) {
     const int c = c0 + lane;
-    const int v = c < NC ? __ldg(hist + (int64_t)c * E + e) : 0;
+    const int v = c < NC ? hist[(int64_t)c * E + e] : 0;  // global or shared memory
     int incl = v;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
@@ -100,7 +103,7 @@ MOE_D void block_offsets(const int32_t* __restrict__ counts, int E, int32_t* s_o
 // (reported by the histogram step).
 MOE_D void ranks_chunk(int c, int lane, const int32_t* __restrict__ idx,
                        const float* __restrict__ prob, int T, int K, int E, int cap,
-                       const int32_t* __restrict__ base, const int32_t* s_off, int32_t* __restrict__ dst_row,
+                       const int32_t* base, const int32_t* s_off, int32_t* __restrict__ dst_row,
                        int32_t* __restrict__ src_token, float* __restrict__ perm_prob) {
   const int64_t t = (int64_t)c * kChunk + lane;
   const bool valid = t < T;
@@ -132,7 +135,7 @@ MOE_D void ranks_chunk(int c, int lane, const int32_t* __restrict__ idx,
         dst_row[t * K + k] = -1;
         continue;
       }
-      const int pos = __ldg(base + (int64_t)c * E + e) + rank[k];
+      const int pos = base[(int64_t)c * E + e] + rank[k];  // global or shared memory
       if (cap > 0 && pos >= cap) {
         dst_row[t * K + k] = -1;
         continue;
@@ -225,6 +228,58 @@ __global__ void __launch_bounds__(256) chunk_ranks_kernel(
                 perm_prob);
 }
 
+// Steps 2 and 3 in one kernel for small batches (NC * E <= kScanInBlock):
+// every block copies the chunk histograms into shared memory and scans them
+// per expert itself (a few thousand integers, L2-resident), so the separate
+// scan launch goes away; block 0 writes counts and offsets.  Same per-warp
+// steps, same maps.
+constexpr int64_t kScanInBlock = 8192;
+
+__global__ void __launch_bounds__(256) chunk_scan_ranks_kernel(
+    const int32_t* __restrict__ idx, const float* __restrict__ prob, int T, int K, int E, int cap,
+    int NC, const int32_t* __restrict__ hist, int32_t* __restrict__ counts_out,
+    int32_t* __restrict__ offsets_out, int32_t* __restrict__ dst_row,
+    int32_t* __restrict__ src_token, float* __restrict__ perm_prob) {
+  extern __shared__ int32_t sh[];
+  int32_t* s_base = sh;                        // [NC][E]: hist, then base in place
+  int32_t* s_cnt = s_base + (int64_t)NC * E;   // [E]
+  int32_t* s_off = s_cnt + E;                  // [E + 1]
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int64_t i = threadIdx.x; i < (int64_t)NC * E; i += blockDim.x) s_base[i] = __ldg(hist + i);
+  __syncthreads();
+  for (int e = warp; e < E; e += 8) scan_expert(e, lane, s_base, NC, E, cap, s_base, s_cnt);
+  __syncthreads();
+  if (warp == 0) {  // s_off = exclusive scan of the counts
+    int running = 0;
+    for (int e0 = 0; e0 < E; e0 += 32) {
+      const int e = e0 + lane;
+      const int v = e < E ? s_cnt[e] : 0;
+      int incl = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+      }
+      if (e < E) {
+        s_off[e] = running + incl - v;
+        if (blockIdx.x == 0) {
+          offsets_out[e] = running + incl - v;
+          counts_out[e] = v;
+        }
+      }
+      running += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) {
+      s_off[E] = running;
+      if (blockIdx.x == 0) offsets_out[E] = running;
+    }
+  }
+  __syncthreads();
+  const int c = blockIdx.x * 8 + warp;
+  if (c < NC)
+    ranks_chunk(c, lane, idx, prob, T, K, E, cap, s_base, s_off, dst_row, src_token, perm_prob);
+}
+
 // One warp per token (the grid covers every token, so the block scheduler
 // balances the load).
 template <typename T, int KMAX>
@@ -252,6 +307,13 @@ cudaError_t launch_permute_maps(const moe_config_t& c, const int32_t* idx, const
   const int blocks = (int)ceil_div(NC, 8);
   chunk_hist_kernel<<<blocks, 256, 8 * c.E * sizeof(int32_t), s>>>(idx, c.T, c.K, c.E, NC, hist,
                                                                   status);
+  if ((int64_t)NC * c.E <= kScanInBlock) {
+    const size_t bytes = sizeof(int32_t) * ((size_t)NC * c.E + 2 * c.E + 1);
+    chunk_scan_ranks_kernel<<<blocks, 256, bytes, s>>>(idx, prob, c.T, c.K, c.E, c.capacity, NC,
+                                                       hist, counts, offsets, dst_row, src_token,
+                                                       perm_prob);
+    return cudaGetLastError();
+  }
   chunk_scan_kernel<<<(unsigned)ceil_div(c.E, 8), 256, 0, s>>>(hist, NC, c.E, c.capacity, base,
                                                                 counts);
   chunk_ranks_kernel<<<blocks, 256, 0, s>>>(idx, prob, c.T, c.K, c.E, c.capacity, NC, base, counts,
