@@ -61,6 +61,9 @@ def parse():
                    help="expert GEMM tiling: auto (CTA pairs when experts average >= 512 rows)")
     p.add_argument("--tokens", type=int, default=0,
                    help="override T (smaller cases for profiler captures; not a bench line)")
+    p.add_argument("--hbm-write", action="store_true",
+                   help="only measure this GPU's write-only and copy HBM bandwidth (torch fill_ / "
+                        "copy_ over 16 GB, best of 10, CUDA events) and print one JSON line")
     p.add_argument("--shape", default="",
                    help="override workload fields, e.g. T=512,h=4096,E=32,F=2048 (profiler cases)")
     return p.parse_args()
@@ -831,8 +834,42 @@ def run_ours(args, w):
         torch.distributed.destroy_process_group()
 
 
+def hbm_write_probe():
+    """Write-only bandwidth (a fill, no reads) beside the copy bandwidth the
+    roofline peaks use: the expert weight gradients write dW and read little,
+    so the fill rate is their roofline."""
+    import torch
+    dev = torch.device("cuda")
+    n = 16 << 30
+    buf = torch.empty(n, dtype=torch.uint8, device=dev)
+    src = torch.empty(n // 2, dtype=torch.uint8, device=dev)
+    dst = torch.empty(n // 2, dtype=torch.uint8, device=dev)
+    for _ in range(3):
+        buf.fill_(1)
+        dst.copy_(src)
+    torch.cuda.synchronize()
+    tw, tc = [], []
+    for _ in range(10):
+        a, b, c = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+        a.record()
+        buf.fill_(1)
+        b.record()
+        dst.copy_(src)
+        c.record()
+        torch.cuda.synchronize()
+        tw.append(a.elapsed_time(b))
+        tc.append(b.elapsed_time(c))
+    print(json.dumps({"write_only_gbs": n / (min(tw) / 1000) / 1e9,
+                      "copy_gbs": n / (min(tc) / 1000) / 1e9,
+                      "how": "torch fill_ of 16 GiB (writes only) and copy_ of 8 GiB (8 GiB read + "
+                             "8 GiB written), best of 10, CUDA events"}), flush=True)
+
+
 def main():
     args = parse()
+    if args.hbm_write:
+        hbm_write_probe()
+        return
     from mixture_experts_layer_softmax_gb300 import workloads
     w = workloads.ALL[args.workload] if args.workload else workloads.MIXTRAL
     if args.tokens:
