@@ -69,44 +69,69 @@ __global__ void __launch_bounds__(256) router_bwd_kernel(
   if (r >= 0) dl_perm[r] = dl;
 }
 
-// dW_r[e, c..c+8) = sum over expert e's rows of dl_perm[r] * x[src_token[r], c..c+8)
-// (fp32, rows in order); db_r[e] = sum of dl_perm over the rows.
+// dW_r[e, c0..c0+256) = sum over expert e's rows r of dl_perm[r] * x[src_token[r], ...]
+// (fp32); db_r[e] = sum of dl_perm over the rows.  One block per (expert,
+// 256 columns): the expert's token ids and dl values are staged in shared
+// memory (1024 rows at a time), 8 row groups of 32 lanes each sum the rows
+// r = r0 + g, r0 + g + 8, ... in order (lane = 8 columns, several row loads in
+// flight), and the 8 group sums are added in group order: a fixed summation
+// order, so reruns are bitwise identical.
 template <typename T>
 __global__ void __launch_bounds__(256) router_wgrad_kernel(
     const T* __restrict__ x, const int32_t* __restrict__ src_token,
     const int32_t* __restrict__ offsets, const float* __restrict__ dl_perm, int h,
     float* __restrict__ dw_r, float* __restrict__ db_r) {
-  constexpr int V = 8;
+  constexpr int V = 8, G = 8, CHUNK = 1024;
+  __shared__ int32_t s_tok[CHUNK];
+  __shared__ float s_dl[CHUNK];
+  __shared__ float s_acc[G][32 * V];
   const int e = blockIdx.x;
-  const int c = (blockIdx.y * blockDim.x + threadIdx.x) * V;
+  const int g = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int c = blockIdx.y * (32 * V) + lane * V;
   const int r0 = __ldg(offsets + e), r1 = __ldg(offsets + e + 1);
-  if (c < h) {
-    float acc[V] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    for (int r = r0; r < r1; ++r) {
-      const float d = __ldg(dl_perm + r);
-      const T* row = x + (int64_t)__ldg(src_token + r) * h + c;
-      float v[V];
-      if constexpr (sizeof(T) == 2) {
-        const Vec<__nv_bfloat16> u = ldg16(reinterpret_cast<const __nv_bfloat16*>(row));
-#pragma unroll
-        for (int i = 0; i < V; ++i) v[i] = __bfloat162float(u.v[i]);
-      } else {
-        const float4 a = __ldg(reinterpret_cast<const float4*>(row));
-        const float4 b = __ldg(reinterpret_cast<const float4*>(row + 4));
-        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
-      }
-#pragma unroll
-      for (int i = 0; i < V; ++i) acc[i] = fmaf(d, v[i], acc[i]);
+  float acc[V] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  float dsum = 0.f;  // db_r: thread 0 adds the dl values in row order
+  for (int q0 = r0; q0 < r1; q0 += CHUNK) {
+    const int n = min(CHUNK, r1 - q0);
+    __syncthreads();
+    for (int i = threadIdx.x; i < n; i += blockDim.x) {
+      s_tok[i] = __ldg(src_token + q0 + i);
+      s_dl[i] = __ldg(dl_perm + q0 + i);
     }
-    float* o = dw_r + (int64_t)e * h + c;
-    *reinterpret_cast<float4*>(o) = make_float4(acc[0], acc[1], acc[2], acc[3]);
-    *reinterpret_cast<float4*>(o + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
+    __syncthreads();
+    if (db_r && blockIdx.y == 0 && threadIdx.x == 0)
+      for (int i = 0; i < n; ++i) dsum += s_dl[i];
+    if (c < h) {
+#pragma unroll 4
+      for (int i = g; i < n; i += G) {
+        const float d = s_dl[i];
+        const T* row = x + (int64_t)s_tok[i] * h + c;
+        float v[V];
+        if constexpr (sizeof(T) == 2) {
+          const Vec<__nv_bfloat16> u = ldg16(reinterpret_cast<const __nv_bfloat16*>(row));
+#pragma unroll
+          for (int j = 0; j < V; ++j) v[j] = __bfloat162float(u.v[j]);
+        } else {
+          const float4 a = __ldg(reinterpret_cast<const float4*>(row));
+          const float4 b = __ldg(reinterpret_cast<const float4*>(row + 4));
+          v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+        }
+#pragma unroll
+        for (int j = 0; j < V; ++j) acc[j] = fmaf(d, v[j], acc[j]);
+      }
+    }
   }
-  if (db_r && blockIdx.y == 0 && threadIdx.x == 0) {
-    float s = 0.f;
-    for (int r = r0; r < r1; ++r) s += __ldg(dl_perm + r);
-    db_r[e] = s;
+#pragma unroll
+  for (int j = 0; j < V; ++j) s_acc[g][lane * V + j] = acc[j];
+  __syncthreads();
+  const int col = blockIdx.y * (32 * V) + threadIdx.x;
+  if (col < h) {
+    float sum = 0.f;
+#pragma unroll
+    for (int k = 0; k < G; ++k) sum += s_acc[k][threadIdx.x];
+    dw_r[(int64_t)e * h + col] = sum;
   }
+  if (db_r && blockIdx.y == 0 && threadIdx.x == 0) db_r[e] = dsum;
 }
 
 // One 128-thread block per token:
@@ -239,7 +264,7 @@ cudaError_t launch_router_bwd(const moe_config_t& c, const float* logits, const 
 cudaError_t launch_router_wgrad(const moe_config_t& c, const void* x, const int32_t* src_token,
                                 const int32_t* offsets, const float* dl_perm, float* dw_r,
                                 float* db_r, cudaStream_t s) {
-  dim3 grid((unsigned)c.E, (unsigned)ceil_div(c.h, 256 * 8));
+  dim3 grid((unsigned)c.E, (unsigned)ceil_div(c.h, 256));
   if (c.dtype == MOE_BF16)
     router_wgrad_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(
         static_cast<const __nv_bfloat16*>(x), src_token, offsets, dl_perm, c.h, dw_r, db_r);
