@@ -82,6 +82,24 @@ def dist_env():
     return ws, int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0"))
 
 
+def max_over_ranks(value: float, world: int, device) -> float:
+    """The largest of every rank's value (each rank gets it): the job's step
+    time is the slowest replica's."""
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(world: int, tokens_per_rank: int, ms: float) -> float:
+    """Whole-job throughput of weak-scaled replicas: every rank processes its
+    own tokens_per_rank tokens per step of `ms` (the max over ranks)."""
+    return world * tokens_per_rank / (ms / 1000.0)
+
+
 # ---------------------------------------------------------------------------
 # clocks sampled during the timed region
 # ---------------------------------------------------------------------------
@@ -650,11 +668,8 @@ def run_ours(args, w):
         except Exception as exc:  # report, keep the eager number
             print(f"graph capture unavailable: {exc}", file=sys.stderr)
             graph_ms = None
-    if world > 1:
-        t = torch.tensor([ms], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
-    value = world * T / (ms / 1000.0)
+    ms = max_over_ranks(ms, world, dev)
+    value = job_tokens_per_s(world, T, ms)
 
     # ---- end to end through moe_layer_fwd with host buffers ----
     # Every step copies its tokens in from pinned host memory and its output
@@ -708,12 +723,9 @@ def run_ours(args, w):
         t1.record(cs)
         torch.cuda.synchronize()
         ems = t0.elapsed_time(t1) / K2
-        if world > 1:
-            t = torch.tensor([ems], dtype=torch.float64, device=dev)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            ems = float(t.item())
+        ems = max_over_ranks(ems, world, dev)
         esz = 2 if w.dtype == "bf16" else 4
-        e2e = {"value": world * T / (ems / 1000.0), "unit": "tokens/s",
+        e2e = {"value": job_tokens_per_s(world, T, ems), "unit": "tokens/s",
                "h2d_bytes_per_step": T * h * esz, "d2h_bytes_per_step": T * h * esz,
                "ms_per_step": ems,
                "how": "moe_layer_fwd per step; tokens copied in from pinned host memory and the "
