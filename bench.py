@@ -791,6 +791,10 @@ def run_ours(args, w):
                                "forward above " + ("gathers the rows inside FC1 instead"
                                                    if gather else "uses it"))
         line["combine_pct_hbm"] = 100.0 * comb_gbs / pk["hbm_gbs"]
+        cnt = counts.cpu().numpy().astype(np.float64)  # the last step's expert loads
+        line["expert_counts"] = {"min": int(cnt.min()), "max": int(cnt.max()),
+                                 "mean": float(cnt.mean()),
+                                 "cv": float(cnt.std() / cnt.mean()) if cnt.mean() > 0 else 0.0}
         line["route_ms"] = stage_ms["route"]
         # the router reads every token row once (its weight stays in L2/shared memory)
         line["route_pct_hbm"] = 100.0 * (T * h * esz) / (stage_ms["route"] / 1000.0) / 1e9 / pk["hbm_gbs"]

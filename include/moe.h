@@ -413,6 +413,13 @@ const char* moe_version(void);
  * moe_get_error.  Never faults or hangs the device. */
 moe_status_t moe_test_bounded_wait(int64_t max_polls, moe_stream_t stream);
 
+/* Test hook (host-side fault injection, no device involvement): the next n
+ * calls that would enqueue GPU work fail as if their first CUDA runtime call
+ * had failed -- they return MOE_ERR_CUDA after validating their arguments and
+ * before anything is enqueued.  Returns the number of injected failures that
+ * were still pending (-1 if n < 0); n = 0 clears them. */
+int32_t moe_test_inject_cuda_failure(int32_t n);
+
 #ifdef __cplusplus
 }
 #endif

@@ -1,6 +1,9 @@
 // The C ABI (include/moe.h): argument validation, workspace carving and the
 // order of the layer's steps.  Host code here only validates and enqueues; it
 // never reads device memory or synchronises (except moe_get_error).
+#include <nvtx3/nvToolsExt.h>
+
+#include <atomic>
 #include <cmath>
 #include <mutex>
 
@@ -75,9 +78,32 @@ struct DeviceInfo {
 DeviceInfo g_dev[kMaxDevices];
 std::mutex g_dev_mu;
 
+// Test hook (moe_test_inject_cuda_failure): calls left that must fail as if
+// their first CUDA runtime call had failed.
+std::atomic<int> g_inject_failures{0};
+
+// NVTX ranges around the steps of a layer pass (host-side annotations: a
+// profiler attributes each step's launches to its range; no cost otherwise).
+class NvtxStage {
+ public:
+  explicit NvtxStage(const char* name) { nvtxRangePushA(name); }
+  void next(const char* name) {
+    nvtxRangePop();
+    nvtxRangePushA(name);
+  }
+  ~NvtxStage() { nvtxRangePop(); }
+  NvtxStage(const NvtxStage&) = delete;
+  NvtxStage& operator=(const NvtxStage&) = delete;
+};
+
 // Status-word address and SM count of the current device (looked up once per
 // device, with that device current).
-const DeviceInfo* device_info() {
+// (inject: a pending injected failure makes this call fail; moe_get_error
+// looks the device up without consuming one.)
+const DeviceInfo* device_info(bool inject = true) {
+  if (inject)
+    for (int n = g_inject_failures.load(); n > 0; n = g_inject_failures.load())
+      if (g_inject_failures.compare_exchange_weak(n, n - 1)) return nullptr;  // injected failure
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
   std::lock_guard<std::mutex> lock(g_dev_mu);
@@ -520,6 +546,7 @@ moe_status_t moe_layer_fwd(const moe_config_t* cfg, const void* x, const float* 
   int32_t* dst_row = at<int32_t>(ws, w.dst_row);
   float* perm_prob = at<float>(ws, w.perm_prob);
   // Route
+  NvtxStage stage("moe_layer_fwd/route");
   cudaError_t e = launch_router(c, x, w_r, gate_bias, sel_bias, at<float>(ws, w.logits), idx,
                                 prob, nullptr, router_scratch(c, ws), d->sms, d->status, s);
   if (e == cudaSuccess && (c.aux_loss_coeff != 0.f || c.z_loss_coeff != 0.f))
@@ -530,6 +557,7 @@ moe_status_t moe_layer_fwd(const moe_config_t* cfg, const void* x, const float* 
   // gather its rows from x instead -- moe_expert_fc1_gather -- but it re-reads
   // each row block once per N tile, and a gathered re-read costs the TMA
   // engine far more than a tiled one: the one-pass scatter is faster.)
+  stage.next("moe_layer_fwd/dispatch");
   if (e == cudaSuccess)
     e = launch_permute_maps(c, idx, prob, at<int32_t>(ws, w.hist), at<int32_t>(ws, w.chunk_base),
                             at<int32_t>(ws, w.counts), offsets, dst_row,
@@ -537,6 +565,7 @@ moe_status_t moe_layer_fwd(const moe_config_t* cfg, const void* x, const float* 
   if (e == cudaSuccess)
     e = launch_scatter_rows(c, x, dst_row, at<void>(ws, w.x_perm), d->sms, d->status, s);
   // Expert computation
+  stage.next("moe_layer_fwd/experts");
   if (e == cudaSuccess)
     e = run_grouped_mlp(c, c.T * c.K, at<void>(ws, w.x_perm), offsets, perm_prob, w1, b1, w2, b2,
                         save ? at<void>(ws, w.act_save) : nullptr, at<void>(ws, w.a),
@@ -557,6 +586,7 @@ moe_status_t moe_layer_fwd(const moe_config_t* cfg, const void* x, const float* 
     shared_y = at<void>(ws, w.shared_y);
   }
   // Combine (probabilities were applied inside the expert GEMMs)
+  stage.next("moe_layer_fwd/combine");
   if (e == cudaSuccess)
     e = launch_combine(c, at<void>(ws, w.y_perm), dst_row, nullptr, shared_y, y, d->sms,
                        d->status, s);
@@ -706,6 +736,7 @@ moe_status_t moe_layer_bwd(const moe_config_t* cfg, const void* x, const float* 
   const int32_t* idx = at<int32_t>(ws, w.topk_idx);
   float* dl_topk = at<float>(ws, w.dl_topk);
   // dy in expert order, then the routed experts' backward
+  NvtxStage stage("moe_layer_bwd/experts");
   cudaError_t e = launch_scatter_rows(c, dy, dst_row, at<void>(ws, w.dy_perm), d->sms, d->status, s);
   if (e == cudaSuccess)
     e = run_mlp_bwd(c, P, c.E, at<void>(ws, w.dy_perm), at<void>(ws, w.x_perm),
@@ -719,6 +750,7 @@ moe_status_t moe_layer_bwd(const moe_config_t* cfg, const void* x, const float* 
                     at<void>(ws, w.shared_dh), nullptr, at<void>(ws, w.shared_dx), dw1_shared,
                     dw2_shared, d, s);
   // Route backward: dprob -> dl -> dW_r, db_r
+  stage.next("moe_layer_bwd/router");
   if (e == cudaSuccess)
     e = launch_dprob_reduce(at<float>(ws, w.dprob_part), P, (c.F + 255) / 256,
                             at<float>(ws, w.dprob_perm), s);
@@ -755,6 +787,7 @@ moe_status_t moe_layer_bwd(const moe_config_t* cfg, const void* x, const float* 
     if (e == cudaSuccess) e = launch_dense_router_wgrad(c, dl_dense, x, dw_r, db_r, s);
   }
   // dx = routed + shared + router contributions
+  stage.next("moe_layer_bwd/combine");
   if (e == cudaSuccess)
     e = launch_bwd_combine(c, at<void>(ws, w.dx_perm), dst_row,
                            c.n_shared ? at<void>(ws, w.shared_dx) : nullptr, dl_topk, idx, w_r,
@@ -765,7 +798,7 @@ moe_status_t moe_layer_bwd(const moe_config_t* cfg, const void* x, const float* 
 moe_status_t moe_get_error(moe_stream_t stream) {
   if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return MOE_ERR_CUDA;
   if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
-  const DeviceInfo* d = device_info();
+  const DeviceInfo* d = device_info(false);
   if (!d) return MOE_ERR_CUDA;
   int v = 0;
   if (cudaMemcpy(&v, d->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
@@ -792,6 +825,11 @@ const char* moe_status_string(moe_status_t s) {
 }
 
 const char* moe_version(void) { return "0.1.0"; }
+
+int32_t moe_test_inject_cuda_failure(int32_t n) {
+  if (n < 0) return -1;
+  return g_inject_failures.exchange(n);
+}
 
 moe_status_t moe_test_bounded_wait(int64_t max_polls, moe_stream_t stream) {
   if (max_polls < 1) return MOE_ERR_INVALID_ARG;

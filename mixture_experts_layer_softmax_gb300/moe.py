@@ -81,6 +81,7 @@ _SIG = {
     "moe_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "moe_version": (ctypes.c_char_p, []),
     "moe_test_bounded_wait": (ctypes.c_int, [ctypes.c_int64, _P]),
+    "moe_test_inject_cuda_failure": (ctypes.c_int32, [ctypes.c_int32]),
 }
 for _name, (_res, _args) in _SIG.items():
     _f = getattr(_lib, _name)
@@ -311,6 +312,10 @@ def moe_get_error(stream=None) -> int:
 
 def moe_test_bounded_wait(max_polls, stream=None):
     _check("moe_test_bounded_wait", _lib.moe_test_bounded_wait(int(max_polls), _stream(stream)))
+
+
+def moe_test_inject_cuda_failure(n) -> int:
+    return int(_lib.moe_test_inject_cuda_failure(int(n)))
 
 
 def raw(name):

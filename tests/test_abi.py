@@ -136,3 +136,10 @@ def test_mxfp8_argument_checks(M):
         bad = _cfg(M, flags=M.MOE_FLAG_RENORM | M.MOE_FLAG_VALIDATE_ONLY, **kw)
         assert f1(ctypes.byref(bad), P, P, P, None, P, P, P, None, None, None) == M.MOE_ERR_UNSUPPORTED
         assert f2(ctypes.byref(bad), P, P, P, P, P, P, None) == M.MOE_ERR_UNSUPPORTED
+
+
+def test_failure_injection_counter(M):
+    assert M.moe_test_inject_cuda_failure(3) == 0
+    assert M.moe_test_inject_cuda_failure(0) == 3   # cleared, the pending count returned
+    assert M.moe_test_inject_cuda_failure(-1) == -1
+    assert M.moe_test_inject_cuda_failure(0) == 0
