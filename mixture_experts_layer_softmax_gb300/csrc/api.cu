@@ -19,7 +19,7 @@ cudaError_t launch_permute_maps(const moe_config_t&, const int32_t*, const float
                                 int32_t*, int32_t*, int32_t*, int32_t*, int32_t*, float*, int*,
                                 cudaStream_t);
 cudaError_t launch_scatter_rows(const moe_config_t&, const void*, const int32_t*, void*, int,
-                                int*, cudaStream_t);
+                                int*, cudaStream_t, bool after_maps = false);
 cudaError_t launch_combine(const moe_config_t&, const void*, const int32_t*, const float*,
                            const void*, void*, int, int*, cudaStream_t);
 cudaError_t launch_expert_gemm_simt(const moe_config_t&, int, int, const void*, const int32_t*,
@@ -327,7 +327,8 @@ moe_status_t moe_permute(const moe_config_t* cfg, const void* x, const int32_t* 
   cudaError_t e = launch_permute_maps(*cfg, topk_idx, topk_prob, at<int32_t>(ws, w.hist),
                                       at<int32_t>(ws, w.chunk_base), counts, offsets, dst_row,
                                       src_token, perm_prob, d->status, s);
-  if (e == cudaSuccess && x) e = launch_scatter_rows(*cfg, x, dst_row, x_perm, d->sms, d->status, s);
+  if (e == cudaSuccess && x)
+    e = launch_scatter_rows(*cfg, x, dst_row, x_perm, d->sms, d->status, s, true);
   return cuda_status(e);
 }
 
@@ -563,7 +564,7 @@ moe_status_t moe_layer_fwd(const moe_config_t* cfg, const void* x, const float* 
                             at<int32_t>(ws, w.counts), offsets, dst_row,
                             at<int32_t>(ws, w.src_token), perm_prob, d->status, s);
   if (e == cudaSuccess)
-    e = launch_scatter_rows(c, x, dst_row, at<void>(ws, w.x_perm), d->sms, d->status, s);
+    e = launch_scatter_rows(c, x, dst_row, at<void>(ws, w.x_perm), d->sms, d->status, s, true);
   // Expert computation
   stage.next("moe_layer_fwd/experts");
   if (e == cudaSuccess)

@@ -29,6 +29,44 @@ namespace moe {
 
 constexpr int kChunk = 32;
 
+// Programmatic dependent launch: a kernel launched with pdl_launch may be
+// scheduled while the previous kernel on the stream is still finishing; it
+// waits here, before its first memory access, until that kernel has
+// completed and its writes are visible (a no-op without a dependency).  The
+// previous kernel lets it be scheduled early with pdl_trigger.
+MOE_D void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+MOE_D void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+static cudaError_t launch_maybe_pdl(bool pdl, void (*kern)(KArgs...), dim3 grid, dim3 block,
+                                   size_t smem, cudaStream_t s, Args... args);
+
+template <typename... KArgs, typename... Args>
+static cudaError_t pdl_launch(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t s, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
+// With pdl false a plain launch: the kernel's pdl_wait returns at once and
+// it starts only after everything before it on the stream has completed.
+template <typename... KArgs, typename... Args>
+static cudaError_t launch_maybe_pdl(bool pdl, void (*kern)(KArgs...), dim3 grid, dim3 block,
+                                   size_t smem, cudaStream_t s, Args... args) {
+  if (pdl) return pdl_launch(kern, grid, block, smem, s, args...);
+  kern<<<grid, block, smem, s>>>(args...);
+  return cudaGetLastError();
+}
+
 // ---- per-warp steps ----------------------------------------------------------
 
 // hist[c][e] for chunk c; `my` is this warp's [E] shared-memory counter row.
@@ -149,7 +187,11 @@ MOE_D void ranks_chunk(int c, int lane, const int32_t* __restrict__ idx,
 }
 
 // Token t's row, read once (16-byte vectors, up to 8 per lane in flight) and
-// written to its K destination rows.
+// written to its K destination rows.  The first batch of the row's vectors is
+// loaded before pdl_wait: x is never written by the map steps this kernel
+// follows (and was final before they started), so under programmatic
+// dependent launch that read overlaps the previous kernel's tail; the
+// destination rows are read only after the wait.
 template <typename T, int KMAX>
 MOE_D void scatter_token(int64_t t, int lane, const T* __restrict__ x,
                          const int32_t* __restrict__ dst_row,
@@ -158,6 +200,14 @@ MOE_D void scatter_token(int64_t t, int lane, const T* __restrict__ x,
   constexpr int kMaxVec = 8;
   const int nvec = h / V;
   const int64_t P = (int64_t)ntok * K;
+  const T* src = x + t * h;
+  Vec<T> buf[kMaxVec];
+#pragma unroll
+  for (int i = 0; i < kMaxVec; ++i) {
+    const int v = i * 32 + lane;
+    if (v < nvec) buf[i] = ld16_stream(src + (int64_t)v * V);
+  }
+  pdl_wait();
   T* dst[KMAX];
 #pragma unroll
   for (int k = 0; k < KMAX; ++k) {
@@ -170,13 +220,13 @@ MOE_D void scatter_token(int64_t t, int lane, const T* __restrict__ x,
         report(status, MOE_ERR_DEVICE_BOUNDS);
     }
   }
-  const T* src = x + t * h;
   for (int v0 = 0; v0 < nvec; v0 += 32 * kMaxVec) {
-    Vec<T> buf[kMaxVec];
+    if (v0 > 0) {
 #pragma unroll
-    for (int i = 0; i < kMaxVec; ++i) {
-      const int v = v0 + i * 32 + lane;
-      if (v < nvec) buf[i] = ld16_stream(src + (int64_t)v * V);
+      for (int i = 0; i < kMaxVec; ++i) {
+        const int v = v0 + i * 32 + lane;
+        if (v < nvec) buf[i] = ld16_stream(src + (int64_t)v * V);
+      }
     }
 #pragma unroll
     for (int k = 0; k < KMAX; ++k) {
@@ -197,6 +247,7 @@ __global__ void __launch_bounds__(256) chunk_hist_kernel(const int32_t* __restri
                                                          int K, int E, int NC,
                                                          int32_t* __restrict__ hist, int* status) {
   extern __shared__ int32_t sh[];  // [8][E]
+  pdl_trigger();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int c = blockIdx.x * 8 + warp;
   if (c < NC) hist_chunk(c, lane, sh + warp * E, idx, T, K, E, hist, status);
@@ -241,6 +292,8 @@ __global__ void __launch_bounds__(256) chunk_scan_ranks_kernel(
     int32_t* __restrict__ offsets_out, int32_t* __restrict__ dst_row,
     int32_t* __restrict__ src_token, float* __restrict__ perm_prob) {
   extern __shared__ int32_t sh[];
+  pdl_wait();
+  pdl_trigger();
   int32_t* s_base = sh;                        // [NC][E]: hist, then base in place
   int32_t* s_cnt = s_base + (int64_t)NC * E;   // [E]
   int32_t* s_off = s_cnt + E;                  // [E + 1]
@@ -288,7 +341,10 @@ __global__ void __launch_bounds__(256) scatter_rows_kernel(const T* __restrict__
                                                            int ntok, int K, int h,
                                                            T* __restrict__ x_perm, int* status) {
   const int64_t t = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
-  if (t < ntok) scatter_token<T, KMAX>(t, threadIdx.x & 31, x, dst_row, ntok, K, h, x_perm, status);
+  if (t < ntok)
+    scatter_token<T, KMAX>(t, threadIdx.x & 31, x, dst_row, ntok, K, h, x_perm, status);
+  else
+    pdl_wait();
 }
 
 int num_chunks(int T) { return (int)ceil_div(T, kChunk); }
@@ -309,10 +365,9 @@ cudaError_t launch_permute_maps(const moe_config_t& c, const int32_t* idx, const
                                                                   status);
   if ((int64_t)NC * c.E <= kScanInBlock) {
     const size_t bytes = sizeof(int32_t) * ((size_t)NC * c.E + 2 * c.E + 1);
-    chunk_scan_ranks_kernel<<<blocks, 256, bytes, s>>>(idx, prob, c.T, c.K, c.E, c.capacity, NC,
-                                                       hist, counts, offsets, dst_row, src_token,
-                                                       perm_prob);
-    return cudaGetLastError();
+    return pdl_launch(chunk_scan_ranks_kernel, dim3(blocks), dim3(256), bytes, s, idx, prob, c.T,
+                      c.K, c.E, c.capacity, NC, (const int32_t*)hist, counts, offsets, dst_row,
+                      src_token, perm_prob);
   }
   chunk_scan_kernel<<<(unsigned)ceil_div(c.E, 8), 256, 0, s>>>(hist, NC, c.E, c.capacity, base,
                                                                 counts);
@@ -329,27 +384,36 @@ int scatter_grid(int ntok, int sms) {
 
 template <typename T>
 static cudaError_t scatter_t(const moe_config_t& c, const void* x, const int32_t* dst_row,
-                             void* x_perm, int* status, cudaStream_t s) {
+                             void* x_perm, int* status, cudaStream_t s, bool pdl) {
   const unsigned grid = (unsigned)ceil_div(c.T, 8);
   const T* xs = static_cast<const T*>(x);
   T* xp = static_cast<T*>(x_perm);
   if (c.K <= 2)
-    scatter_rows_kernel<T, 2><<<grid, 256, 0, s>>>(xs, dst_row, c.T, c.K, c.h, xp, status);
+    return launch_maybe_pdl(pdl, scatter_rows_kernel<T, 2>, dim3(grid), dim3(256), 0, s, xs, dst_row,
+                            c.T, c.K, c.h, xp, status);
   else if (c.K <= 4)
-    scatter_rows_kernel<T, 4><<<grid, 256, 0, s>>>(xs, dst_row, c.T, c.K, c.h, xp, status);
+    return launch_maybe_pdl(pdl, scatter_rows_kernel<T, 4>, dim3(grid), dim3(256), 0, s, xs, dst_row,
+                            c.T, c.K, c.h, xp, status);
   else if (c.K <= 8)
-    scatter_rows_kernel<T, 8><<<grid, 256, 0, s>>>(xs, dst_row, c.T, c.K, c.h, xp, status);
+    return launch_maybe_pdl(pdl, scatter_rows_kernel<T, 8>, dim3(grid), dim3(256), 0, s, xs, dst_row,
+                            c.T, c.K, c.h, xp, status);
   else
-    scatter_rows_kernel<T, 16><<<grid, 256, 0, s>>>(xs, dst_row, c.T, c.K, c.h, xp, status);
+    return launch_maybe_pdl(pdl, scatter_rows_kernel<T, 16>, dim3(grid), dim3(256), 0, s, xs, dst_row,
+                            c.T, c.K, c.h, xp, status);
   return cudaGetLastError();
 }
 
+// after_maps: the launch directly follows this library's map steps on the
+// stream, so it may overlap their tail (programmatic dependent launch); any
+// other caller gets a plain launch.
 cudaError_t launch_scatter_rows(const moe_config_t& c, const void* x, const int32_t* dst_row,
-                                void* x_perm, int sms, int* status, cudaStream_t s) {
+                                void* x_perm, int sms, int* status, cudaStream_t s,
+                                bool after_maps) {
   (void)sms;
   if (c.T == 0) return cudaSuccess;
-  if (c.dtype == MOE_BF16) return scatter_t<__nv_bfloat16>(c, x, dst_row, x_perm, status, s);
-  return scatter_t<float>(c, x, dst_row, x_perm, status, s);
+  if (c.dtype == MOE_BF16)
+    return scatter_t<__nv_bfloat16>(c, x, dst_row, x_perm, status, s, after_maps);
+  return scatter_t<float>(c, x, dst_row, x_perm, status, s, after_maps);
 }
 
 }  // namespace moe

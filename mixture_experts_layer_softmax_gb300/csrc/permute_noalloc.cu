@@ -24,7 +24,7 @@ cudaError_t launch_permute_maps(const moe_config_t&, const int32_t*, const float
                                 int32_t*, int32_t*, int32_t*, int32_t*, int32_t*, float*, int*,
                                 cudaStream_t);
 cudaError_t launch_scatter_rows(const moe_config_t&, const void*, const int32_t*, void*, int,
-                                int*, cudaStream_t);
+                                int*, cudaStream_t, bool after_maps = false);
 int num_chunks(int T);
 moe_status_t validate_config(const moe_config_t* c);
 int* device_status_word();
@@ -99,6 +99,6 @@ extern "C" moe_status_t moe_permute_noalloc(const moe_config_t* cfg, const void*
   cudaError_t e = moe::launch_permute_maps(*cfg, topk_idx, topk_prob, hist, base, counts, offsets,
                                            dst_row, src_token, perm_prob, status, s);
   if (e == cudaSuccess && x)
-    e = moe::launch_scatter_rows(*cfg, x, dst_row, x_perm, d->sms, status, s);
+    e = moe::launch_scatter_rows(*cfg, x, dst_row, x_perm, d->sms, status, s, true);
   return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
