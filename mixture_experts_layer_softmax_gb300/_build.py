@@ -25,7 +25,7 @@ NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "--expt-relaxed-constexpr
                      "-Xcompiler", "-fPIC,-O2", "-I", INCLUDE]
 
 LIBS = {
-    "libmoe_gb300.so": ["api.cu", "router.cu", "permute.cu", "combine.cu", "gemm_simt.cu",
+    "libmoe_gb300.so": ["api.cu", "router.cu", "router_tc.cu", "permute.cu", "combine.cu", "gemm_simt.cu",
                         "gemm_tc.cu", "gemm_tc2.cu", "gemm_tc_bwd.cu", "bwd.cu", "permute_noalloc.cu",
                         "aux_loss.cu", "gemm_mxfp8.cu"],
     "libmoe_synth.so": ["synth.cu"],

@@ -60,6 +60,16 @@ MOE_HD int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 MOE_HD size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 // Exact GELU (erf form) and SiLU in fp32.  erff/expf are CUDA's own.
+// The exact three-way bf16 split of an fp32 value: hi = bf16(w),
+// mid = bf16(w - hi), lo = bf16(w - hi - mid); each difference is exact in
+// fp32 and w = hi + mid + lo (8 + 8 + 8 mantissa bits).
+MOE_D void split3_bf16(float w, __nv_bfloat16& hi, __nv_bfloat16& mid, __nv_bfloat16& lo) {
+  hi = __float2bfloat16_rn(w);
+  const float r1 = w - __bfloat162float(hi);
+  mid = __float2bfloat16_rn(r1);
+  lo = __float2bfloat16_rn(r1 - __bfloat162float(mid));
+}
+
 MOE_D float gelu_f(float z) { return 0.5f * z * (1.0f + erff(z * 0.70710678118654752f)); }
 MOE_D float sigmoid_f(float z) { return 1.0f / (1.0f + expf(-z)); }
 MOE_D float silu_f(float z) { return z * sigmoid_f(z); }

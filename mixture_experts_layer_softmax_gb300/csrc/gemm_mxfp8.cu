@@ -322,14 +322,6 @@ MOE_D void decode_tile(const MxCtl& c, int E, int nblk, int tile, int& e, int& m
   mb = local - nb * mblk;
 }
 
-MOE_D void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          dst),
-      "l"(src), "r"(bytes), "r"(bar)
-      : "memory");
-}
-
 template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_mxfp8_kernel(const __grid_constant__ CUtensorMap tmA,
@@ -434,9 +426,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc::tma_load_2d(a_dst, &tmA, kb * BK, a_row, fb);
           tc::tma_load_2d(b_dst, &tmB, kb * BK, b_row0, fb);
           tc::tma_load_2d(b_dst + B_BYTES / 2, &tmB, kb * BK, b_row1, fb);
-          bulk_load(sf_dst, p.a_sf + (a_atom + kb) * ATOM, ATOM, fb);
-          bulk_load(sf_dst + ATOM, p.b_sf + (b_atom0 + kb) * ATOM, ATOM, fb);
-          if (two_b) bulk_load(sf_dst + 2 * ATOM, p.b_sf + (b_atom1 + kb) * ATOM, ATOM, fb);
+          tc::bulk_load(sf_dst, p.a_sf + (a_atom + kb) * ATOM, ATOM, fb);
+          tc::bulk_load(sf_dst + ATOM, p.b_sf + (b_atom0 + kb) * ATOM, ATOM, fb);
+          if (two_b) tc::bulk_load(sf_dst + 2 * ATOM, p.b_sf + (b_atom1 + kb) * ATOM, ATOM, fb);
           issued |= 1u << stage;
           issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
           if (++stage == STAGES) { stage = 0; phase ^= 1; }

@@ -64,20 +64,10 @@ struct SmemCtl {
 constexpr size_t kSmemBytes = 1024 + (size_t)STAGES * STAGE_BYTES + sizeof(SmemCtl);
 
 // ---- cluster / pair PTX ------------------------------------------------------
-MOE_D uint32_t cluster_ctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-MOE_D uint32_t mapa(uint32_t addr, uint32_t rank) {
-  uint32_t out;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(out) : "r"(addr), "r"(rank));
-  return out;
-}
-MOE_D void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
-                   : "memory");
-}
+using tc::arrive_cluster;
+using tc::cluster_ctarank;
+using tc::cluster_sync;
+using tc::mapa;
 MOE_D void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, int32_t c0, int32_t c1,
                             uint32_t bar_cluster) {
   asm volatile(
@@ -115,10 +105,6 @@ MOE_D void commit_pair_multicast(uint32_t bar, uint16_t mask) {
       " [%0], %1;" ::"r"(bar),
       "h"(mask)
       : "memory");
-}
-MOE_D void arrive_cluster(uint32_t bar_cluster) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster)
-               : "memory");
 }
 
 MOE_D void decode_tile(const SmemCtl& c, int E, int nblk, int tile, int& e, int& mb, int& nb) {

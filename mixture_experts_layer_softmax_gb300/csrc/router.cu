@@ -8,7 +8,9 @@
 // selected scores by their sum (MOE_FLAG_RENORM).
 //
 // Kernels:
-//  * bf16 tokens (every E): the gating GEMM runs on the tensor cores.  W_r
+//  * bf16 tokens, E <= 8: router_tc_small (router_tc.cu), the whole route in
+//    one launch on the tensor cores.
+//  * other bf16 tokens: the gating GEMM runs on the tensor cores.  W_r
 //    (fp32) is split exactly into three bf16 parts, w = hi + mid + lo (24
 //    mantissa bits = 3 x 8), tiled so that each GEMM tile holds the three
 //    parts of a group of experts; x (bf16, exact) times each part is exact in
@@ -26,209 +28,9 @@
 
 #include <algorithm>
 
-#include "common.cuh"
+#include "router_select.cuh"
 
 namespace moe {
-
-struct RouterArgs {
-  int T, E, K, h;
-  int score;
-  bool renorm, force_balance;
-  const float* sel_bias;
-  int32_t* topk_idx;
-  float* topk_prob;
-  uint8_t* routing_map;
-};
-
-// fp32(sigma(l)) with sigma evaluated in double.  Kept out of line: the
-// double-precision path must stay behind a real branch (GB300's FP64 rate is
-// low), never be computed speculatively for every key.
-__device__ __noinline__ float sigmoid_exact_f32(float l) {
-  return (float)(1.0 / (1.0 + exp(-(double)l)));
-}
-
-// Selection key of one (token, expert): softmax uses the logit, sigmoid uses
-// fp32(sigma(l)) with sigma evaluated in double; then + sel_bias in fp32.
-MOE_D float selection_key(float l, int e, const RouterArgs& a) {
-  float key = l;
-  if (a.score == MOE_SCORE_SIGMOID) key = sigmoid_exact_f32(l);
-  if (a.sel_bias) key = __fadd_rn(key, __ldg(a.sel_bias + e));
-  return key;
-}
-
-// The same key with sigma in fp32 (CUDA's expf, within 2 ulp, then a rounded
-// add and a rounded divide): it differs from selection_key by at most
-// 4.2e-7 * sigma + ulp(key) <= 5.4e-7 + 1.2e-7 |b|.
-MOE_D float selection_key_fast(float l, int e, const RouterArgs& a) {
-  float key = l;
-  if (a.score == MOE_SCORE_SIGMOID) key = sigmoid_f(l);
-  if (a.sel_bias) key = __fadd_rn(key, __ldg(a.sel_bias + e));
-  return key;
-}
-
-// Order-preserving map of fp32 keys onto uint32 (larger key, larger code;
-// -0 is folded onto +0 so the two compare equal, as floats do).  Every finite
-// key maps above 0.
-MOE_D uint32_t sortable_key(float k) {
-  const uint32_t b = __float_as_uint(k == 0.f ? 0.f : k);
-  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
-}
-MOE_D float from_sortable_key(uint32_t u) {
-  return __uint_as_float((u & 0x80000000u) ? (u & 0x7fffffffu) : ~u);
-}
-
-// Selects K experts for one token whose logits are spread over the warp
-// (slot j of lane l is expert l + 32 j) and writes idx/prob/routing_map.
-//
-// Sigmoid keys are first ranked with the fp32 sigma.  That ranking equals
-// the one of the exact keys whenever the K + 1 best fast keys are separated
-// by more than twice their error bound (the selected set and its order cannot
-// change); otherwise, for that token only, the keys are recomputed with the
-// double-precision sigma and ranked again.
-template <int J>
-MOE_D void select_and_write(const float (&logit)[J], int t, const RouterArgs& a, int lane) {
-  const unsigned FULL = 0xffffffffu;
-  uint32_t taken = 0u;  // bit j: slot j of this lane is selected (a register, not an array)
-  float key[J];
-  int my_idx = -1;      // lane k < K ends up holding the k-th selected expert
-  float my_logit = 0.f; // and its logit
-  if (a.force_balance) {
-    if (lane < a.K) my_idx = (int)(((int64_t)t * a.K + lane) % a.E);
-#pragma unroll
-    for (int j = 0; j < J; ++j) {
-      const int e = lane + 32 * j;
-      // expert e is selected iff (e - t*K) mod E < K
-      const int64_t d = (((int64_t)e - (int64_t)t * a.K) % a.E + a.E) % a.E;
-      if (e < a.E && d < a.K) taken |= 1u << j;
-    }
-  } else {
-    bool exact = a.score != MOE_SCORE_SIGMOID;  // logits are the exact softmax keys
-    for (int pass = 0; pass < 2; ++pass) {
-      taken = 0u;
-      if (exact) {
-#pragma unroll
-        for (int j = 0; j < J; ++j) {
-          const int e = lane + 32 * j;
-          key[j] = -FLT_MAX;
-          if (e < a.E) key[j] = selection_key(logit[j], e, a);
-        }
-      } else {
-#pragma unroll
-        for (int j = 0; j < J; ++j) {
-          const int e = lane + 32 * j;
-          key[j] = -FLT_MAX;
-          if (e < a.E) key[j] = selection_key_fast(logit[j], e, a);
-        }
-      }
-      // the fast pass also ranks the (K+1)-th key, to check the K-th gap
-      const int rounds = exact ? a.K : min(a.K + 1, a.E);
-      uint32_t skey[J];
-#pragma unroll
-      for (int j = 0; j < J; ++j) skey[j] = sortable_key(key[j]);
-      bool safe = true;
-      float prev = 0.f;
-      for (int k = 0; k < rounds; ++k) {
-        // this lane's best untaken candidate (ascending j: ties keep the
-        // lower expert), then the warp's largest key and, among the lanes
-        // holding it, the lowest expert index: two warp reductions
-        uint32_t lk = 0u;
-        int li = 0x7fffffff;
-#pragma unroll
-        for (int j = 0; j < J; ++j) {
-          const int e = lane + 32 * j;
-          if (e < a.E && !((taken >> j) & 1u) && skey[j] > lk) {
-            lk = skey[j];
-            li = e;
-          }
-        }
-        const uint32_t m = __reduce_max_sync(FULL, lk);
-        const int bi = (int)__reduce_min_sync(FULL, lk == m ? (uint32_t)li : 0xffffffffu);
-        const float bk = from_sortable_key(m);
-        if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-        if (k < a.K && lane == k) my_idx = bi;
-        if (!exact && k > 0 && !(prev - bk > 4e-6f * (1.f + fabsf(prev) + fabsf(bk))))
-          safe = false;  // warp-uniform: bk and prev are the same on every lane
-        prev = bk;
-      }
-      if (exact || safe) break;
-      exact = true;
-    }
-    // the (K+1)-th key of the fast pass was marked taken only to rank it
-    if (a.routing_map) {
-      taken = 0u;
-#pragma unroll
-      for (int k = 0; k < 16; ++k) {
-        if (k >= a.K) break;
-        const int e = __shfl_sync(FULL, my_idx, k);
-        if ((e & 31) == lane) taken |= 1u << (e >> 5);
-      }
-    }
-  }
-  // logit of this lane's selected expert
-  {
-    float sel_l = 0.f;
-#pragma unroll
-    for (int j = 0; j < J; ++j) {
-      // fetch logit of expert my_idx from lane my_idx & 31, slot my_idx >> 5
-      const int src = my_idx & 31;
-      const float v = __shfl_sync(FULL, logit[j], src);
-      if (my_idx >= 0 && (my_idx >> 5) == j) sel_l = v;
-    }
-    my_logit = sel_l;
-  }
-  const bool active = lane < a.K;
-  float p = 0.f;
-  if (a.score == MOE_SCORE_SOFTMAX) {
-    if (a.renorm) {
-      float m = active ? my_logit : -INFINITY;
-#pragma unroll
-      for (int off = 16; off >= 1; off >>= 1) m = fmaxf(m, __shfl_xor_sync(FULL, m, off));
-      const float ex = active ? expf(my_logit - m) : 0.f;
-      float s = ex;
-#pragma unroll
-      for (int off = 16; off >= 1; off >>= 1) s += __shfl_xor_sync(FULL, s, off);
-      p = ex / s;
-    } else {
-      float m = -INFINITY;
-#pragma unroll
-      for (int j = 0; j < J; ++j)
-        if (lane + 32 * j < a.E) m = fmaxf(m, logit[j]);
-#pragma unroll
-      for (int off = 16; off >= 1; off >>= 1) m = fmaxf(m, __shfl_xor_sync(FULL, m, off));
-      float s = 0.f;
-#pragma unroll
-      for (int j = 0; j < J; ++j)
-        if (lane + 32 * j < a.E) s += expf(logit[j] - m);
-#pragma unroll
-      for (int off = 16; off >= 1; off >>= 1) s += __shfl_xor_sync(FULL, s, off);
-      p = expf(my_logit - m) / s;
-    }
-  } else {
-    const float sg = active ? sigmoid_f(my_logit) : 0.f;
-    float s = 0.f;
-    if (a.renorm) {
-      s = sg;
-    } else {
-#pragma unroll
-      for (int j = 0; j < J; ++j)
-        if (lane + 32 * j < a.E) s += sigmoid_f(logit[j]);
-    }
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) s += __shfl_xor_sync(FULL, s, off);
-    p = sg / s;
-  }
-  if (active) {
-    a.topk_idx[(int64_t)t * a.K + lane] = my_idx;
-    a.topk_prob[(int64_t)t * a.K + lane] = p;
-  }
-  if (a.routing_map) {
-#pragma unroll
-    for (int j = 0; j < J; ++j) {
-      const int e = lane + 32 * j;
-      if (e < a.E) a.routing_map[(int64_t)t * a.E + e] = (taken >> j) & 1u;
-    }
-  }
-}
 
 // ---- top-k on given logits: one warp per token --------------------------
 // logits: [T, E] fp32; or, when parts is given, the tensor-core router's
@@ -311,12 +113,7 @@ __global__ void split_router_weight_kernel(const float* __restrict__ w_r, int E,
       const float wv[4] = {w.x, w.y, w.z, w.w};
       __nv_bfloat16 hi[4], mid[4], lo[4];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        hi[j] = __float2bfloat16_rn(wv[j]);
-        const float r1 = wv[j] - __bfloat162float(hi[j]);
-        mid[j] = __float2bfloat16_rn(r1);
-        lo[j] = __float2bfloat16_rn(r1 - __bfloat162float(mid[j]));
-      }
+      for (int j = 0; j < 4; ++j) split3_bf16(wv[j], hi[j], mid[j], lo[j]);
       hv = *reinterpret_cast<const uint2*>(hi);
       mv = *reinterpret_cast<const uint2*>(mid);
       lv = *reinterpret_cast<const uint2*>(lo);
@@ -555,6 +352,10 @@ cudaError_t launch_router_gemm_tc(int T, const void* x, int h, const void* w3, i
                                   int bn, float* logit_parts, int ldo, const int32_t* offsets,
                                   int ksplit, int64_t split_stride, int sms, int* status,
                                   cudaStream_t s);
+bool router_tc_small_ok(const moe_config_t& c);
+cudaError_t launch_router_tc_small(const moe_config_t& c, const void* x, const float* w_r,
+                                   const float* gate_bias, float* logits, const RouterArgs& a,
+                                   int sms, int* status, cudaStream_t s);
 
 cudaError_t launch_router(const moe_config_t& c, const void* x, const float* w_r,
                           const float* gate_bias, const float* sel_bias, float* logits,
@@ -562,6 +363,8 @@ cudaError_t launch_router(const moe_config_t& c, const void* x, const float* w_r
                           int sms, int* status, cudaStream_t s) {
   if (c.T == 0) return cudaSuccess;
   RouterArgs a = make_args(c, sel_bias, idx, prob, map);
+  if (router_tc_small_ok(c))  // one launch: gating, slice sum and selection
+    return launch_router_tc_small(c, x, w_r, gate_bias, logits, a, sms, status, s);
   if (c.dtype == MOE_BF16) {
     const int ept = router_ept(c.E), bn = router_bn(c.E);
     const int ntiles = router_ntiles(c.E);

@@ -82,6 +82,63 @@ MOE_D bool mbar_wait(uint32_t bar, uint32_t parity, const WaitCtl& w) {
   }
 }
 
+// The same bounded wait with cluster-scope acquire: for a barrier that CTAs
+// of the cluster arrive on remotely (release.cluster) after writing this
+// CTA's shared memory.
+MOE_D bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred P1;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 P1, [%1], %2;\n\t"
+      "selp.b32 %0, 1, 0, P1;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+MOE_D bool mbar_wait_cluster(uint32_t bar, uint32_t parity, const WaitCtl& w) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (int64_t i = 1;; ++i) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    if ((i & 63) == 0) {
+      if (w.abort && *w.abort) return false;
+      if ((w.max_polls > 0 && i >= w.max_polls) || globaltimer_ns() - t0 > w.limit_ns) {
+        report(w.status, MOE_ERR_TIMEOUT);
+        if (w.abort) *w.abort = 1;
+        return false;
+      }
+    }
+  }
+}
+
+// ---- clusters -----------------------------------------------------------------
+MOE_D uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// The address of this CTA's shared-memory location `addr` in CTA `rank`.
+MOE_D uint32_t mapa(uint32_t addr, uint32_t rank) {
+  uint32_t out;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(out) : "r"(addr), "r"(rank));
+  return out;
+}
+MOE_D void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
+// Arrive on an mbarrier of any CTA of the cluster (address from mapa).
+MOE_D void arrive_cluster(uint32_t bar_cluster) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster)
+               : "memory");
+}
+MOE_D void st_cluster_f32x4(uint32_t addr, float a, float b, float c, float d) {
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b),
+               "f"(c), "f"(d)
+               : "memory");
+}
+
 // ---- TMA --------------------------------------------------------------------
 MOE_D void tma_load_2d(uint32_t dst, const CUtensorMap* map, int32_t c0, int32_t c1,
                        uint32_t bar) {
@@ -101,6 +158,16 @@ MOE_D void tma_gather4(uint32_t dst, const CUtensorMap* map, int32_t c0, int32_t
       " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(r0), "r"(r1), "r"(r2), "r"(r3),
       "r"(bar)
+      : "memory");
+}
+// Untiled bulk copy of `bytes` (a multiple of 16) from global to shared
+// memory, both addresses 16-byte aligned; completes as transaction bytes on
+// the mbarrier `bar`.
+MOE_D void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst),
+      "l"(src), "r"(bytes), "r"(bar)
       : "memory");
 }
 MOE_D void prefetch_tensormap(const CUtensorMap* map) {

@@ -83,10 +83,14 @@ def test_router_sigmoid_near_ties_bit_exact(bias):
     (256, 128, 8, 2, 0, "f32", False), (100, 256, 16, 4, 0, "bf16", True),
     (100, 64, 32, 8, 1, "f32", False), (300, 512, 128, 8, 0, "bf16", True),
     (200, 7168, 256, 8, 1, "bf16", False), (64, 200, 5, 2, 0, "bf16", False),
-    # fused bf16 router with 16 and 32 padded experts, and with several token
-    # groups per warp; a 32-expert weight too large for shared memory (tensor cores)
+    # 16, 20 and 32 experts (tensor cores, one tile of experts), a large batch of
+    # the streamed router, and a 32-expert weight with a long h
     (130, 1024, 32, 4, 0, "bf16", True), (90, 512, 20, 3, 1, "bf16", False),
     (20000, 256, 8, 2, 0, "bf16", True), (77, 2048, 32, 8, 1, "bf16", False),
+    # the one-launch router (bf16, E <= 8): a ragged last tile, a long h, and
+    # h <= 64, where the second CTA of the pair has no K block
+    (8193, 4096, 8, 2, 1, "bf16", True), (300, 4608, 8, 2, 0, "bf16", False),
+    (100, 64, 8, 2, 0, "bf16", True), (129, 8, 3, 1, 1, "bf16", False),
 ])
 def test_router_gating_matches_oracle(T, h, E, K, score, dtype, gate_bias):
     M = lib()
@@ -111,6 +115,42 @@ def test_router_gating_matches_oracle(T, h, E, K, score, dtype, gate_bias):
     margin = O.selection_margin(ol, K, score)
     ok = margin >= 1e-5
     np.testing.assert_array_equal(to_np(idx)[ok], oi[ok])
+
+
+@pytest.mark.parametrize("E,K,score,renorm,bias,force", [
+    (8, 2, 0, True, False, False), (8, 2, 0, False, False, False), (8, 8, 0, True, False, False),
+    (8, 3, 1, True, True, False), (8, 4, 1, False, False, False), (5, 2, 1, True, True, False),
+    (8, 2, 0, True, False, True), (6, 3, 1, True, False, True), (1, 1, 0, True, False, False),
+])
+def test_router_small_e_selection_matches_warp_selection(E, K, score, renorm, bias, force):
+    """The one-launch router for E <= 8 selects with one thread per token; on
+    the logits it wrote, the warp-per-token selection must give the same
+    experts and bit-identical probabilities."""
+    M = lib()
+    T, h = 1000, 512
+    x = inputs.normal((T, h), 1.0, 31, 1, "bf16")
+    w_r = inputs.normal((E, h), 0.05, 31, 2)
+    if score == M.MOE_SCORE_SIGMOID:  # many near ties among the sigmoid keys
+        w_r[:, :] *= 0.02
+    b = inputs.normal((E,), 0.01, 31, 3) if bias else None
+    flags = (M.MOE_FLAG_RENORM if renorm else 0) | (M.MOE_FLAG_FORCE_BALANCE if force else 0)
+    cfg = M.make_config(T, h, E, K, 16, M.MOE_BF16, score, M.MOE_ACT_SWIGLU, 0, 0, flags)
+    logits = torch.empty(T, E, dtype=torch.float32, device="cuda")
+    idx = torch.empty(T, K, dtype=torch.int32, device="cuda")
+    prob = torch.empty(T, K, dtype=torch.float32, device="cuda")
+    rmap = torch.empty(T, E, dtype=torch.uint8, device="cuda")
+    ws = torch.empty(M.moe_workspace_size(cfg), dtype=torch.uint8, device="cuda")
+    bd = None if b is None else to_dev(b, "f32")
+    M.moe_router_topk(cfg, to_dev(x, "bf16"), to_dev(w_r, "f32"), None, bd, logits, idx, prob,
+                      rmap, ws)
+    idx2 = torch.empty_like(idx)
+    prob2 = torch.empty_like(prob)
+    rmap2 = torch.empty_like(rmap)
+    M.moe_router_topk_from_logits(cfg, logits, bd, idx2, prob2, rmap2)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(to_np(idx), to_np(idx2))
+    np.testing.assert_array_equal(to_np(prob).view(np.uint32), to_np(prob2).view(np.uint32))
+    np.testing.assert_array_equal(to_np(rmap), to_np(rmap2))
 
 
 @pytest.mark.parametrize("T,E,K,skew", [
