@@ -93,8 +93,14 @@ constexpr size_t smem_bytes() {
          sizeof(SmemCtl<Tile<BNT>::STAGES>);
 }
 
+// Tile -> (group e, m block, n block).  Within a group the m blocks run
+// fastest, so the CTAs that run together share one weight panel; with
+// n_fastest (the router's gating GEMM: one group, a weight of a few MB, a
+// token matrix that may exceed L2) the n blocks of one m block run together
+// and share its token rows instead.
 template <typename Ctl>
-MOE_D void decode_tile(const Ctl& c, int E, int nblk, int tile, int& e, int& mb, int& nb) {
+MOE_D void decode_tile(const Ctl& c, int E, int nblk, int tile, int& e, int& mb, int& nb,
+                       bool n_fastest = false) {
   int lo = 0, hi = E - 1;  // largest e with tile_start[e] <= tile
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
@@ -102,6 +108,11 @@ MOE_D void decode_tile(const Ctl& c, int E, int nblk, int tile, int& e, int& mb,
   }
   e = lo;
   const int local = tile - c.tile_start[e];
+  if (n_fastest) {
+    mb = local / nblk;
+    nb = local - mb * nblk;
+    return;
+  }
   const int mblk = (c.off[e + 1] - c.off[e] + BM - 1) / BM;
   nb = local / mblk;
   mb = local - nb * mblk;
@@ -208,7 +219,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
       int e, mb, nb;
-      decode_tile(ctl, E, nblk, tile / S, e, mb, nb);
+      decode_tile(ctl, E, nblk, tile / S, e, mb, nb, MODE == kTcF32);
       const int m_e = ctl.off[e + 1] - ctl.off[e];
       int b_row0, b_row1 = 0;
       if (MODE == kTcSwiGLU) {
@@ -257,7 +268,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0, issued = 0, issued_par = 0;
       for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
         int e, mb, nb;
-        decode_tile(ctl, E, nblk, tile / S, e, mb, nb);
+        decode_tile(ctl, E, nblk, tile / S, e, mb, nb, MODE == kTcF32);
         const int kb0 = MODE == kTcF32 ? (tile % S) * p.kb_per : 0;
         const int kb1 = MODE == kTcF32 ? min(KB, kb0 + p.kb_per) : KB;
         const int a_row = ctl.off[e] + mb * BM;
@@ -337,7 +348,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t acc_phase = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
       int e, mb, nb;
-      decode_tile(ctl, E, nblk, tile / S, e, mb, nb);
+      decode_tile(ctl, E, nblk, tile / S, e, mb, nb, MODE == kTcF32);
       if (!tc::mbar_wait(tc::smem_u32(&ctl.tmem_full[acc]), acc_phase, wc)) break;
       tc::fence_after_sync();
       const int m_e = ctl.off[e + 1] - ctl.off[e];
