@@ -75,7 +75,11 @@ MOE_D float from_sortable_key(uint32_t u) {
 // the one of the exact keys whenever the K + 1 best fast keys are separated
 // by more than twice their error bound (the selected set and its order cannot
 // change); otherwise, for that token only, the keys are recomputed with the
-// double-precision sigma and ranked again.
+// double-precision sigma and ranked again.  The exact pass evaluates only the
+// experts whose fast key is within twice the error bound of the (K+1)-th fast
+// key: any other expert has K + 1 experts whose exact keys are strictly above
+// its own, so it cannot be selected (GB300's FP64 rate makes the full
+// re-evaluation a long tail for the warps that need it).
 template <int J>
 MOE_D void select_and_write(const float (&logit)[J], int t, const RouterArgs& a, int lane) {
   const unsigned FULL = 0xffffffffu;
@@ -94,14 +98,16 @@ MOE_D void select_and_write(const float (&logit)[J], int t, const RouterArgs& a,
     }
   } else {
     bool exact = a.score != MOE_SCORE_SIGMOID;  // logits are the exact softmax keys
+    float cutoff = -INFINITY;  // exact pass after a fast one: keys that may reach the top K + 1
+    float last = 0.f;          // the last key the fast pass ranked
     for (int pass = 0; pass < 2; ++pass) {
       taken = 0u;
       if (exact) {
 #pragma unroll
         for (int j = 0; j < J; ++j) {
           const int e = lane + 32 * j;
-          key[j] = -FLT_MAX;
-          if (e < a.E) key[j] = selection_key(logit[j], e, a);
+          const bool cand = e < a.E && (pass == 0 || key[j] >= cutoff);  // key[]: fast keys
+          key[j] = cand ? selection_key(logit[j], e, a) : -FLT_MAX;
         }
       } else {
 #pragma unroll
@@ -140,9 +146,11 @@ MOE_D void select_and_write(const float (&logit)[J], int t, const RouterArgs& a,
         if (!exact && k > 0 && !(prev - bk > 4e-6f * (1.f + fabsf(prev) + fabsf(bk))))
           safe = false;  // warp-uniform: bk and prev are the same on every lane
         prev = bk;
+        last = bk;
       }
       if (exact || safe) break;
       exact = true;
+      if (rounds == a.K + 1) cutoff = last - 4e-6f * (1.f + fabsf(last));
     }
     // the (K+1)-th key of the fast pass was marked taken only to rank it
     if (a.routing_map) {
@@ -245,13 +253,26 @@ MOE_D void select_row8(const float (&l)[8], int t, const RouterArgs& a) {
       if (k < a.K) sel[k] = (int)(((int64_t)t * a.K + k) % a.E);
   } else {
     bool exact = a.score != MOE_SCORE_SIGMOID;
+    float fk[8];                // fast keys (sigmoid, first pass)
+    float cutoff = -INFINITY;   // exact pass: only keys that may reach the top K + 1
+#pragma unroll
+    for (int e = 0; e < 8; ++e) fk[e] = 0.f;
+#pragma unroll
     for (int pass = 0; pass < 2; ++pass) {
       uint32_t sk[8];  // order-preserving codes; 0 (below every key) past E
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
         uint32_t c = 0u;
-        if (e < a.E)
-          c = sortable_key(exact ? selection_key(l[e], e, a) : selection_key_fast(l[e], e, a));
+        if (e < a.E) {
+          if (!exact) {
+            fk[e] = selection_key_fast(l[e], e, a);
+            c = sortable_key(fk[e]);
+          } else if (pass == 0 || fk[e] >= cutoff) {
+            c = sortable_key(selection_key(l[e], e, a));
+          } else {
+            c = sortable_key(-FLT_MAX);
+          }
+        }
         sk[e] = c;
       }
       int rank[8];
@@ -287,6 +308,14 @@ MOE_D void select_row8(const float (&l)[8], int t, const RouterArgs& a) {
         }
       if (safe) break;
       exact = true;
+      if (rounds == a.K + 1) {
+        uint32_t lc = 0u;  // the code of rank K (a register select: no dynamic index)
+#pragma unroll
+        for (int k = 0; k < 9; ++k)
+          if (k == a.K) lc = code_at[k];
+        const float last = from_sortable_key(lc);
+        cutoff = last - 4e-6f * (1.f + fabsf(last));
+      }
     }
   }
   uint32_t taken = 0u;
