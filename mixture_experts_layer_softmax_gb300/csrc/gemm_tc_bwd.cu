@@ -460,29 +460,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = [] {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      return reinterpret_cast<EncodeTiledFn>(ptr);
-    return (EncodeTiledFn) nullptr;
-  }();
-  return fn;
-}
-
 // bf16 map with a {64, rows} box: 2-D [rows, cols] when depth == 0, else
 // 3-D [depth][rows][cols].  128-byte swizzle, zero fill out of bounds.
 bool encode_map(CUtensorMap* m, const void* base, uint64_t depth, uint64_t rows, uint64_t cols,
                 uint32_t box_rows) {
-  EncodeTiledFn fn = encode_fn();
+  tc::EncodeTiledFn fn = tc::encode_tiled_fn();
   if (!fn) return false;
   const cuuint64_t dims[3] = {cols, rows, depth ? depth : 1};
   const cuuint64_t strides[2] = {cols * 2, rows * cols * 2};

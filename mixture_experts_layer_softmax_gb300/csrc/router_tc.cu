@@ -32,7 +32,6 @@
 // wait is bounded; a wait that gives up records MOE_ERR_TIMEOUT, every role
 // leaves its loop, copies and MMAs in flight are waited for, TMEM is freed.
 #include <algorithm>
-#include <mutex>
 
 #include "router_select.cuh"
 #include "tc_ptx.cuh"
@@ -316,25 +315,6 @@ __global__ void __cluster_dims__(kRCl, 1, 1) __launch_bounds__(kRThreads, 1)
   }
 }
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn router_encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(ptr);
-  });
-  return fn;
-}
-
 }  // namespace
 
 // bf16 tokens, E <= 8, h a multiple of 8 (TMA row strides are multiples of 16 bytes).
@@ -348,7 +328,7 @@ cudaError_t launch_router_tc_small(const moe_config_t& c, const void* x, const f
   (void)sms;  // one cluster per tile, whatever the SM count
   if (c.T == 0) return cudaSuccess;
   if (!router_tc_small_ok(c)) return cudaErrorInvalidValue;
-  EncodeTiledFn fn = router_encode_fn();
+  tc::EncodeTiledFn fn = tc::encode_tiled_fn();
   if (!fn) return cudaErrorInvalidValue;
   CUtensorMap mx, mw;
   {
