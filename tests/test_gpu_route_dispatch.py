@@ -91,6 +91,7 @@ def test_router_sigmoid_near_ties_bit_exact(bias):
     # h <= 64, where the second CTA of the pair has no K block
     (8193, 4096, 8, 2, 1, "bf16", True), (300, 4608, 8, 2, 0, "bf16", False),
     (100, 64, 8, 2, 0, "bf16", True), (129, 8, 3, 1, 1, "bf16", False),
+    (1, 512, 8, 2, 0, "bf16", True), (1, 512, 8, 8, 1, "bf16", False),
 ])
 def test_router_gating_matches_oracle(T, h, E, K, score, dtype, gate_bias):
     M = lib()
