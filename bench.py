@@ -536,11 +536,15 @@ def run_ours(args, w):
             M.moe_unpermute_combine(cfg, y_perm, dst_row, None, y_s if w.n_shared else None, y)
             mark(6)
 
-    # kernels of this library per step: route (bf16: split W_r, the gating
-    # GEMM, selection; fp32: one fused kernel for E <= 32, else GEMM and
-    # selection), dispatch (histogram, scan, ranks, row scatter), FC1 and FC2,
-    # the shared expert's two GEMMs (+ its offsets in moe_layer_fwd), combine
-    route_k = 3 if w.dtype == "bf16" else (1 if E <= 32 else 2)
+    # kernels of this library per step: route (bf16: one kernel for E <= 8,
+    # else split W_r, the gating GEMM, selection; fp32: one fused kernel for
+    # E <= 32, else GEMM and selection), dispatch (maps, row scatter), FC1 and
+    # FC2, the shared expert's two GEMMs (+ its offsets in moe_layer_fwd),
+    # combine
+    if w.dtype == "bf16":
+        route_k = 1 if E <= 8 else 3
+    else:
+        route_k = 1 if E <= 32 else 2
     # dispatch: histogram, per-expert scan (folded into the ranks kernel when
     # ceil(T/32) * E <= 8192), ranks, and the row scatter unless FC1 gathers
     maps_k = 2 if ((T + 31) // 32) * E <= 8192 else 3
