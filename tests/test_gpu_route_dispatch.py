@@ -84,11 +84,12 @@ def test_router_sigmoid_near_ties_bit_exact(bias):
     (100, 64, 32, 8, 1, "f32", False), (300, 512, 128, 8, 0, "bf16", True),
     (200, 7168, 256, 8, 1, "bf16", False), (64, 200, 5, 2, 0, "bf16", False),
     # 16, 20 and 32 experts (tensor cores, one tile of experts), a large batch of
-    # the streamed router, and a 32-expert weight with a long h
+    # the one-launch router (more clusters than fit at once), and a 32-expert
+    # weight with a long h
     (130, 1024, 32, 4, 0, "bf16", True), (90, 512, 20, 3, 1, "bf16", False),
     (20000, 256, 8, 2, 0, "bf16", True), (77, 2048, 32, 8, 1, "bf16", False),
     # the one-launch router (bf16, E <= 8): a ragged last tile, a long h, and
-    # h <= 64, where the second CTA of the pair has no K block
+    # h <= 64 (a single K block: three of the cluster's four CTAs have none)
     (8193, 4096, 8, 2, 1, "bf16", True), (300, 4608, 8, 2, 0, "bf16", False),
     (100, 64, 8, 2, 0, "bf16", True), (129, 8, 3, 1, 1, "bf16", False),
     (1, 512, 8, 2, 0, "bf16", True), (1, 512, 8, 8, 1, "bf16", False),
