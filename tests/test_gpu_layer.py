@@ -99,6 +99,11 @@ def small_workloads():
         W.Workload("edge_single_expert", T=130, h=128, E=1, K=1, F=136, seed=9),
         W.Workload("edge_gelu_bf16_bias", T=200, h=128, E=8, K=2, F=256, act=W.GELU, has_bias=True,
                    seed=9),
+        # the one-launch router inside the layer: sigmoid keys with a selection
+        # bias and a shared expert, and force-balanced routing
+        W.DSV3.replace(name="dsv3_like_E8_small", T=400, h=256, E=8, K=2, F=128),
+        W.Workload("mixtral_like_balanced_small", T=512, h=256, E=8, K=2, F=128,
+                   force_balance=True, seed=9),
     ]
 
 
