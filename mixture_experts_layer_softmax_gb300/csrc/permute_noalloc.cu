@@ -88,9 +88,12 @@ extern "C" moe_status_t moe_permute_noalloc(const moe_config_t* cfg, const void*
   if ((x == nullptr) != (x_perm == nullptr)) return MOE_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(x_perm)) return MOE_ERR_INVALID_ARG;
   if (cfg->flags & MOE_FLAG_VALIDATE_ONLY) return MOE_OK;
+  // The status word first: a failed lookup (or an injected failure) returns
+  // MOE_ERR_CUDA before anything is queued, as every other entry point does.
+  int* status = moe::device_status_word();
+  if (!status) return MOE_ERR_CUDA;
   NoAllocDevice* d = nullptr;
   if ((st = noalloc_setup(&d)) != MOE_OK) return st;
-  int* status = moe::device_status_word();
   // Both tables are fully rewritten by every call before they are read, so
   // nothing needs clearing between calls.
   int32_t* hist = d->scratch;

@@ -33,7 +33,7 @@ Sources (page title, then section / equation):
   parameters and total parameters" (a bias-free SwiGLU expert holds three
   h x F matrices).
 
-Readings where the pages are silent (each also listed in the design doc):
+Readings where the pages are silent, ambiguous or leave a step open:
 
 * Sigmoid normalisation: with RENORM the denominator runs over the selected
   top-K (DeepSeek-V3 style); without it, over all E experts (the page's

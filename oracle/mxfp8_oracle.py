@@ -24,7 +24,7 @@ Sources:
   - element code: x / 2^X rounded to nearest, ties to even, values beyond the
     largest finite magnitude saturated to +-448.
 
-Readings (each also listed in the design doc):
+Readings where the pages leave a step open:
 
 * Blocks run along the reduction (K) dimension of each GEMM operand: along h
   for x_perm and W1, along F for a and W2.  K is a multiple of 32.

@@ -108,6 +108,14 @@ def test_other_entry_points_validate(M):
     assert M.raw("moe_grouped_mlp_fwd")(ctypes.byref(gelu_b), P, P, P, P, None, P, None, None, P,
                                         P, big, None) == 1
     assert M.raw("moe_test_bounded_wait")(0, None) == 1
+    nal = M.raw("moe_permute_noalloc")
+    assert nal(ctypes.byref(cfg), P, P, P, P, P, P, P, P, P, None) == M.MOE_OK
+    assert nal(ctypes.byref(cfg), None, P, P, None, P, P, P, P, P, None) == M.MOE_OK  # maps only
+    assert nal(ctypes.byref(cfg), P, P, P, None, P, P, P, P, P, None) == M.MOE_ERR_INVALID_ARG
+    assert nal(ctypes.byref(cfg), P + 8, P, P, P, P, P, P, P, P, None) == M.MOE_ERR_INVALID_ARG
+    assert nal(ctypes.byref(cfg), P, P, P, P, None, P, P, P, P, None) == M.MOE_ERR_INVALID_ARG
+    assert nal(ctypes.byref(cfg), P, None, P, P, P, P, P, P, P, None) == M.MOE_ERR_INVALID_ARG
+    assert nal(None, P, P, P, P, P, P, P, P, P, None) == M.MOE_ERR_INVALID_ARG
 
 
 def test_mxfp8_argument_checks(M):

@@ -105,6 +105,13 @@ def test_step_entry_points_write_only_their_buffers():
     dst_row, src_token = g.new((T, K), i32, -1), g.new((P,), i32, -1)
     perm_prob = g.new((P,), torch.float32, float("nan"))
     M.moe_permute(cfg, x, idx, prob, x_perm, counts, offsets, dst_row, src_token, perm_prob, ws)
+    # the allocation-free dispatch writes the same buffers (and only them)
+    x_perm2 = g.new((P, h), torch.bfloat16, float("nan"))
+    counts2, offsets2 = g.new((E,), i32, -1), g.new((E + 1,), i32, -1)
+    dst_row2, src_token2 = g.new((T, K), i32, -1), g.new((P,), i32, -1)
+    perm_prob2 = g.new((P,), torch.float32, float("nan"))
+    M.moe_permute_noalloc(cfg, x, idx, prob, x_perm2, counts2, offsets2, dst_row2, src_token2,
+                          perm_prob2)
     H = g.new((P, 2 * F), torch.bfloat16, float("nan"))
     a = g.new((P, F), torch.bfloat16, float("nan"))
     M.moe_expert_fc1(cfg, x_perm, offsets, perm_prob, w1, None, H, a)
@@ -118,6 +125,10 @@ def test_step_entry_points_write_only_their_buffers():
     assert M.moe_get_error() == M.MOE_OK
     g.check()
     assert torch.isfinite(y.float()).all()
+    for a_, b_ in ((counts, counts2), (offsets, offsets2), (dst_row, dst_row2),
+                   (src_token, src_token2), (perm_prob, perm_prob2),
+                   (x_perm.view(torch.int16), x_perm2.view(torch.int16))):
+        assert torch.equal(a_, b_)
 
 
 def test_mxfp8_entry_points_write_only_their_buffers():

@@ -66,3 +66,51 @@ def test_noalloc_rejects_sizes_beyond_its_scratch():
     st = M.raw("moe_permute_noalloc")(ctypes.byref(cfg), None, 1 << 20, None, None, 1 << 20,
                                        1 << 20, 1 << 20, 1 << 20, None, None)
     assert st == M.MOE_ERR_UNSUPPORTED
+
+
+def test_noalloc_reports_bad_expert_ids_without_faulting():
+    """An out-of-range expert id is skipped and reported through the status
+    word, as moe_permute does; the next call on the shared scratch is clean."""
+    M = lib()
+    T, E, K, h = 64, 8, 2, 32
+    P = T * K
+    idx = np.tile(np.array([[0, 1]], np.int32), (T, 1))
+    idx[5, 1] = 99
+    cfg = M.make_config(T, h, E, K, 8, M.MOE_BF16, 0, M.MOE_ACT_SWIGLU, 0, 0, M.MOE_FLAG_RENORM)
+    x = torch.zeros(T, h, dtype=torch.bfloat16, device="cuda")
+    x_perm = torch.zeros(P, h, dtype=torch.bfloat16, device="cuda")
+    out = [torch.zeros(n, dtype=torch.int32, device="cuda") for n in (E, E + 1, P, P)]
+    M.moe_permute_noalloc(cfg, x, torch.from_numpy(idx).cuda(), None, x_perm, out[0], out[1],
+                          out[2], out[3], None)
+    assert M.moe_get_error() == M.MOE_ERR_DEVICE_BOUNDS
+    assert M.moe_get_error() == M.MOE_OK
+    assert int(out[1][-1]) == P - 1
+    idx[5, 1] = 2
+    M.moe_permute_noalloc(cfg, x, torch.from_numpy(idx).cuda(), None, x_perm, out[0], out[1],
+                          out[2], out[3], None)
+    assert M.moe_get_error() == M.MOE_OK
+    assert int(out[1][-1]) == P
+
+
+def test_noalloc_injected_failure_enqueues_nothing():
+    M = lib()
+    T, E, K, h = 100, 8, 2, 64
+    P = T * K
+    idx, prob = _routing(T, E, K, seed=7)
+    cfg = M.make_config(T, h, E, K, 8)
+    x = to_dev(inputs.normal((T, h), 1.0, 8, 1, "bf16"), "bf16")
+    bufs = _buffers(T, E, K, h)
+    assert M.moe_test_inject_cuda_failure(1) == 0
+    with pytest.raises(M.MoeError) as ei:
+        M.moe_permute_noalloc(cfg, x, torch.from_numpy(idx).cuda(), to_dev(prob, "f32"),
+                              bufs["x_perm"], bufs["counts"], bufs["offsets"], bufs["dst_row"],
+                              bufs["src_token"], bufs["perm_prob"])
+    assert ei.value.status == M.MOE_ERR_CUDA
+    torch.cuda.synchronize()
+    assert (bufs["counts"] == -1).all() and (bufs["dst_row"] == -1).all()
+    assert M.moe_test_inject_cuda_failure(0) == 0
+    M.moe_permute_noalloc(cfg, x, torch.from_numpy(idx).cuda(), to_dev(prob, "f32"),
+                          bufs["x_perm"], bufs["counts"], bufs["offsets"], bufs["dst_row"],
+                          bufs["src_token"], bufs["perm_prob"])
+    torch.cuda.synchronize()
+    assert int(bufs["offsets"][-1]) == P
