@@ -39,6 +39,12 @@ METRIC = "MoE-layer tokens/s on 1 GB300; grouped-GEMM % bf16 peak; permute/combi
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
+# stage boundaries recorded by moe_layer_fwd / moe_layer_bwd (moe_set_stage_events)
+FWD_STAGES = ["route", "dispatch", "fc1", "fc2", "shared", "combine"]
+BWD_STAGES = ["dy_scatter", "fc2_dgrad", "fc2_wgrad", "fc1_dgrad", "fc1_wgrad", "shared",
+              "router", "combine"]
+
+
 def parse():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
@@ -217,6 +223,22 @@ class OracleSample:
         self.w1s = w.host("w1_shared") if w.n_shared else None
         self.w2s = w.host("w2_shared") if w.n_shared else None
         self.experts = need
+        if w.backward:
+            # The training step on the sampled tokens as a compact layer of its
+            # own: only their experts (renumbered 0..n-1), their routing kept.
+            # Each token's dx, and its share of the weight gradients, depend
+            # only on its own experts, so the sample's work and its dx are the
+            # full step's for those tokens.
+            remap = {e: i for i, e in enumerate(need)}
+            logits, idx, probs = self.routing
+            tk = self.tokens
+            self.sub_routing = (logits[tk][:, need], np.vectorize(remap.get)(idx[tk]).astype(np.int32),
+                                probs[tk])
+            self.sub_x = self.x[tk]
+            self.sub_dy = w.host("dy")[tk]
+            self.sub_w_r = self.w_r[need]
+            self.sub_w1 = np.stack([self.w1[e] for e in need])
+            self.sub_w2 = np.stack([self.w2[e] for e in need])
 
     def run(self):
         from oracle import moe_oracle as O
@@ -224,6 +246,16 @@ class OracleSample:
         return O.layer_fwd(self.x, self.w_r, self.w1, self.w2, w.K, w.score, w.act, b1=self.b1,
                            b2=self.b2, w1_shared=self.w1s, w2_shared=self.w2s,
                            tokens=self.tokens, routing=self.routing)["y"]
+
+    def run_train(self):
+        """Forward then backward of the sampled tokens; returns their dx."""
+        from oracle import moe_oracle as O
+        w = self.w
+        args = (self.sub_x, self.sub_w_r, self.sub_w1, self.sub_w2)
+        O.layer_fwd(*args, w.K, w.score, w.act, w1_shared=self.w1s, w2_shared=self.w2s,
+                    routing=self.sub_routing)
+        return O.layer_bwd(*args, self.sub_dy, w.K, w.score, w.act, w1_shared=self.w1s,
+                           w2_shared=self.w2s, routing=self.sub_routing)["dx"]
 
 
 def blas_threads():
@@ -239,6 +271,8 @@ def blas_threads():
 
 def auto_sample(w):
     per_tok = 2.0 * (w.K + w.n_shared) * (3 if w.act == 1 else 2) * w.h * w.F
+    if w.backward:  # forward + backward: about three times the forward's work
+        per_tok *= 3
     return int(max(16, min(1024, 1.5e11 / per_tok)))
 
 
@@ -248,19 +282,20 @@ def run_reference(args, w):
         return
     S = args.sample_tokens or auto_sample(w)
     samp = OracleSample(w, S)
+    run = samp.run_train if w.backward else samp.run
     for _ in range(args.warmup):
-        samp.run()
+        run()
     times = []
     for _ in range(args.steps):
         t0 = time.perf_counter()
-        samp.run()
+        run()
         times.append(time.perf_counter() - t0)
     n = len(samp.tokens)
     ms = 1000.0 * statistics.mean(times)
     value = n / (ms / 1000.0)
     cores = blas_threads()
     sample = (f"{n} tokens of {w.name} routed only to experts {samp.experts}; float64 numpy "
-              f"oracle, one sample per step")
+              f"oracle ({'forward + backward' if w.backward else 'forward'}), one sample per step")
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
@@ -286,14 +321,17 @@ def workload_config(w):
 # ---------------------------------------------------------------------------
 # our arm
 # ---------------------------------------------------------------------------
-def kernel_hash():
+def kernel_hash(sources=None):
     h = hashlib.sha256()
-    for f in ("gemm_tc.cu", "gemm_tc2.cu", "tc_ptx.cuh", "common.cuh"):
+    for f in sources or ("gemm_tc.cu", "gemm_tc2.cu", "tc_ptx.cuh", "common.cuh"):
         h.update(open(os.path.join(ROOT, "mixture_experts_layer_softmax_gb300", "csrc", f), "rb").read())
     return h.hexdigest()[:16]
 
 
-def traffic_record(w):
+def traffic_record(w, stage="fc1"):
+    """DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum
+    from one ncu capture) of the kernel of `stage`, if profiles/traffic.json
+    holds a record for this workload taken with the current kernel sources."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
@@ -301,9 +339,61 @@ def traffic_record(w):
         rec = json.load(open(path)).get(w.name)
     except Exception:
         return None
-    if not rec or rec.get("kernel_hash") != kernel_hash():
+    if rec and stage != "fc1":
+        rec = rec.get("stages", {}).get(stage)
+    if not rec or rec.get("kernel_hash") != kernel_hash(rec.get("sources")):
         return None
-    return rec.get("fc1_bytes_per_launch")
+    return rec.get("bytes_per_launch", rec.get("fc1_bytes_per_launch"))
+
+
+def expert_gemm_work(w):
+    """Algorithmic work of each routed-expert grouped GEMM of the training
+    step: (FLOPs, bytes) per launch, every operand read once and every result
+    written once (b = 2 bytes, P = T*K permuted rows, R1 = 2F for SwiGLU)."""
+    T, h, E, K, F = w.T, w.h, w.E, w.K, w.F
+    P, R1, b = T * K, w.w1_rows, 2
+    nt = (F + 255) // 256  # dprob partials of the FC2 data gradient
+    return {
+        # x_perm, W1 in; a and the saved pre-activation H out
+        "fc1": (2.0 * P * h * R1, b * (P * h + E * R1 * h + P * F + P * R1)),
+        # a, W2 in; y_perm out
+        "fc2": (2.0 * P * F * h, b * (P * F + E * h * F + P * h)),
+        # dy_perm, W2, H in; dH and the dprob partials out
+        "fc2_dgrad": (2.0 * P * h * F, b * (P * h + E * h * F + P * R1 + P * R1) + 4 * P * nt),
+        # dy_perm, a in; dW2 out
+        "fc2_wgrad": (2.0 * P * h * F, b * (P * h + P * F + E * h * F)),
+        # dH, W1 in; dx_perm out
+        "fc1_dgrad": (2.0 * P * R1 * h, b * (P * R1 + E * R1 * h + P * h)),
+        # dH, x_perm in; dW1 out
+        "fc1_wgrad": (2.0 * P * R1 * h, b * (P * R1 + P * h + E * R1 * h)),
+    }
+
+
+GEMM_KERNELS = {
+    "fc1": "grouped_gemm_tc_kernel<FC1>", "fc2": "grouped_gemm_tc_kernel<FC2>",
+    "fc2_dgrad": "grouped_gemm_tc_bwd_kernel<dgrad> (FC2, dSwiGLU + dprob epilogue)",
+    "fc2_wgrad": "grouped_gemm_tc_bwd_kernel<wgrad> (dW2)",
+    "fc1_dgrad": "grouped_gemm_tc_bwd_kernel<dgrad> (FC1)",
+    "fc1_wgrad": "grouped_gemm_tc_bwd_kernel<wgrad> (dW1)",
+}
+
+
+def kernel_roofline(name, flops, nbytes, ms, pk, pk_kind, peak_tf):
+    """Roofline of one launch: bound by HBM when its arithmetic intensity is
+    below the ridge point of the measured peaks, else by the tensor cores."""
+    gbs = nbytes / (ms / 1000.0) / 1e9
+    tfs = flops / (ms / 1000.0) / 1e12
+    ridge = peak_tf * 1e12 / (pk["hbm_gbs"] * 1e9)
+    hbm = flops / nbytes < ridge
+    r = {"kernel": name, "bound": "hbm" if hbm else "tensor",
+         "achieved": gbs if hbm else tfs, "peak": pk["hbm_gbs"] if hbm else peak_tf,
+         "unit": "GB/s" if hbm else "TFLOP/s",
+         "peak_kind": (f"{pk_kind} HBM copy" if hbm else f"{pk_kind} bf16 burst (cuBLAS)"),
+         "bytes_per_launch": nbytes, "flops_per_launch": flops, "ms_per_launch": ms,
+         "hbm_gbs": gbs, "tflops": tfs, "tensor_frac": tfs / peak_tf,
+         "hbm_frac": gbs / pk["hbm_gbs"]}
+    r["frac"] = r["achieved"] / r["peak"]
+    return r
 
 
 def time_mxfp8(M, torch, w, cfg, x, w_r, gate_bias, sel_bias, w1, w2, w1s, w2s, flush_buf, hold,
@@ -487,7 +577,7 @@ def run_ours(args, w):
         # backward, each one C-ABI call, on the same workspace
         cfg = M.config_for(w, M.MOE_FLAG_SAVE_FOR_BWD | tiling)
         ws = torch.empty(M.moe_workspace_size(cfg), dtype=torch.uint8, device=dev)
-        dy = gen("dy", (T, h), bf, seed + 1)
+        dy = gen("dy", (T, h), bf, seed)
         dx = torch.empty(T, h, dtype=bf, device=dev)
         dw_r = torch.empty(E, h, dtype=torch.float32, device=dev)
         dw1 = torch.empty_like(w1)
@@ -496,15 +586,16 @@ def run_ours(args, w):
         dw2s = torch.empty_like(w2s) if w.n_shared else None
         stages = ["forward", "backward"]
 
-        def step(ev=None):
+        def step(ev=None, x_=None, dy_=None, dx_=None):
             if ev is not None:
                 ev[0].record(stream)
-            M.moe_layer_fwd(cfg, x, w_r, gate_bias, sel_bias, w1, b1, w2, b2, w1s, w2s, y, None,
-                            None, ws)
+            M.moe_layer_fwd(cfg, x if x_ is None else x_, w_r, gate_bias, sel_bias, w1, b1, w2,
+                            b2, w1s, w2s, y, None, None, ws)
             if ev is not None:
                 ev[1].record(stream)
-            M.moe_layer_bwd(cfg, x, w_r, w1, w2, w1s, w2s, dy, dx, dw_r, None, dw1, dw2, dw1s,
-                            dw2s, ws)
+            M.moe_layer_bwd(cfg, x if x_ is None else x_, w_r, w1, w2, w1s, w2s,
+                            dy if dy_ is None else dy_, dx if dx_ is None else dx_, dw_r, None,
+                            dw1, dw2, dw1s, dw2s, ws)
             if ev is not None:
                 ev[2].record(stream)
     else:
@@ -569,6 +660,19 @@ def run_ours(args, w):
         raise RuntimeError(f"device status after warm-up: {M.moe_status_string(st)}")
 
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in range(args.steps)]
+    # Training: the library records these events at the stage boundaries
+    # inside moe_layer_fwd / moe_layer_bwd (moe_set_stage_events), on the
+    # stream that launches the kernels, so every expert GEMM of the step is
+    # timed on its own inside the timed steps.
+    st_fwd = st_bwd = None
+    if train:
+        st_fwd = [[torch.cuda.Event(enable_timing=True) for _ in FWD_STAGES + ["end"]]
+                  for _ in range(args.steps)]
+        st_bwd = [[torch.cuda.Event(enable_timing=True) for _ in BWD_STAGES + ["end"]]
+                  for _ in range(args.steps)]
+        for e in [e for row in st_fwd + st_bwd for e in row]:
+            e.record(stream)  # creates the CUDA event
+        torch.cuda.synchronize()
     sampler = ClockSampler(local)
     sampler.start()
     time.sleep(0.3)
@@ -579,10 +683,16 @@ def run_ours(args, w):
     t_wall = time.perf_counter()
     for i in range(args.steps):
         flush_buf.fill_(1)
+        if train:
+            M.moe_set_stage_events(M.MOE_PASS_FWD, st_fwd[i])
+            M.moe_set_stage_events(M.MOE_PASS_BWD, st_bwd[i])
         hold()
         step(evs[i])
     torch.cuda.synchronize()
     t_wall = time.perf_counter() - t_wall
+    if train:
+        M.moe_set_stage_events(M.MOE_PASS_FWD, [])
+        M.moe_set_stage_events(M.MOE_PASS_BWD, [])
     sampler.window(False)
     if world > 1:
         torch.distributed.barrier()
@@ -639,6 +749,12 @@ def run_ours(args, w):
                                                             perm_prob, ws))
     per_step = [e[0].elapsed_time(e[n_ev - 1]) for e in evs]
     stage_ms = {s: statistics.mean(e[i].elapsed_time(e[i + 1]) for e in evs) for i, s in enumerate(stages)}
+    sub_ms = None
+    if train:
+        sub_ms = {"forward": {n: statistics.mean(r[j].elapsed_time(r[j + 1]) for r in st_fwd)
+                              for j, n in enumerate(FWD_STAGES)},
+                  "backward": {n: statistics.mean(r[j].elapsed_time(r[j + 1]) for r in st_bwd)
+                               for j, n in enumerate(BWD_STAGES)}}
     ms_eager = ms = statistics.mean(per_step)
 
     # The same step captured once in a CUDA graph (the layer never syncs or
@@ -675,44 +791,61 @@ def run_ours(args, w):
     ms = max_over_ranks(ms, world, dev)
     value = job_tokens_per_s(world, T, ms)
 
-    # ---- end to end through moe_layer_fwd with host buffers ----
-    # Every step copies its tokens in from pinned host memory and its output
+    # ---- end to end through the public calls with host buffers ----
+    # Every step copies its inputs in from pinned host memory and its result
     # back to pinned host memory; a copy stream overlaps step i+1's upload and
     # step i's download with step i's compute (double-buffered on both sides).
-    # All copies lie inside the timed region.
+    # All copies lie inside the timed region.  Forward: x in, y out through
+    # moe_layer_fwd.  Training: x and dy in, dx out (the gradient handed to
+    # the layer below) through moe_layer_fwd + moe_layer_bwd; the weight
+    # gradients stay on the device, where an optimizer step would use them.
     e2e = None
-    if not args.no_e2e and not train:
+    if not args.no_e2e:
         K2 = max(args.steps, 2)
-        x_host = [x.cpu().pin_memory(), x.cpu().pin_memory()]
-        y_host = [torch.empty(T, h, dtype=bf).pin_memory() for _ in range(2)]
-        x_in = [torch.empty_like(x), torch.empty_like(x)]
-        y_out = [torch.empty_like(y), torch.empty_like(y)]
+        srcs = [x, dy] if train else [x]
+        dsts = [dx] if train else [y]
+        host_in = [[t.cpu().pin_memory() for t in srcs] for _ in range(2)]
+        host_out = [[torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in dsts]
+                    for _ in range(2)]
+        dev_in = [[torch.empty_like(t) for t in srcs] for _ in range(2)]
+        dev_out = [[torch.empty_like(t) for t in dsts] for _ in range(2)]
         cs = torch.cuda.Stream(dev)
         ev_up = [torch.cuda.Event(), torch.cuda.Event()]
         ev_comp = [torch.cuda.Event(), torch.cuda.Event()]
         ev_down = [torch.cuda.Event(), torch.cuda.Event()]
 
+        def compute(b):
+            if train:
+                step(x_=dev_in[b][0], dy_=dev_in[b][1], dx_=dev_out[b][0])
+            else:
+                M.moe_layer_fwd(cfg, dev_in[b][0], w_r, gate_bias, sel_bias, w1, b1, w2, b2, w1s,
+                                w2s, dev_out[b][0], None, None, ws)
+
+        def upload(b):
+            for d_, h_ in zip(dev_in[b], host_in[b]):
+                d_.copy_(h_, non_blocking=True)
+
         def pipeline(n):
             with torch.cuda.stream(cs):
-                x_in[0].copy_(x_host[0], non_blocking=True)
+                upload(0)
                 ev_up[0].record(cs)
             for i in range(n):
                 b = i % 2
                 stream.wait_event(ev_up[b])
                 if i >= 2:
-                    stream.wait_event(ev_down[b])  # y_out[b] has been read back
-                M.moe_layer_fwd(cfg, x_in[b], w_r, gate_bias, sel_bias, w1, b1, w2, b2, w1s, w2s,
-                                y_out[b], None, None, ws)
+                    stream.wait_event(ev_down[b])  # dev_out[b] has been read back
+                compute(b)
                 ev_comp[b].record(stream)
                 with torch.cuda.stream(cs):
                     if i + 1 < n:
                         nb_ = (i + 1) % 2
                         if i >= 1:
-                            cs.wait_event(ev_comp[nb_])  # step i-1 is done reading x_in[nb_]
-                        x_in[nb_].copy_(x_host[nb_], non_blocking=True)
+                            cs.wait_event(ev_comp[nb_])  # step i-1 is done reading dev_in[nb_]
+                        upload(nb_)
                         ev_up[nb_].record(cs)
                     cs.wait_event(ev_comp[b])
-                    y_host[b].copy_(y_out[b], non_blocking=True)
+                    for h_, d_ in zip(host_out[b], dev_out[b]):
+                        h_.copy_(d_, non_blocking=True)
                     ev_down[b].record(cs)
 
         pipeline(3)
@@ -728,12 +861,15 @@ def run_ours(args, w):
         torch.cuda.synchronize()
         ems = t0.elapsed_time(t1) / K2
         ems = max_over_ranks(ems, world, dev)
-        esz = 2 if w.dtype == "bf16" else 4
+        nbytes = lambda ts: sum(t.numel() * t.element_size() for t in ts)
         e2e = {"value": job_tokens_per_s(world, T, ems), "unit": "tokens/s",
-               "h2d_bytes_per_step": T * h * esz, "d2h_bytes_per_step": T * h * esz,
+               "h2d_bytes_per_step": nbytes(srcs), "d2h_bytes_per_step": nbytes(dsts),
                "ms_per_step": ems,
-               "how": "moe_layer_fwd per step; tokens copied in from pinned host memory and the "
-                      "output copied back every step, on a copy stream overlapped with compute"}
+               "how": ("moe_layer_fwd + moe_layer_bwd per step; x and dy copied in from pinned "
+                       "host memory and dx copied back every step" if train else
+                       "moe_layer_fwd per step; tokens copied in from pinned host memory and the "
+                       "output copied back every step") +
+                      ", on a copy stream overlapped with compute"}
 
     mx = None
     if (not train and not args.no_mxfp8 and w.dtype == "bf16" and w.act == 1
@@ -770,6 +906,31 @@ def run_ours(args, w):
         line["layer_pct_bf16_peak"] = 100.0 * line["layer_tflops"] / peak_tf
         line["forward_tflops"] = fwd_fl / (stage_ms["forward"] / 1000.0) / 1e12
         line["backward_tflops"] = 2 * fwd_fl / (stage_ms["backward"] / 1000.0) / 1e12
+        line["stages_ms"] = {"forward": stage_ms["forward"], "backward": stage_ms["backward"],
+                             **{f"fwd_{k}": v for k, v in sub_ms["forward"].items()},
+                             **{f"bwd_{k}": v for k, v in sub_ms["backward"].items()}}
+        # every routed-expert GEMM timed alone inside the timed steps (events the
+        # library records at the stage boundaries, on the launching stream)
+        work = expert_gemm_work(w)
+        times = {"fc1": sub_ms["forward"]["fc1"], "fc2": sub_ms["forward"]["fc2"],
+                 **{k: sub_ms["backward"][k] for k in
+                    ("fc2_dgrad", "fc2_wgrad", "fc1_dgrad", "fc1_wgrad")}}
+        kern = {k: kernel_roofline(GEMM_KERNELS[k], work[k][0], work[k][1], times[k], pk,
+                                   pk_kind, peak_tf) for k in work}
+        for k, r in kern.items():
+            r["traffic"] = traffic_record(w, k)
+        top = max(kern, key=lambda k: kern[k]["ms_per_launch"])
+        line["roofline"] = dict(kern[top], stage=top)
+        line["expert_gemms"] = kern
+        line["expert_gemms_how"] = (
+            "bytes: every operand read once and every result written once (weights, permuted "
+            "activations, saved pre-activations, weight gradients); bound hbm when FLOP/byte is "
+            "below the ridge point of the measured peaks; the weight-gradient kernels only write "
+            "to HBM what they produce, so `python bench.py --hbm-write`'s write-only rate is "
+            "their practical ceiling")
+        w_bytes = 2 * (w.E + w.n_shared) * (w.w1_rows * h + h * F)
+        line["forward_weight_stream_frac"] = (w_bytes / (stage_ms["forward"] / 1000.0) / 1e9
+                                              / pk["hbm_gbs"])
     else:
         fc1_flops = 2.0 * P * h * w.w1_rows
         fc2_flops = 2.0 * P * F * h
@@ -830,25 +991,30 @@ def run_ours(args, w):
     if not args.no_cpu_baseline:
         S = args.sample_tokens or auto_sample(w)
         samp = OracleSample(w, S)
+        run = samp.run_train if train else samp.run
         t0 = time.perf_counter()
         reps = 0
         ref = None
         while True:
-            ref = samp.run()
+            ref = run()
             reps += 1
             if time.perf_counter() - t0 > 10.0 or reps >= 50:
                 break
         el = time.perf_counter() - t0
         n = len(samp.tokens)
+        what = "forward + backward" if train else "forward"
         line["cpu_baseline"] = {
             "value": reps * n / el, "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
             "sample": f"{n} tokens of the timed workload routed only to experts {samp.experts}, "
-                      f"float64 oracle repeated {reps}x ({el:.1f} s)"}
-        # correctness column: the same tokens from the GPU output of the last step
-        gpu_rows = y[torch.from_numpy(samp.tokens).to(dev)].float().cpu().numpy().astype(np.float64)
+                      f"float64 oracle {what} repeated {reps}x ({el:.1f} s)"}
+        # correctness column: the same tokens from the GPU result of the last
+        # step (y for the forward, dx for the training step)
+        out = dx if train else y
+        gpu_rows = out[torch.from_numpy(samp.tokens).to(dev)].float().cpu().numpy().astype(np.float64)
         err = float(np.abs(gpu_rows - ref).max())
         bound = 2e-2 * float(np.abs(ref).max()) + 1e-3
-        line["check"] = {"tokens": n, "max_abs_err": err, "bound": bound, "ok": err <= bound}
+        line["check"] = {"tokens": n, "tensor": "dx" if train else "y", "max_abs_err": err,
+                         "bound": bound, "ok": err <= bound}
     print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()

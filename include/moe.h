@@ -406,6 +406,27 @@ const char* moe_status_string(moe_status_t status);
 /* Library version, "major.minor.patch". */
 const char* moe_version(void);
 
+/* Stage timing for profilers and benchmarks (a measurement aid, not part of
+ * the method; the pages' counterpart is the per-stage time breakdown of the
+ * review page, §1.3 and §8).  Registers, for the calling host thread, up to
+ * 16 CUDA events (cudaEvent_t, created by the caller on the device the layer
+ * runs on) that moe_layer_fwd (pass MOE_PASS_FWD) or moe_layer_bwd
+ * (MOE_PASS_BWD) record with cudaEventRecord on their own stream at stage
+ * boundary i, for i < n and events[i] != NULL:
+ *   forward:  0 start, 1 after route, 2 after dispatch, 3 after FC1,
+ *             4 after FC2, 5 after the shared expert, 6 after combine;
+ *   backward: 0 start, 1 after the dy scatter, 2 after the FC2 data gradient,
+ *             3 after dW2, 4 after the FC1 data gradient, 5 after dW1,
+ *             6 after the shared expert, 7 after the router, 8 after combine.
+ * So the time between events 4 and 5 of the backward is the dW1 grouped GEMM
+ * alone, on the stream that launched it.  n = 0 clears the pass.  The events
+ * stay registered until replaced; a failed record returns MOE_ERR_CUDA from
+ * the layer call.  Only the layer calls record; other entry points ignore the
+ * registration.  Errors: MOE_ERR_INVALID_ARG for an unknown pass, n outside
+ * [0, 16], or events NULL with n > 0. */
+typedef enum { MOE_PASS_FWD = 0, MOE_PASS_BWD = 1 } moe_pass_t;
+moe_status_t moe_set_stage_events(int32_t pass, void* const* events, int32_t n);
+
 /* Test hook for the bounded-wait machinery: launches one block that waits on
  * an mbarrier nothing will ever complete, with the same bounded wait the
  * tensor-core GEMM uses, capped at `max_polls` polls.  The kernel gives up,

@@ -82,6 +82,23 @@ std::mutex g_dev_mu;
 // their first CUDA runtime call had failed.
 std::atomic<int> g_inject_failures{0};
 
+// Stage timing (moe_set_stage_events): per host thread and pass, the caller's
+// CUDA events that the layer calls record at their stage boundaries.
+constexpr int kMaxStageEvents = 16;
+struct StageEvents {
+  cudaEvent_t ev[kMaxStageEvents] = {};
+  int n = 0;
+};
+thread_local StageEvents g_stage_events[2];
+
+// Records boundary i of pass p (MOE_PASS_FWD / MOE_PASS_BWD) on stream s when
+// the calling thread registered an event for it; otherwise does nothing.
+cudaError_t mark_stage(int pass, int i, cudaStream_t s) {
+  const StageEvents& se = g_stage_events[pass];
+  if (i >= se.n || !se.ev[i]) return cudaSuccess;
+  return cudaEventRecord(se.ev[i], s);
+}
+
 // NVTX ranges around the steps of a layer pass (host-side annotations: a
 // profiler attributes each step's launches to its range; no cost otherwise).
 class NvtxStage {
@@ -223,23 +240,31 @@ cudaError_t run_mlp_bwd(const moe_config_t& c, int rows, int E, const void* dy_r
                         const void* x_rows, const void* H, const void* a, const int32_t* offsets,
                         const float* prob, const void* w1, const void* w2, void* dH,
                         float* dprob_part, void* dx_rows, void* dw1, void* dw2,
-                        const DeviceInfo* d, cudaStream_t s) {
+                        const DeviceInfo* d, cudaStream_t s, int mark = -1) {
   const int F = c.F, h = c.h;
   if (rows == 0) {  // no rows: every weight gradient is zero
     cudaError_t e = cudaMemsetAsync(dw1, 0, (size_t)E * 2 * F * h * 2, s);
     if (e == cudaSuccess) e = cudaMemsetAsync(dw2, 0, (size_t)E * h * F * 2, s);
     return e;
   }
+  // mark: the first of four stage boundaries to record after the four GEMMs
+  // (FC2 dgrad, FC2 wgrad, FC1 dgrad, FC1 wgrad), or -1 for none
+  auto after = [&](cudaError_t e, int k) {
+    return (e == cudaSuccess && mark >= 0) ? mark_stage(MOE_PASS_BWD, mark + k, s) : e;
+  };
   cudaError_t e = launch_tc_dgrad(true, rows, dy_rows, h, w2, E, F, offsets, prob, H, dH,
                                   dprob_part, d->sms, d->status, s);
+  e = after(e, 0);
   if (e == cudaSuccess)
     e = launch_tc_wgrad(rows, dy_rows, h, a, F, E, offsets, dw2, d->sms, d->status, s);
+  e = after(e, 1);
   if (e == cudaSuccess)
     e = launch_tc_dgrad(false, rows, dH, 2 * F, w1, E, h, offsets, nullptr, nullptr, dx_rows,
                         nullptr, d->sms, d->status, s);
+  e = after(e, 2);
   if (e == cudaSuccess)
     e = launch_tc_wgrad(rows, dH, 2 * F, x_rows, h, E, offsets, dw1, d->sms, d->status, s);
-  return e;
+  return after(e, 3);
 }
 
 }  // namespace
@@ -548,7 +573,9 @@ moe_status_t moe_layer_fwd(const moe_config_t* cfg, const void* x, const float* 
   float* perm_prob = at<float>(ws, w.perm_prob);
   // Route
   NvtxStage stage("moe_layer_fwd/route");
-  cudaError_t e = launch_router(c, x, w_r, gate_bias, sel_bias, at<float>(ws, w.logits), idx,
+  cudaError_t e = mark_stage(MOE_PASS_FWD, 0, s);
+  if (e == cudaSuccess)
+    e = launch_router(c, x, w_r, gate_bias, sel_bias, at<float>(ws, w.logits), idx,
                                 prob, nullptr, router_scratch(c, ws), d->sms, d->status, s);
   if (e == cudaSuccess && (c.aux_loss_coeff != 0.f || c.z_loss_coeff != 0.f))
     e = launch_aux_loss(c, at<float>(ws, w.logits), idx, 0.f, 0.f, at<float>(ws, w.aux_losses),
@@ -559,6 +586,7 @@ moe_status_t moe_layer_fwd(const moe_config_t* cfg, const void* x, const float* 
   // each row block once per N tile, and a gathered re-read costs the TMA
   // engine far more than a tiled one: the one-pass scatter is faster.)
   stage.next("moe_layer_fwd/dispatch");
+  if (e == cudaSuccess) e = mark_stage(MOE_PASS_FWD, 1, s);
   if (e == cudaSuccess)
     e = launch_permute_maps(c, idx, prob, at<int32_t>(ws, w.hist), at<int32_t>(ws, w.chunk_base),
                             at<int32_t>(ws, w.counts), offsets, dst_row,
@@ -567,10 +595,15 @@ moe_status_t moe_layer_fwd(const moe_config_t* cfg, const void* x, const float* 
     e = launch_scatter_rows(c, x, dst_row, at<void>(ws, w.x_perm), d->sms, d->status, s, true);
   // Expert computation
   stage.next("moe_layer_fwd/experts");
+  if (e == cudaSuccess) e = mark_stage(MOE_PASS_FWD, 2, s);
   if (e == cudaSuccess)
-    e = run_grouped_mlp(c, c.T * c.K, at<void>(ws, w.x_perm), offsets, perm_prob, w1, b1, w2, b2,
-                        save ? at<void>(ws, w.act_save) : nullptr, at<void>(ws, w.a),
+    e = run_expert_gemm(c, 1, c.T * c.K, at<void>(ws, w.x_perm), offsets, perm_prob, w1, b1,
+                        save ? at<void>(ws, w.act_save) : nullptr, at<void>(ws, w.a), d, s);
+  if (e == cudaSuccess) e = mark_stage(MOE_PASS_FWD, 3, s);
+  if (e == cudaSuccess)
+    e = run_expert_gemm(c, 2, c.T * c.K, at<void>(ws, w.a), offsets, perm_prob, w2, b2, nullptr,
                         at<void>(ws, w.y_perm), d, s);
+  if (e == cudaSuccess) e = mark_stage(MOE_PASS_FWD, 4, s);
   const void* shared_y = nullptr;
   if (e == cudaSuccess && c.n_shared) {
     moe_config_t cs = c;  // one always-on expert over all T tokens, weight 1
@@ -588,9 +621,11 @@ moe_status_t moe_layer_fwd(const moe_config_t* cfg, const void* x, const float* 
   }
   // Combine (probabilities were applied inside the expert GEMMs)
   stage.next("moe_layer_fwd/combine");
+  if (e == cudaSuccess) e = mark_stage(MOE_PASS_FWD, 5, s);
   if (e == cudaSuccess)
     e = launch_combine(c, at<void>(ws, w.y_perm), dst_row, nullptr, shared_y, y, d->sms,
                        d->status, s);
+  if (e == cudaSuccess) e = mark_stage(MOE_PASS_FWD, 6, s);
   if (e == cudaSuccess && topk_idx_out)
     e = cudaMemcpyAsync(topk_idx_out, idx, sizeof(int32_t) * c.T * c.K, cudaMemcpyDeviceToDevice, s);
   if (e == cudaSuccess && topk_prob_out)
@@ -738,12 +773,15 @@ moe_status_t moe_layer_bwd(const moe_config_t* cfg, const void* x, const float* 
   float* dl_topk = at<float>(ws, w.dl_topk);
   // dy in expert order, then the routed experts' backward
   NvtxStage stage("moe_layer_bwd/experts");
-  cudaError_t e = launch_scatter_rows(c, dy, dst_row, at<void>(ws, w.dy_perm), d->sms, d->status, s);
+  cudaError_t e = mark_stage(MOE_PASS_BWD, 0, s);
+  if (e == cudaSuccess)
+    e = launch_scatter_rows(c, dy, dst_row, at<void>(ws, w.dy_perm), d->sms, d->status, s);
+  if (e == cudaSuccess) e = mark_stage(MOE_PASS_BWD, 1, s);
   if (e == cudaSuccess)
     e = run_mlp_bwd(c, P, c.E, at<void>(ws, w.dy_perm), at<void>(ws, w.x_perm),
                     at<void>(ws, w.act_save), at<void>(ws, w.a), offsets,
                     at<float>(ws, w.perm_prob), w1, w2, at<void>(ws, w.dh),
-                    at<float>(ws, w.dprob_part), at<void>(ws, w.dx_perm), dw1, dw2, d, s);
+                    at<float>(ws, w.dprob_part), at<void>(ws, w.dx_perm), dw1, dw2, d, s, 2);
   // the shared expert: one group of all T tokens, weight 1
   if (e == cudaSuccess && c.n_shared)
     e = run_mlp_bwd(c, c.T, 1, dy, x, at<void>(ws, w.shared_h), at<void>(ws, w.shared_a),
@@ -752,6 +790,7 @@ moe_status_t moe_layer_bwd(const moe_config_t* cfg, const void* x, const float* 
                     dw2_shared, d, s);
   // Route backward: dprob -> dl -> dW_r, db_r
   stage.next("moe_layer_bwd/router");
+  if (e == cudaSuccess) e = mark_stage(MOE_PASS_BWD, 6, s);
   if (e == cudaSuccess)
     e = launch_dprob_reduce(at<float>(ws, w.dprob_part), P, (c.F + 255) / 256,
                             at<float>(ws, w.dprob_perm), s);
@@ -789,10 +828,12 @@ moe_status_t moe_layer_bwd(const moe_config_t* cfg, const void* x, const float* 
   }
   // dx = routed + shared + router contributions
   stage.next("moe_layer_bwd/combine");
+  if (e == cudaSuccess) e = mark_stage(MOE_PASS_BWD, 7, s);
   if (e == cudaSuccess)
     e = launch_bwd_combine(c, at<void>(ws, w.dx_perm), dst_row,
                            c.n_shared ? at<void>(ws, w.shared_dx) : nullptr, dl_topk, idx, w_r,
                            dx_add, dx, nullptr, d->sms, d->status, s);
+  if (e == cudaSuccess) e = mark_stage(MOE_PASS_BWD, 8, s);
   return cuda_status(e);
 }
 
@@ -826,6 +867,16 @@ const char* moe_status_string(moe_status_t s) {
 }
 
 const char* moe_version(void) { return "0.1.0"; }
+
+moe_status_t moe_set_stage_events(int32_t pass, void* const* events, int32_t n) {
+  if (pass != MOE_PASS_FWD && pass != MOE_PASS_BWD) return MOE_ERR_INVALID_ARG;
+  if (n < 0 || n > kMaxStageEvents || (n > 0 && !events)) return MOE_ERR_INVALID_ARG;
+  StageEvents& se = g_stage_events[pass];
+  for (int i = 0; i < kMaxStageEvents; ++i)
+    se.ev[i] = i < n ? static_cast<cudaEvent_t>(events[i]) : nullptr;
+  se.n = n;
+  return MOE_OK;
+}
 
 int32_t moe_test_inject_cuda_failure(int32_t n) {
   if (n < 0) return -1;

@@ -78,6 +78,8 @@ _SIG = {
     "moe_router_aux_loss": (ctypes.c_int, [_CFG, _P, _P, ctypes.c_float, ctypes.c_float, _P, _P,
                                            _P, ctypes.c_size_t, _P]),
     "moe_get_error": (ctypes.c_int, [_P]),
+    "moe_set_stage_events": (ctypes.c_int, [ctypes.c_int32, ctypes.POINTER(ctypes.c_void_p),
+                                            ctypes.c_int32]),
     "moe_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "moe_version": (ctypes.c_char_p, []),
     "moe_test_bounded_wait": (ctypes.c_int, [ctypes.c_int64, _P]),
@@ -308,6 +310,27 @@ def moe_layer_losses(cfg, losses, ws, stream=None):
 
 def moe_get_error(stream=None) -> int:
     return int(_lib.moe_get_error(_stream(stream)))
+
+
+MOE_PASS_FWD, MOE_PASS_BWD = 0, 1
+
+
+def moe_set_stage_events(pass_, events):
+    """Registers CUDA events that moe_layer_fwd / moe_layer_bwd record at their
+    stage boundaries (moe.h lists them).  `events`: a list of
+    torch.cuda.Event (already recorded once, so that the CUDA event exists),
+    raw cudaEvent_t integers, or None entries; [] clears the pass."""
+    handles = []
+    for ev in events:
+        if ev is None:
+            handles.append(None)
+            continue
+        hnd = int(getattr(ev, "cuda_event", ev))
+        if hnd == 0:
+            raise ValueError("a torch.cuda.Event is created lazily: record it once first")
+        handles.append(hnd)
+    arr = (ctypes.c_void_p * max(len(handles), 1))(*handles)
+    _check("moe_set_stage_events", _lib.moe_set_stage_events(int(pass_), arr, len(handles)))
 
 
 def moe_test_bounded_wait(max_polls, stream=None):

@@ -151,3 +151,13 @@ def test_failure_injection_counter(M):
     assert M.moe_test_inject_cuda_failure(0) == 3   # cleared, the pending count returned
     assert M.moe_test_inject_cuda_failure(-1) == -1
     assert M.moe_test_inject_cuda_failure(0) == 0
+
+
+def test_stage_event_registration_checks(M):
+    f = M.raw("moe_set_stage_events")
+    arr = (ctypes.c_void_p * 17)()
+    assert f(0, arr, 0) == M.MOE_OK and f(1, None, 0) == M.MOE_OK   # clear
+    assert f(2, arr, 1) == M.MOE_ERR_INVALID_ARG                    # unknown pass
+    assert f(0, arr, 17) == M.MOE_ERR_INVALID_ARG                   # more than 16
+    assert f(0, None, 3) == M.MOE_ERR_INVALID_ARG
+    assert f(1, arr, 16) == M.MOE_OK and f(1, arr, 0) == M.MOE_OK   # NULL entries are skipped

@@ -197,3 +197,32 @@ def test_layer_backward_with_load_balancing_losses(w):
         slack = 2.0 ** -23 * float(np.abs(to_np(out[name])).max())
         ok, err, bound = tol_ok(got, want, "f32")
         assert err <= bound + slack, (name, err, bound, slack)
+
+
+def test_stage_events_time_the_layer_stages_without_changing_results():
+    """moe_set_stage_events: the layer calls record the registered events at
+    their stage boundaries, in order, and the results stay bit-identical to
+    a run without them."""
+    M = lib()
+    L = Layer(_bwd_workloads()[0])
+    _, plain = _run_layer_bwd(M, L)
+    fwd = [torch.cuda.Event(enable_timing=True) for _ in range(7)]
+    bwd = [torch.cuda.Event(enable_timing=True) for _ in range(9)]
+    for ev in fwd + bwd:
+        ev.record()
+    torch.cuda.synchronize()
+    M.moe_set_stage_events(M.MOE_PASS_FWD, fwd)
+    M.moe_set_stage_events(M.MOE_PASS_BWD, bwd)
+    try:
+        _, timed = _run_layer_bwd(M, L)
+    finally:
+        M.moe_set_stage_events(M.MOE_PASS_FWD, [])
+        M.moe_set_stage_events(M.MOE_PASS_BWD, [])
+    for k in plain:
+        assert torch.equal(_bits(plain[k]), _bits(timed[k])), k
+    for evs in (fwd, bwd):
+        gaps = [a.elapsed_time(b) for a, b in zip(evs[:-1], evs[1:])]
+        assert all(g >= 0.0 for g in gaps), gaps        # recorded in boundary order
+        total = evs[0].elapsed_time(evs[-1])
+        assert abs(sum(gaps) - total) <= 1e-3 + 1e-3 * total
+    assert bwd[4].elapsed_time(bwd[5]) > 0.0             # the dW1 GEMM ran between 4 and 5
