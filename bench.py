@@ -241,11 +241,21 @@ class OracleSample:
             self.sub_w2 = np.stack([self.w2[e] for e in need])
 
     def run(self):
-        from oracle import moe_oracle as O
+        """The sampled tokens' layer output by the plain C++ oracle (double
+        loops, OpenMP over tokens), from the routing decided for every token."""
+        from oracle import moe_oracle_c as C
         w = self.w
-        return O.layer_fwd(self.x, self.w_r, self.w1, self.w2, w.K, w.score, w.act, b1=self.b1,
-                           b2=self.b2, w1_shared=self.w1s, w2_shared=self.w2s,
-                           tokens=self.tokens, routing=self.routing)["y"]
+        _, idx, probs = self.routing
+        return C.layer_fwd(self.x, idx, probs, self.w1, self.w2, w.act, b1=self.b1, b2=self.b2,
+                           w1_shared=self.w1s, w2_shared=self.w2s, tokens=self.tokens)
+
+    def cores(self):
+        from oracle import moe_oracle_c as C
+        return (blas_threads() if self.w.backward else C.threads()) or 1
+
+    def kind(self):
+        return ("float64 numpy oracle forward + backward" if self.w.backward else
+                "plain C++ oracle (double loops, OpenMP over tokens) forward")
 
     def run_train(self):
         """Forward then backward of the sampled tokens; returns their dx."""
@@ -293,9 +303,9 @@ def run_reference(args, w):
     n = len(samp.tokens)
     ms = 1000.0 * statistics.mean(times)
     value = n / (ms / 1000.0)
-    cores = blas_threads()
-    sample = (f"{n} tokens of {w.name} routed only to experts {samp.experts}; float64 numpy "
-              f"oracle ({'forward + backward' if w.backward else 'forward'}), one sample per step")
+    cores = samp.cores()
+    sample = (f"{n} tokens of {w.name} routed only to experts {samp.experts}; {samp.kind()}, "
+              f"one sample per step")
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
@@ -1002,11 +1012,10 @@ def run_ours(args, w):
                 break
         el = time.perf_counter() - t0
         n = len(samp.tokens)
-        what = "forward + backward" if train else "forward"
         line["cpu_baseline"] = {
-            "value": reps * n / el, "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
+            "value": reps * n / el, "unit": "tokens/s", "cores": samp.cores(), "kind": "oracle",
             "sample": f"{n} tokens of the timed workload routed only to experts {samp.experts}, "
-                      f"float64 oracle {what} repeated {reps}x ({el:.1f} s)"}
+                      f"{samp.kind()} repeated {reps}x ({el:.1f} s)"}
         # correctness column: the same tokens from the GPU result of the last
         # step (y for the forward, dx for the training step)
         out = dx if train else y
