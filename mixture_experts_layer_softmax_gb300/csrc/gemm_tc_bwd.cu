@@ -133,45 +133,71 @@ MOE_D void load8(const __nv_bfloat16* src, float* v) {
 // slots (row `lane`, 16-B chunk c at c ^ (lane & 7)) -> one TMA store (rows
 // past M are clipped).  A slot is refilled once the store issued from it two
 // boxes earlier has read it, so the other slot's store stays in flight.  The
-// accumulator is released (tmem_empty) right after its last read.  have_rows
-// false: the expert has no rows and the tile is zeros.
-MOE_D void wgrad_store_tile(uint32_t tbase, bool have_rows, int e, int mb, int nb, int q,
-                            int lane, uint8_t* staging, const CUtensorMap* tmC,
-                            uint32_t tmem_empty_bar) {
-  uint8_t* slots = staging + q * 2 * 4096;
-#pragma unroll 1
-  for (int j = 0; j < BN / 64; ++j) {
-    uint8_t* box = slots + (j & 1) * 4096;
-    uint32_t r[64];
+// TMEM load of the next 64 columns is issued before this box is converted and
+// stored (two register buffers), so its latency overlaps the store path
+// instead of adding to it.  The accumulator is released (tmem_empty) once its
+// last load has completed.  have_rows false: the expert has no rows and the
+// tile is zeros.
+MOE_D void wgrad_box(const uint32_t (&r)[64], bool have_rows, uint8_t* box, int lane) {
+  if (lane == 0) bulk_wait_read1();  // the store from this slot (two boxes back) has read it
+  __syncwarp();
+#pragma unroll
+  for (int g = 0; g < 8; ++g) {
+    uint4 u = make_uint4(0u, 0u, 0u, 0u);
     if (have_rows) {
-      tc::tmem_ld_32x32b_x64(tbase + j * 64, r);
-    } else {
-#pragma unroll
-      for (int i = 0; i < 64; ++i) r[i] = 0u;
-    }
-    if (j == BN / 64 - 1) {  // every TMEM read of this tile is done: release it
-      tc::fence_before_sync();
-      __syncwarp();
-      if (lane == 0) tc::mbar_arrive(tmem_empty_bar);
-    }
-    if (lane == 0) bulk_wait_read1();  // the store from this slot (box j - 2) has read it
-    __syncwarp();
-#pragma unroll
-    for (int g = 0; g < 8; ++g) {
-      uint4 u;
       u.x = pack2(__uint_as_float(r[g * 8 + 0]), __uint_as_float(r[g * 8 + 1]));
       u.y = pack2(__uint_as_float(r[g * 8 + 2]), __uint_as_float(r[g * 8 + 3]));
       u.z = pack2(__uint_as_float(r[g * 8 + 4]), __uint_as_float(r[g * 8 + 5]));
       u.w = pack2(__uint_as_float(r[g * 8 + 6]), __uint_as_float(r[g * 8 + 7]));
-      *reinterpret_cast<uint4*>(box + lane * 128 + ((g ^ (lane & 7)) << 4)) = u;
     }
-    tc::fence_proxy_async_smem();
-    __syncwarp();
+    *reinterpret_cast<uint4*>(box + lane * 128 + ((g ^ (lane & 7)) << 4)) = u;
+  }
+  tc::fence_proxy_async_smem();
+  __syncwarp();
+}
+
+MOE_D void wgrad_store_tile(uint32_t tbase, bool have_rows, int e, int mb, int nb, int q,
+                            int lane, uint8_t* staging, const CUtensorMap* tmC,
+                            uint32_t tmem_empty_bar) {
+  static_assert(BN == 256, "four 64-column boxes per tile");
+  uint8_t* slots = staging + q * 2 * 4096;
+  uint32_t ra[64], rb[64];
+  if (have_rows) {
+    tc::tmem_ld_32x32b_x64_nowait(tbase, ra);
+    tc::tmem_ld_wait_x64(ra);
+  }
+  auto store = [&](int j) {
     if (lane == 0) {
-      tma_store_3d(tmC, nb * BN + j * 64, mb * BM + q * 32, e, tc::smem_u32(box));
+      tma_store_3d(tmC, nb * BN + j * 64, mb * BM + q * 32, e, tc::smem_u32(slots + (j & 1) * 4096));
       bulk_commit();
     }
+  };
+  auto release = [&]() {  // every TMEM load of this tile has completed
+    tc::fence_before_sync();
+    __syncwarp();
+    if (lane == 0) tc::mbar_arrive(tmem_empty_bar);
+  };
+  // box 0 from ra while box 1 loads into rb; box 1 from rb while box 2 loads
+  // into ra; box 2 from ra while box 3 loads into rb; box 3 from rb
+  if (have_rows) tc::tmem_ld_32x32b_x64_nowait(tbase + 64, rb);
+  wgrad_box(ra, have_rows, slots, lane);
+  store(0);
+  if (have_rows) {
+    tc::tmem_ld_wait_x64(rb);
+    tc::tmem_ld_32x32b_x64_nowait(tbase + 128, ra);
   }
+  wgrad_box(rb, have_rows, slots + 4096, lane);
+  store(1);
+  if (have_rows) {
+    tc::tmem_ld_wait_x64(ra);
+    tc::tmem_ld_32x32b_x64_nowait(tbase + 192, rb);
+  }
+  wgrad_box(ra, have_rows, slots, lane);
+  store(2);
+  if (have_rows) tc::tmem_ld_wait_x64(rb);
+  release();
+  wgrad_box(rb, have_rows, slots + 4096, lane);
+  store(3);
 }
 
 template <int KIND>

@@ -342,6 +342,38 @@ MOE_D void tmem_ld_32x32b_x64(uint32_t taddr, uint32_t (&r)[64]) {
 }
 MOE_D void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
+// The same 32 lanes x 64 columns without the wait, so the load overlaps other
+// work; the registers may only be read after tmem_ld_wait_x64 on them.
+MOE_D void tmem_ld_32x32b_x64_nowait(uint32_t taddr, uint32_t (&r)[64]) {
+#define MOE_R8(i) "=r"(r[i]), "=r"(r[i + 1]), "=r"(r[i + 2]), "=r"(r[i + 3]), "=r"(r[i + 4]), \
+                  "=r"(r[i + 5]), "=r"(r[i + 6]), "=r"(r[i + 7])
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%64];\n\t"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,"
+      "%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%65];"
+      : MOE_R8(0), MOE_R8(8), MOE_R8(16), MOE_R8(24), MOE_R8(32), MOE_R8(40), MOE_R8(48),
+        MOE_R8(56)
+      : "r"(taddr), "r"(taddr + 32)
+      : "memory");
+#undef MOE_R8
+}
+// Waits for this thread's TMEM loads.  The 64 destination registers are
+// operands (read and written), so no use of them can be scheduled before the
+// wait.
+MOE_D void tmem_ld_wait_x64(uint32_t (&r)[64]) {
+#define MOE_W8(i) "+r"(r[i]), "+r"(r[i + 1]), "+r"(r[i + 2]), "+r"(r[i + 3]), "+r"(r[i + 4]), \
+                  "+r"(r[i + 5]), "+r"(r[i + 6]), "+r"(r[i + 7])
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : MOE_W8(0), MOE_W8(8), MOE_W8(16), MOE_W8(24), MOE_W8(32), MOE_W8(40),
+                 MOE_W8(48), MOE_W8(56)
+               :
+               : "memory");
+#undef MOE_W8
+}
+
 // ---- host: the driver's tensor-map encoder ------------------------------------
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
