@@ -556,7 +556,9 @@ def run_ours(args, w):
     gate_bias = torch.from_numpy(gb).to(dev) if gb is not None else None
 
     tiling = {"auto": 0, "1cta": M.MOE_FLAG_GEMM_1CTA, "2cta": M.MOE_FLAG_GEMM_2CTA}[args.tiling]
-    cfg = M.config_for(w, tiling)
+    # the router hands the dispatch its per-chunk expert histograms (as
+    # moe_layer_fwd does internally)
+    cfg = M.config_for(w, tiling | M.MOE_FLAG_HIST_FROM_ROUTER)
     ws = torch.empty(M.moe_workspace_size(cfg), dtype=torch.uint8, device=dev)
     i32 = dict(dtype=torch.int32, device=dev)
     idx = torch.empty(T, K, **i32)
@@ -642,13 +644,16 @@ def run_ours(args, w):
     # E <= 32, else GEMM and selection), dispatch (maps, row scatter), FC1 and
     # FC2, the shared expert's two GEMMs (+ its offsets in moe_layer_fwd),
     # combine
+    # The router also hands the dispatch its per-chunk expert histograms: the
+    # one-launch router (bf16, E <= 8) from its epilogue, the other paths by
+    # the histogram step launched right after them.
     if w.dtype == "bf16":
-        route_k = 1 if E <= 8 else 3
+        route_k = 1 if E <= 8 else 3 + 1
     else:
-        route_k = 1 if E <= 32 else 2
-    # dispatch: histogram, per-expert scan (folded into the ranks kernel when
+        route_k = (1 if E <= 32 else 2) + 1
+    # dispatch: per-expert scan (folded into the ranks kernel when
     # ceil(T/32) * E <= 8192), ranks, and the row scatter unless FC1 gathers
-    maps_k = 2 if ((T + 31) // 32) * E <= 8192 else 3
+    maps_k = 1 if ((T + 31) // 32) * E <= 8192 else 2
     dispatch_k = maps_k + (0 if (gather and not train) else 1)
     launches_per_step = route_k + dispatch_k + 2 + ((3 if train else 2) if w.n_shared else 0) + 1
     if train:  # backward: scatter, 4 GEMMs (+4 shared), dprob, router, router wgrad, combine
@@ -1030,34 +1035,37 @@ def run_ours(args, w):
 
 
 def hbm_write_probe():
-    """Write-only bandwidth (a fill, no reads) beside the copy bandwidth the
-    roofline peaks use: the expert weight gradients write dW and read little,
-    so the fill rate is their roofline."""
+    """Write-only bandwidth (writes, no reads) beside the copy bandwidth the
+    roofline peaks use: the expert weight gradients write dW and read little.
+    Writes are timed as zero_() (a memset) and as fill_() of an int64 view
+    (8-byte stores); a uint8 fill_ is not bandwidth-bound (about half of
+    either) and is reported only for comparison."""
     import torch
     dev = torch.device("cuda")
     n = 16 << 30
     buf = torch.empty(n, dtype=torch.uint8, device=dev)
     src = torch.empty(n // 2, dtype=torch.uint8, device=dev)
     dst = torch.empty(n // 2, dtype=torch.uint8, device=dev)
-    for _ in range(3):
-        buf.fill_(1)
-        dst.copy_(src)
+    ops = {"zero_": lambda: buf.zero_(), "fill_int64": lambda: buf.view(torch.int64).fill_(1),
+           "fill_uint8": lambda: buf.fill_(1), "copy": lambda: dst.copy_(src)}
+    for f in ops.values():
+        f()
     torch.cuda.synchronize()
-    tw, tc = [], []
-    for _ in range(10):
-        a, b, c = (torch.cuda.Event(enable_timing=True) for _ in range(3))
-        a.record()
-        buf.fill_(1)
-        b.record()
-        dst.copy_(src)
-        c.record()
-        torch.cuda.synchronize()
-        tw.append(a.elapsed_time(b))
-        tc.append(b.elapsed_time(c))
-    print(json.dumps({"write_only_gbs": n / (min(tw) / 1000) / 1e9,
-                      "copy_gbs": n / (min(tc) / 1000) / 1e9,
-                      "how": "torch fill_ of 16 GiB (writes only) and copy_ of 8 GiB (8 GiB read + "
-                             "8 GiB written), best of 10, CUDA events"}), flush=True)
+    best = {}
+    for name, f in ops.items():
+        ts = []
+        for _ in range(10):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            f()
+            b.record()
+            torch.cuda.synchronize()
+            ts.append(a.elapsed_time(b))
+        best[name] = n / (min(ts) / 1000) / 1e9
+    print(json.dumps({"write_only_gbs": max(best["zero_"], best["fill_int64"]),
+                      "copy_gbs": best["copy"], "by_op_gbs": best,
+                      "how": "16 GiB written by zero_ / an int64 fill_ (writes only), 8 GiB copied "
+                             "(8 GiB read + 8 GiB written), best of 10, CUDA events"}), flush=True)
 
 
 def main():
