@@ -746,6 +746,7 @@ def run_ours(args, w):
                   for _ in range(args.steps)]
             for i in range(args.steps):
                 flush_buf.fill_(1)
+                hold()  # as in the eager timing: the flush's write-backs drain first
                 ev[i][0].record(stream)
                 g.replay()
                 ev[i][1].record(stream)
@@ -789,6 +790,7 @@ def run_ours(args, w):
             torch.cuda.synchronize()
             for i in range(args.steps):
                 flush_buf.fill_(1)
+                hold()
                 gev[i][0].record(stream)
                 g.replay()
                 gev[i][1].record(stream)
@@ -985,7 +987,8 @@ def run_ours(args, w):
                 "permute_ms": permute_graph_ms,
                 "permute_pct_hbm": 100.0 * perm_bytes / (permute_graph_ms / 1000.0) / 1e9 / pk["hbm_gbs"],
                 "how": "moe_router_topk and moe_permute each captured alone in a CUDA graph, "
-                       "replayed with the L2 flushed before every replay"}
+                       "replayed with the L2 flushed (and its write-backs drained behind a "
+                       "GPU-side sleep) before every replay"}
         if mx is not None:
             # FP8 tensor peak: the measured bf16 burst x the nominal fp8/bf16 ratio (4.5 / 2.25)
             fp8_peak = 2.0 * peak_tf

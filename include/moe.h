@@ -80,7 +80,19 @@ enum {
    * tcgen05 cta_group::2) when experts average >= 512 rows, single CTAs
    * (128-row tiles) otherwise.  These force one or the other. */
   MOE_FLAG_GEMM_1CTA = 64u,
-  MOE_FLAG_GEMM_2CTA = 128u
+  MOE_FLAG_GEMM_2CTA = 128u,
+  /* Route -> Dispatch hand-off (review §4.3.1, permutation fusion):
+   * moe_router_topk also leaves the per-chunk expert histograms of the
+   * topk_idx it writes (tokens in chunks of 32: the first step of the
+   * dispatch maps) in the workspace, computed by the router's own epilogue
+   * where it can (bf16, E <= 8) and by one extra step otherwise; moe_permute
+   * and moe_permute_mxfp8 given the same flag, the same workspace and that
+   * unmodified topk_idx start from them instead of counting again.  The
+   * caller promises the hand-off: a histogram that does not match topk_idx
+   * gives wrong maps (out-of-range rows are never written: they are reported
+   * as MOE_ERR_DEVICE_BOUNDS).  moe_layer_fwd does this internally.
+   * moe_permute_noalloc ignores the flag (it has no workspace). */
+  MOE_FLAG_HIST_FROM_ROUTER = 256u
 };
 
 typedef struct {

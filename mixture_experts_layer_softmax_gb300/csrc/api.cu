@@ -12,12 +12,12 @@
 namespace moe {
 cudaError_t launch_router(const moe_config_t&, const void*, const float*, const float*,
                           const float*, float*, int32_t*, float*, uint8_t*, const RouterScratch&,
-                          int, int*, cudaStream_t);
+                          int, int*, cudaStream_t, int32_t* hist = nullptr);
 cudaError_t launch_router_select(const moe_config_t&, const float*, const float*, int32_t*,
                                  float*, uint8_t*, cudaStream_t);
 cudaError_t launch_permute_maps(const moe_config_t&, const int32_t*, const float*, int32_t*,
                                 int32_t*, int32_t*, int32_t*, int32_t*, int32_t*, float*, int*,
-                                cudaStream_t);
+                                cudaStream_t, bool hist_ready = false);
 cudaError_t launch_scatter_rows(const moe_config_t&, const void*, const int32_t*, void*, int,
                                 int*, cudaStream_t, bool after_maps = false);
 cudaError_t launch_combine(const moe_config_t&, const void*, const int32_t*, const float*,
@@ -151,7 +151,7 @@ moe_status_t check_config(const moe_config_t* c) {
     return MOE_ERR_INVALID_ARG;
   const uint32_t known = MOE_FLAG_RENORM | MOE_FLAG_FORCE_BALANCE | MOE_FLAG_VALIDATE_ONLY |
                          MOE_FLAG_SAVE_FOR_BWD | MOE_FLAG_GEMM_SIMT | MOE_FLAG_GEMM_1CTA |
-                         MOE_FLAG_GEMM_2CTA;
+                         MOE_FLAG_GEMM_2CTA | MOE_FLAG_HIST_FROM_ROUTER;
   if (c->flags & ~known) return MOE_ERR_INVALID_ARG;
   if ((c->flags & MOE_FLAG_GEMM_1CTA) && (c->flags & MOE_FLAG_GEMM_2CTA)) return MOE_ERR_INVALID_ARG;
   if (!std::isfinite(c->aux_loss_coeff) || !std::isfinite(c->z_loss_coeff))
@@ -305,7 +305,8 @@ moe_status_t moe_router_topk(const moe_config_t* cfg, const void* x, const float
   if (!al16(x) || !al16(w_r)) return MOE_ERR_INVALID_ARG;
   // bf16 tokens: the tensor-core router keeps its split weight and partial
   // sums in the workspace; fp32 tokens need it only for E > 32 without logits
-  const bool need_ws = cfg->dtype == MOE_BF16 || (!logits && cfg->E > 32);
+  const bool want_hist = (cfg->flags & MOE_FLAG_HIST_FROM_ROUTER) != 0;
+  const bool need_ws = cfg->dtype == MOE_BF16 || (!logits && cfg->E > 32) || want_hist;
   if (need_ws && (st = check_ws(cfg, ws, ws_bytes)) != MOE_OK) return st;
   if (cfg->flags & MOE_FLAG_VALIDATE_ONLY) return MOE_OK;
   if (cfg->T == 0) return MOE_OK;
@@ -315,9 +316,10 @@ moe_status_t moe_router_topk(const moe_config_t* cfg, const void* x, const float
   if (!lg && cfg->E > 32 && cfg->dtype != MOE_BF16) lg = at<float>(ws, workspace_layout(*cfg).logits);
   RouterScratch rs{};
   if (need_ws) rs = router_scratch(*cfg, ws);
+  int32_t* hist = want_hist ? at<int32_t>(ws, workspace_layout(*cfg).hist) : nullptr;
   return cuda_status(launch_router(*cfg, x, w_r, gate_bias, sel_bias, lg, topk_idx, topk_prob,
                                    routing_map, rs, d->sms, d->status,
-                                   static_cast<cudaStream_t>(stream)));
+                                   static_cast<cudaStream_t>(stream), hist));
 }
 
 moe_status_t moe_router_topk_from_logits(const moe_config_t* cfg, const float* logits,
@@ -351,7 +353,8 @@ moe_status_t moe_permute(const moe_config_t* cfg, const void* x, const int32_t* 
   const Workspace w = workspace_layout(*cfg);
   cudaError_t e = launch_permute_maps(*cfg, topk_idx, topk_prob, at<int32_t>(ws, w.hist),
                                       at<int32_t>(ws, w.chunk_base), counts, offsets, dst_row,
-                                      src_token, perm_prob, d->status, s);
+                                      src_token, perm_prob, d->status, s,
+                                      (cfg->flags & MOE_FLAG_HIST_FROM_ROUTER) != 0);
   if (e == cudaSuccess && x)
     e = launch_scatter_rows(*cfg, x, dst_row, x_perm, d->sms, d->status, s, true);
   return cuda_status(e);
@@ -469,7 +472,8 @@ moe_status_t moe_permute_mxfp8(const moe_config_t* cfg, const void* x, const int
   const Workspace w = workspace_layout(*cfg);
   cudaError_t e = launch_permute_maps(*cfg, topk_idx, topk_prob, at<int32_t>(ws, w.hist),
                                       at<int32_t>(ws, w.chunk_base), counts, offsets, dst_row,
-                                      src_token, perm_prob, d->status, s);
+                                      src_token, perm_prob, d->status, s,
+                                      (cfg->flags & MOE_FLAG_HIST_FROM_ROUTER) != 0);
   if (e == cudaSuccess)
     e = launch_scatter_quantize(*cfg, x, topk_idx, dst_row, offsets, x_q, x_sf, d->sms,
                                 d->status, s);
@@ -576,7 +580,8 @@ moe_status_t moe_layer_fwd(const moe_config_t* cfg, const void* x, const float* 
   cudaError_t e = mark_stage(MOE_PASS_FWD, 0, s);
   if (e == cudaSuccess)
     e = launch_router(c, x, w_r, gate_bias, sel_bias, at<float>(ws, w.logits), idx,
-                                prob, nullptr, router_scratch(c, ws), d->sms, d->status, s);
+                      prob, nullptr, router_scratch(c, ws), d->sms, d->status, s,
+                      at<int32_t>(ws, w.hist));  // the dispatch's chunk histograms too
   if (e == cudaSuccess && (c.aux_loss_coeff != 0.f || c.z_loss_coeff != 0.f))
     e = launch_aux_loss(c, at<float>(ws, w.logits), idx, 0.f, 0.f, at<float>(ws, w.aux_losses),
                         nullptr, at<double>(ws, w.aux_part_p), at<double>(ws, w.aux_part_z),
@@ -590,7 +595,8 @@ moe_status_t moe_layer_fwd(const moe_config_t* cfg, const void* x, const float* 
   if (e == cudaSuccess)
     e = launch_permute_maps(c, idx, prob, at<int32_t>(ws, w.hist), at<int32_t>(ws, w.chunk_base),
                             at<int32_t>(ws, w.counts), offsets, dst_row,
-                            at<int32_t>(ws, w.src_token), perm_prob, d->status, s);
+                            at<int32_t>(ws, w.src_token), perm_prob, d->status, s,
+                            /*hist_ready=*/true);
   if (e == cudaSuccess)
     e = launch_scatter_rows(c, x, dst_row, at<void>(ws, w.x_perm), d->sms, d->status, s, true);
   // Expert computation

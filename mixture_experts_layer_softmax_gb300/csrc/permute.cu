@@ -142,7 +142,8 @@ MOE_D void block_offsets(const int32_t* __restrict__ counts, int E, int32_t* s_o
 MOE_D void ranks_chunk(int c, int lane, const int32_t* __restrict__ idx,
                        const float* __restrict__ prob, int T, int K, int E, int cap,
                        const int32_t* base, const int32_t* s_off, int32_t* __restrict__ dst_row,
-                       int32_t* __restrict__ src_token, float* __restrict__ perm_prob) {
+                       int32_t* __restrict__ src_token, float* __restrict__ perm_prob,
+                       int* status) {
   const int64_t t = (int64_t)c * kChunk + lane;
   const bool valid = t < T;
   const unsigned lt_mask = (1u << lane) - 1u;
@@ -179,6 +180,11 @@ MOE_D void ranks_chunk(int c, int lane, const int32_t* __restrict__ idx,
         continue;
       }
       const int r = s_off[e] + pos;
+      if (r < 0 || (int64_t)r >= (int64_t)T * K) {  // histograms that do not match idx
+        report(status, MOE_ERR_DEVICE_BOUNDS);
+        dst_row[t * K + k] = -1;
+        continue;
+      }
       dst_row[t * K + k] = r;
       src_token[r] = (int32_t)t;
       if (perm_prob) perm_prob[r] = prob ? __ldg(prob + t * K + k) : 1.f;
@@ -269,14 +275,14 @@ __global__ void __launch_bounds__(256) chunk_ranks_kernel(
     const int32_t* __restrict__ idx, const float* __restrict__ prob, int T, int K, int E, int cap,
     int NC, const int32_t* __restrict__ base, const int32_t* __restrict__ counts,
     int32_t* __restrict__ offsets_out, int32_t* __restrict__ dst_row,
-    int32_t* __restrict__ src_token, float* __restrict__ perm_prob) {
+    int32_t* __restrict__ src_token, float* __restrict__ perm_prob, int* status) {
   __shared__ int32_t s_off[257];
   __shared__ int32_t s_warp[8];
   block_offsets(counts, E, s_off, s_warp, offsets_out);
   const int c = blockIdx.x * 8 + (threadIdx.x >> 5);
   if (c < NC)
     ranks_chunk(c, threadIdx.x & 31, idx, prob, T, K, E, cap, base, s_off, dst_row, src_token,
-                perm_prob);
+                perm_prob, status);
 }
 
 // Steps 2 and 3 in one kernel for small batches (NC * E <= kScanInBlock):
@@ -290,7 +296,7 @@ __global__ void __launch_bounds__(256) chunk_scan_ranks_kernel(
     const int32_t* __restrict__ idx, const float* __restrict__ prob, int T, int K, int E, int cap,
     int NC, const int32_t* __restrict__ hist, int32_t* __restrict__ counts_out,
     int32_t* __restrict__ offsets_out, int32_t* __restrict__ dst_row,
-    int32_t* __restrict__ src_token, float* __restrict__ perm_prob) {
+    int32_t* __restrict__ src_token, float* __restrict__ perm_prob, int* status) {
   extern __shared__ int32_t sh[];
   pdl_wait();
   pdl_trigger();
@@ -330,7 +336,8 @@ __global__ void __launch_bounds__(256) chunk_scan_ranks_kernel(
   __syncthreads();
   const int c = blockIdx.x * 8 + warp;
   if (c < NC)
-    ranks_chunk(c, lane, idx, prob, T, K, E, cap, s_base, s_off, dst_row, src_token, perm_prob);
+    ranks_chunk(c, lane, idx, prob, T, K, E, cap, s_base, s_off, dst_row, src_token, perm_prob,
+                status);
 }
 
 // One warp per token (the grid covers every token, so the block scheduler
@@ -349,10 +356,23 @@ __global__ void __launch_bounds__(256) scatter_rows_kernel(const T* __restrict__
 
 int num_chunks(int T) { return (int)ceil_div(T, kChunk); }
 
+// Step 1 alone: the per-chunk histograms of idx (the router's hand-off to
+// the dispatch when its own epilogue does not produce them).
+cudaError_t launch_chunk_hist(const moe_config_t& c, const int32_t* idx, int32_t* hist,
+                              int* status, cudaStream_t s) {
+  if (c.T == 0) return cudaSuccess;
+  const int NC = num_chunks(c.T);
+  chunk_hist_kernel<<<(unsigned)ceil_div(NC, 8), 256, 8 * c.E * sizeof(int32_t), s>>>(
+      idx, c.T, c.K, c.E, NC, hist, status);
+  return cudaGetLastError();
+}
+
+// hist_ready: hist already holds idx's chunk histograms (written by the
+// router), so step 1 is skipped.
 cudaError_t launch_permute_maps(const moe_config_t& c, const int32_t* idx, const float* prob,
                                 int32_t* hist, int32_t* base, int32_t* counts, int32_t* offsets,
                                 int32_t* dst_row, int32_t* src_token, float* perm_prob,
-                                int* status, cudaStream_t s) {
+                                int* status, cudaStream_t s, bool hist_ready) {
   const int NC = num_chunks(c.T);
   if (c.T == 0) {
     // no rows: counts and offsets are all zero
@@ -361,18 +381,19 @@ cudaError_t launch_permute_maps(const moe_config_t& c, const int32_t* idx, const
     return e;
   }
   const int blocks = (int)ceil_div(NC, 8);
-  chunk_hist_kernel<<<blocks, 256, 8 * c.E * sizeof(int32_t), s>>>(idx, c.T, c.K, c.E, NC, hist,
-                                                                  status);
+  if (!hist_ready)
+    chunk_hist_kernel<<<blocks, 256, 8 * c.E * sizeof(int32_t), s>>>(idx, c.T, c.K, c.E, NC, hist,
+                                                                    status);
   if ((int64_t)NC * c.E <= kScanInBlock) {
     const size_t bytes = sizeof(int32_t) * ((size_t)NC * c.E + 2 * c.E + 1);
     return pdl_launch(chunk_scan_ranks_kernel, dim3(blocks), dim3(256), bytes, s, idx, prob, c.T,
                       c.K, c.E, c.capacity, NC, (const int32_t*)hist, counts, offsets, dst_row,
-                      src_token, perm_prob);
+                      src_token, perm_prob, status);
   }
   chunk_scan_kernel<<<(unsigned)ceil_div(c.E, 8), 256, 0, s>>>(hist, NC, c.E, c.capacity, base,
                                                                 counts);
   chunk_ranks_kernel<<<blocks, 256, 0, s>>>(idx, prob, c.T, c.K, c.E, c.capacity, NC, base, counts,
-                                            offsets, dst_row, src_token, perm_prob);
+                                            offsets, dst_row, src_token, perm_prob, status);
   return cudaGetLastError();
 }
 

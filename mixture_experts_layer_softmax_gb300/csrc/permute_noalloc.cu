@@ -22,7 +22,7 @@
 namespace moe {
 cudaError_t launch_permute_maps(const moe_config_t&, const int32_t*, const float*, int32_t*,
                                 int32_t*, int32_t*, int32_t*, int32_t*, int32_t*, float*, int*,
-                                cudaStream_t);
+                                cudaStream_t, bool hist_ready = false);
 cudaError_t launch_scatter_rows(const moe_config_t&, const void*, const int32_t*, void*, int,
                                 int*, cudaStream_t, bool after_maps = false);
 int num_chunks(int T);

@@ -355,16 +355,41 @@ cudaError_t launch_router_gemm_tc(int T, const void* x, int h, const void* w3, i
 bool router_tc_small_ok(const moe_config_t& c);
 cudaError_t launch_router_tc_small(const moe_config_t& c, const void* x, const float* w_r,
                                    const float* gate_bias, float* logits, const RouterArgs& a,
-                                   int sms, int* status, cudaStream_t s);
+                                   int32_t* hist, int sms, int* status, cudaStream_t s);
 
+cudaError_t launch_chunk_hist(const moe_config_t& c, const int32_t* idx, int32_t* hist,
+                              int* status, cudaStream_t s);
+
+static cudaError_t launch_router_body(const moe_config_t& c, const void* x, const float* w_r,
+                                      const float* gate_bias, const float* sel_bias,
+                                      float* logits, int32_t* idx, float* prob, uint8_t* map,
+                                      const RouterScratch& rs, int sms, int* status,
+                                      cudaStream_t s);
+
+// hist (or null): also leave the dispatch's per-chunk expert histograms of
+// idx there -- from the one-launch router's epilogue when it runs, else by
+// the dispatch's own histogram step right after the route.
 cudaError_t launch_router(const moe_config_t& c, const void* x, const float* w_r,
                           const float* gate_bias, const float* sel_bias, float* logits,
                           int32_t* idx, float* prob, uint8_t* map, const RouterScratch& rs,
-                          int sms, int* status, cudaStream_t s) {
+                          int sms, int* status, cudaStream_t s, int32_t* hist) {
   if (c.T == 0) return cudaSuccess;
+  if (router_tc_small_ok(c)) {  // one launch: gating, slice sum, selection (and histograms)
+    RouterArgs a = make_args(c, sel_bias, idx, prob, map);
+    return launch_router_tc_small(c, x, w_r, gate_bias, logits, a, hist, sms, status, s);
+  }
+  cudaError_t e = launch_router_body(c, x, w_r, gate_bias, sel_bias, logits, idx, prob, map, rs,
+                                     sms, status, s);
+  if (e == cudaSuccess && hist) e = launch_chunk_hist(c, idx, hist, status, s);
+  return e;
+}
+
+static cudaError_t launch_router_body(const moe_config_t& c, const void* x, const float* w_r,
+                                      const float* gate_bias, const float* sel_bias,
+                                      float* logits, int32_t* idx, float* prob, uint8_t* map,
+                                      const RouterScratch& rs, int sms, int* status,
+                                      cudaStream_t s) {
   RouterArgs a = make_args(c, sel_bias, idx, prob, map);
-  if (router_tc_small_ok(c))  // one launch: gating, slice sum and selection
-    return launch_router_tc_small(c, x, w_r, gate_bias, logits, a, sms, status, s);
   if (c.dtype == MOE_BF16) {
     const int ept = router_ept(c.E), bn = router_bn(c.E);
     const int ntiles = router_ntiles(c.E);

@@ -119,29 +119,48 @@ MOE_D void select_and_write(const float (&logit)[J], int t, const RouterArgs& a,
       }
       // the fast pass also ranks the (K+1)-th key, to check the K-th gap
       const int rounds = exact ? a.K : min(a.K + 1, a.E);
-      uint32_t skey[J];
+      // This lane's candidates sorted once, best first (larger key; equal
+      // keys: lower expert), so each round offers just the head of the list
+      // and the winning lane shifts its list by one.  Codes are 0 past E
+      // (below every key).
+      uint32_t sc[J];
+      int se[J];
 #pragma unroll
-      for (int j = 0; j < J; ++j) skey[j] = sortable_key(key[j]);
+      for (int j = 0; j < J; ++j) {
+        const int e = lane + 32 * j;
+        sc[j] = e < a.E ? sortable_key(key[j]) : 0u;
+        se[j] = e;
+      }
+#pragma unroll
+      for (int pass = 0; pass < J; ++pass)  // odd-even transposition sort
+#pragma unroll
+        for (int j = pass & 1; j + 1 < J; j += 2) {
+          const bool swap = sc[j + 1] > sc[j] || (sc[j + 1] == sc[j] && se[j + 1] < se[j]);
+          const uint32_t c0 = sc[j], c1 = sc[j + 1];
+          const int e0 = se[j], e1 = se[j + 1];
+          sc[j] = swap ? c1 : c0;
+          sc[j + 1] = swap ? c0 : c1;
+          se[j] = swap ? e1 : e0;
+          se[j + 1] = swap ? e0 : e1;
+        }
       bool safe = true;
       float prev = 0.f;
       for (int k = 0; k < rounds; ++k) {
-        // this lane's best untaken candidate (ascending j: ties keep the
-        // lower expert), then the warp's largest key and, among the lanes
-        // holding it, the lowest expert index: two warp reductions
-        uint32_t lk = 0u;
-        int li = 0x7fffffff;
-#pragma unroll
-        for (int j = 0; j < J; ++j) {
-          const int e = lane + 32 * j;
-          if (e < a.E && !((taken >> j) & 1u) && skey[j] > lk) {
-            lk = skey[j];
-            li = e;
-          }
-        }
+        // the warp's largest head key and, among the lanes holding it, the
+        // lowest expert index: two warp reductions
+        const uint32_t lk = sc[0];
         const uint32_t m = __reduce_max_sync(FULL, lk);
-        const int bi = (int)__reduce_min_sync(FULL, lk == m ? (uint32_t)li : 0xffffffffu);
+        const int bi = (int)__reduce_min_sync(FULL, lk == m ? (uint32_t)se[0] : 0xffffffffu);
         const float bk = from_sortable_key(m);
-        if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+        if ((bi & 31) == lane) {
+          taken |= 1u << (bi >> 5);
+#pragma unroll
+          for (int j = 0; j + 1 < J; ++j) {
+            sc[j] = sc[j + 1];
+            se[j] = se[j + 1];
+          }
+          sc[J - 1] = 0u;
+        }
         if (k < a.K && lane == k) my_idx = bi;
         if (!exact && k > 0 && !(prev - bk > 4e-6f * (1.f + fabsf(prev) + fabsf(bk))))
           safe = false;  // warp-uniform: bk and prev are the same on every lane
@@ -242,8 +261,9 @@ MOE_D float butterfly_sum8(const float (&v)[8]) {
 // expert's rank in that order is counted in one parallel pass (experts with a
 // larger key, or an equal key and a lower index, come first): the k-th
 // selected expert is the one of rank k.  The probabilities are evaluated
-// branch-free for all 8 slots and masked.
-MOE_D void select_row8(const float (&l)[8], int t, const RouterArgs& a) {
+// branch-free for all 8 slots and masked.  Returns the selected set as a
+// bit mask (bit e: expert e).
+MOE_D uint32_t select_row8(const float (&l)[8], int t, const RouterArgs& a) {
   int sel[8];
 #pragma unroll
   for (int k = 0; k < 8; ++k) sel[k] = 0;
@@ -386,6 +406,7 @@ MOE_D void select_row8(const float (&l)[8], int t, const RouterArgs& a) {
     }
   if (a.routing_map)
     for (int e = 0; e < a.E; ++e) a.routing_map[(int64_t)t * a.E + e] = (taken >> e) & 1u;
+  return taken;
 }
 
 }  // namespace moe

@@ -75,6 +75,7 @@ struct RouterTcParams {
   int T, h, E;
   const float* gate_bias;
   float* logits;
+  int32_t* hist;  // [ceil(T/32)][E] per-chunk expert histograms of the selection, or null
   RouterArgs a;
   int* status;
 };
@@ -295,6 +296,7 @@ __global__ void __cluster_dims__(kRCl, 1, 1) __launch_bounds__(kRThreads, 1)
           for (int e = 0; e < 8; ++e)
             if (e < p.E) l[e] = __fadd_rn(l[e], __ldg(p.gate_bias + e));
         const int64_t t = (int64_t)tile * kRBN + rank * kRFin + ct;
+        uint32_t taken = 0u;
         if (t < p.T) {
           if (p.logits) {
             float* lrow = p.logits + t * p.E;
@@ -302,7 +304,19 @@ __global__ void __cluster_dims__(kRCl, 1, 1) __launch_bounds__(kRThreads, 1)
             for (int e = 0; e < 8; ++e)
               if (e < p.E) lrow[e] = l[e];
           }
-          select_row8(l, (int)t, ra);
+          taken = select_row8(l, (int)t, ra);
+        }
+        // the dispatch's chunk histogram: this warp's 32 tokens are exactly
+        // one chunk of 32 (tiles and the 64-token quarters are chunk-aligned)
+        if (p.hist) {
+          const int64_t t0 = t - lane;
+          int cnt = 0;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const int ce = (int)__reduce_add_sync(FULL, (taken >> e) & 1u);
+            if (lane == e) cnt = ce;
+          }
+          if (t0 < p.T && lane < p.E) p.hist[(t0 / 32) * p.E + lane] = cnt;
         }
       }
     }
@@ -324,7 +338,7 @@ bool router_tc_small_ok(const moe_config_t& c) {
 
 cudaError_t launch_router_tc_small(const moe_config_t& c, const void* x, const float* w_r,
                                    const float* gate_bias, float* logits, const RouterArgs& a,
-                                   int sms, int* status, cudaStream_t s) {
+                                   int32_t* hist, int sms, int* status, cudaStream_t s) {
   (void)sms;  // one cluster per tile, whatever the SM count
   if (c.T == 0) return cudaSuccess;
   if (!router_tc_small_ok(c)) return cudaErrorInvalidValue;
@@ -353,7 +367,7 @@ cudaError_t launch_router_tc_small(const moe_config_t& c, const void* x, const f
   }
   RouterTcParams p;
   p.T = c.T; p.h = c.h; p.E = c.E;
-  p.gate_bias = gate_bias; p.logits = logits; p.a = a; p.status = status;
+  p.gate_bias = gate_bias; p.logits = logits; p.hist = hist; p.a = a; p.status = status;
   cudaError_t e = cudaFuncSetAttribute(router_tc_small_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kRSmem);
   if (e != cudaSuccess) return e;

@@ -30,6 +30,7 @@ MOE_ACT_GELU, MOE_ACT_SWIGLU = 0, 1
 MOE_FLAG_RENORM, MOE_FLAG_FORCE_BALANCE = 1, 2
 MOE_FLAG_VALIDATE_ONLY, MOE_FLAG_SAVE_FOR_BWD, MOE_FLAG_GEMM_SIMT = 8, 16, 32
 MOE_FLAG_GEMM_1CTA, MOE_FLAG_GEMM_2CTA = 64, 128
+MOE_FLAG_HIST_FROM_ROUTER = 256
 
 
 class moe_config_t(ctypes.Structure):

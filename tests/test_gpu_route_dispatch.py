@@ -248,3 +248,49 @@ def test_bounded_wait_times_out_and_context_survives():
     assert M.moe_get_error() == M.MOE_OK
     t = torch.ones(8, device="cuda")
     assert float(t.sum()) == 8.0
+
+
+@pytest.mark.parametrize("T,h,E,K,dtype", [
+    (1000, 256, 8, 2, "bf16"),    # one-launch router: histograms from its epilogue
+    (257, 128, 6, 3, "bf16"),     # ragged last chunk, E < 8
+    (1, 64, 8, 1, "bf16"),
+    (777, 128, 64, 8, "bf16"),    # tensor-core gating GEMM + selection, then the histogram step
+    (300, 64, 16, 4, "f32"),
+])
+def test_router_histogram_hand_off_gives_the_same_dispatch(T, h, E, K, dtype):
+    """MOE_FLAG_HIST_FROM_ROUTER: the router leaves the per-chunk histograms in
+    the workspace and moe_permute starts from them; maps and rows are bit-for-
+    bit those of moe_permute counting on its own."""
+    M = lib()
+    x = to_dev(inputs.normal((T, h), 1.0, T + E, 1, dtype), dtype)
+    w_r = to_dev(inputs.normal((E, h), 0.05, T + E, 2), "f32")
+    dt = M.MOE_BF16 if dtype == "bf16" else M.MOE_F32
+    base = M.MOE_FLAG_RENORM
+    cfg_h = M.make_config(T, h, E, K, 8, dt, 0, M.MOE_ACT_SWIGLU, 0, 0, base | M.MOE_FLAG_HIST_FROM_ROUTER)
+    cfg = M.make_config(T, h, E, K, 8, dt, 0, M.MOE_ACT_SWIGLU, 0, 0, base)
+    ws = torch.full((M.moe_workspace_size(cfg_h),), 0x7f, dtype=torch.uint8, device="cuda")
+    i32 = dict(dtype=torch.int32, device="cuda")
+    P = T * K
+    idx, prob = torch.empty(T, K, **i32), torch.empty(T, K, device="cuda")
+    M.moe_router_topk(cfg_h, x, w_r, None, None, None, idx, prob, None, ws)
+
+    def dispatch(c, w):
+        out = dict(x_perm=torch.empty(P, h, dtype=x.dtype, device="cuda"),
+                   counts=torch.empty(E, **i32), offsets=torch.empty(E + 1, **i32),
+                   dst_row=torch.empty(T, K, **i32), src_token=torch.empty(P, **i32),
+                   perm_prob=torch.empty(P, device="cuda"))
+        M.moe_permute(c, x, idx, prob, out["x_perm"], out["counts"], out["offsets"],
+                      out["dst_row"], out["src_token"], out["perm_prob"], w)
+        return out
+
+    got = dispatch(cfg_h, ws)
+    want = dispatch(cfg, torch.empty(M.moe_workspace_size(cfg), dtype=torch.uint8, device="cuda"))
+    torch.cuda.synchronize()
+    assert M.moe_get_error() == M.MOE_OK
+    for k in want:
+        a, b = want[k], got[k]
+        if a.dtype in (torch.bfloat16, torch.float32) and k == "x_perm":
+            a, b = a.view(torch.int16 if a.dtype == torch.bfloat16 else torch.int32), \
+                b.view(torch.int16 if b.dtype == torch.bfloat16 else torch.int32)
+        assert torch.equal(a, b), k
+    assert int(got["offsets"][-1]) == P
