@@ -960,11 +960,23 @@ def run_ours(args, w):
         pair = args.tiling == "2cta" or (args.tiling == "auto" and P >= 512 * E)
         fc1_kernel = ("grouped_gemm_tc2_kernel<FC1> (CTA pairs)" if pair
                       else "grouped_gemm_tc_kernel<FC1>")
-        line["roofline"] = {"kernel": fc1_kernel, "bound": "tensor",
-                            "achieved": fc1_tf, "peak": peak_tf, "unit": "TFLOP/s",
-                            "frac": fc1_tf / peak_tf, "peak_kind": f"{pk_kind} bf16 burst (cuBLAS)",
-                            "traffic": traffic_record(w), "flops_per_launch": fc1_flops,
-                            "ms_per_launch": stage_ms["fc1"]}
+        if w.dtype == "bf16":
+            line["roofline"] = {"kernel": fc1_kernel, "bound": "tensor",
+                                "achieved": fc1_tf, "peak": peak_tf, "unit": "TFLOP/s",
+                                "frac": fc1_tf / peak_tf,
+                                "peak_kind": f"{pk_kind} bf16 burst (cuBLAS)",
+                                "traffic": traffic_record(w), "flops_per_launch": fc1_flops,
+                                "ms_per_launch": stage_ms["fc1"]}
+        else:
+            # fp32 runs the SIMT grouped GEMM on the FP32 ALUs: the peak is 152 SMs x
+            # 128 FP32 lanes x 2 FLOP (FMA) x 2.07 GHz = 80.5 TFLOP/s
+            alu_peak = 152 * 128 * 2 * 2.07e9 / 1e12
+            line["roofline"] = {"kernel": "grouped_gemm_simt_kernel<FC1> (fp32)", "bound": "alu",
+                                "achieved": fc1_tf, "peak": alu_peak, "unit": "TFLOP/s",
+                                "frac": fc1_tf / alu_peak,
+                                "peak_kind": "nominal fp32 FMA rate (152 SMs x 128 lanes x 2.07 GHz)",
+                                "traffic": None, "flops_per_launch": fc1_flops,
+                                "ms_per_launch": stage_ms["fc1"]}
         line["grouped_gemm_pct_bf16_peak"] = 100.0 * gemm_tf / peak_tf
         line["grouped_gemm_tflops"] = gemm_tf
         line["permute_pct_hbm"] = 100.0 * perm_gbs / pk["hbm_gbs"]
