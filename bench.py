@@ -968,13 +968,14 @@ def run_ours(args, w):
                                 "traffic": traffic_record(w), "flops_per_launch": fc1_flops,
                                 "ms_per_launch": stage_ms["fc1"]}
         else:
-            # fp32 runs the SIMT grouped GEMM on the FP32 ALUs: the peak is 152 SMs x
-            # 128 FP32 lanes x 2 FLOP (FMA) x 2.07 GHz = 80.5 TFLOP/s
-            alu_peak = 152 * 128 * 2 * 2.07e9 / 1e12
+            # fp32 runs the SIMT grouped GEMM on the FP32 ALUs: the peak is the SM count
+            # x 128 FP32 lanes x 2 FLOP (FMA) x the maximum SM clock (2.07 GHz)
+            n_sm = torch.cuda.get_device_properties(dev).multi_processor_count
+            alu_peak = n_sm * 128 * 2 * 2.07e9 / 1e12
             line["roofline"] = {"kernel": "grouped_gemm_simt_kernel<FC1> (fp32)", "bound": "alu",
                                 "achieved": fc1_tf, "peak": alu_peak, "unit": "TFLOP/s",
                                 "frac": fc1_tf / alu_peak,
-                                "peak_kind": "nominal fp32 FMA rate (152 SMs x 128 lanes x 2.07 GHz)",
+                                "peak_kind": f"nominal fp32 FMA rate ({n_sm} SMs x 128 lanes x 2.07 GHz)",
                                 "traffic": None, "flops_per_launch": fc1_flops,
                                 "ms_per_launch": stage_ms["fc1"]}
         line["grouped_gemm_pct_bf16_peak"] = 100.0 * gemm_tf / peak_tf
