@@ -284,7 +284,8 @@ def test_router_histogram_hand_off_gives_the_same_dispatch(T, h, E, K, dtype):
         return out
 
     got = dispatch(cfg_h, ws)
-    want = dispatch(cfg, torch.empty(M.moe_workspace_size(cfg), dtype=torch.uint8, device="cuda"))
+    ws_plain = torch.empty(M.moe_workspace_size(cfg), dtype=torch.uint8, device="cuda")
+    want = dispatch(cfg, ws_plain)
     torch.cuda.synchronize()
     assert M.moe_get_error() == M.MOE_OK
     for k in want:
@@ -294,3 +295,17 @@ def test_router_histogram_hand_off_gives_the_same_dispatch(T, h, E, K, dtype):
                 b.view(torch.int16 if b.dtype == torch.bfloat16 else torch.int32)
         assert torch.equal(a, b), k
     assert int(got["offsets"][-1]) == P
+    if dtype == "bf16" and h % 128 == 0:  # the MXFP8 dispatch takes the same hand-off
+        sfb = M.moe_mxfp8_scale_bytes(P, h, E)
+        res = []
+        for c, w in ((cfg_h, ws), (cfg, ws_plain)):
+            q = torch.zeros(P, h, dtype=torch.uint8, device="cuda")
+            sf = torch.zeros(max(sfb, 16), dtype=torch.uint8, device="cuda")
+            m = [torch.empty(E, **i32), torch.empty(E + 1, **i32), torch.empty(T, K, **i32),
+                 torch.empty(P, **i32), torch.empty(P, device="cuda")]
+            M.moe_permute_mxfp8(c, x, idx, prob, q, sf, *m, w)
+            res.append([q, sf] + m)
+        torch.cuda.synchronize()
+        assert M.moe_get_error() == M.MOE_OK
+        for a, b in zip(*res):
+            assert torch.equal(a, b)
