@@ -11,6 +11,16 @@
 // kernel this halves the B bytes each SM pulls from L2 and its shared-memory
 // stage (32 KB, so 6 stages fit).
 //
+// Half tiles: an expert's last row block with at most 128 rows is computed
+// as a 128 x 256 tile (M128 N256 K16 pair MMAs, which take half the cycles
+// of M256 ones) instead of a padded 256-row one.  CTA r then loads 64 A rows
+// [64r, 64r+64) and still 128 B rows; its TMEM lanes 0-63 receive its 64 rows
+// x output columns 0-127 (products with CTA 0's B rows) in accumulator
+// columns 0-127, and lanes 64-127 the same 64 rows x output columns 128-255
+// (CTA 1's B rows).  For SwiGLU each CTA loads 64 gate rows and the matching
+// 64 up rows, so that a lane's gate and up values of one hidden column share
+// the lane: gate in accumulator columns 0-63, up in 64-127.
+//
 // Protocol (all waits bounded):
 //   full[s]       even CTA, count 1: its producer posts expect_tx for both CTAs'
 //                 bytes; both CTAs' TMA loads complete on it (.cta_group::2).
@@ -107,7 +117,8 @@ MOE_D void commit_pair_multicast(uint32_t bar, uint16_t mask) {
       : "memory");
 }
 
-MOE_D void decode_tile(const SmemCtl& c, int E, int nblk, int tile, int& e, int& mb, int& nb) {
+MOE_D void decode_tile(const SmemCtl& c, int E, int nblk, int tile, int& e, int& mb, int& nb,
+                       bool& half) {
   int lo = 0, hi = E - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
@@ -118,6 +129,7 @@ MOE_D void decode_tile(const SmemCtl& c, int E, int nblk, int tile, int& e, int&
   const int mblk = (c.off[e + 1] - c.off[e] + BMC - 1) / BMC;
   nb = local / mblk;
   mb = local - nb * mblk;
+  half = c.off[e + 1] - c.off[e] - mb * BMC <= BM;  // at most 128 rows left
 }
 
 MOE_D uint32_t pack_bf16x2(float a, float b) {
@@ -150,10 +162,30 @@ MOE_D void tma_gather4_pair(uint32_t dst, const CUtensorMap* map, int32_t c0, in
       : "memory");
 }
 
+// Bytes both CTAs' loads of one stage deliver (the even CTA's expect_tx).
+MOE_D uint32_t stage_tx(bool half) {
+  return half ? 2u * (A_BYTES / 2 + B_BYTES) : 2u * STAGE_BYTES;
+}
+
+// First weight row this CTA loads for N block nb of expert e.  SwiGLU (B =
+// [gate; up] per expert): a full tile's CTA r loads 128 gate (r = 0) or up
+// (r = 1) rows; a half tile's CTA r loads gate rows [64r, 64r + 64) of the
+// block and the matching up rows (returned: the first gate row).  Otherwise
+// CTA r loads B rows [128r, 128r + 128) of the block's 256.
+template <int MODE>
+MOE_D int b_first_row_t(const Tc2Params& p, int e, int nb, uint32_t rank, bool half) {
+  if (MODE == kSwiGLU)
+    return half ? e * p.Nb + nb * BNL + (int)rank * (BNL / 2)
+                : e * p.Nb + (int)rank * p.N + nb * BNL;
+  return e * p.Nb + nb * BN + (int)rank * BNL;
+}
+
 template <int MODE, bool GATHER>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     grouped_gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmA,
-                            const __grid_constant__ CUtensorMap tmB, const Tc2Params p) {
+                            const __grid_constant__ CUtensorMap tmB,
+                            const __grid_constant__ CUtensorMap tmA64,
+                            const __grid_constant__ CUtensorMap tmB64, const Tc2Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -168,6 +200,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int E = p.E;
   const int nblk = MODE == kSwiGLU ? (p.N + BNL - 1) / BNL : (p.N + BN - 1) / BN;
   const int KB = (p.Kd + BK - 1) / BK;
+  auto b_first_row = [](const Tc2Params& pp, int e, int nb, uint32_t r, bool half) {
+    return b_first_row_t<MODE>(pp, e, nb, r, half);
+  };
+  // The B rows of one stage: one 128-row box, or for a SwiGLU half tile a
+  // 64-row box of gate rows and one of the matching up rows (p.N rows further).
+  auto load_b = [](uint32_t dst, const CUtensorMap* m128, const CUtensorMap* m64, int k, int row,
+                   int n_rows, bool half, uint32_t bar) {
+    if (MODE == kSwiGLU && half) {
+      tma_load_2d_pair(dst, m64, k, row, bar);
+      tma_load_2d_pair(dst + B_BYTES / 2, m64, k, row + n_rows, bar);
+    } else {
+      tma_load_2d_pair(dst, m128, k, row, bar);
+    }
+  };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -183,6 +229,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tc::fence_barrier_init();
     tc::prefetch_tensormap(&tmA);
     tc::prefetch_tensormap(&tmB);
+    if (!GATHER) tc::prefetch_tensormap(&tmA64);
+    if (MODE == kSwiGLU) tc::prefetch_tensormap(&tmB64);
   }
   if (warp == 1) {
     tmem_alloc_pair(tc::smem_u32(&ctl.tmem_base), TMEM_COLS);
@@ -222,12 +270,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int tile = cid; tile < total && ok; tile += ncl) {
       int e, mb, nb;
-      decode_tile(ctl, E, nblk, tile, e, mb, nb);
-      const int lrow0 = mb * BMC + (int)rank * BM;  // first A row of this CTA, inside the expert
+      bool half;
+      decode_tile(ctl, E, nblk, tile, e, mb, nb, half);
+      const int rows_cta = half ? BM / 2 : BM;
+      const int lrow0 = mb * BMC + (int)rank * rows_cta;  // first A row of this CTA, inside the expert
       const int m_e = ctl.off[e + 1] - ctl.off[e];
-      const int b_row = MODE == kSwiGLU ? e * p.Nb + (int)rank * p.N + nb * BNL
-                                        : e * p.Nb + nb * BN + (int)rank * BNL;
-      // this lane's 4 rows (4 lane .. 4 lane + 3) of the CTA's 128
+      const int b_row = b_first_row(p, e, nb, rank, half);
+      // this lane's 4 rows (4 lane .. 4 lane + 3) of the CTA's 128 (64 in a
+      // half tile: lanes 16..31 then load nothing)
+      const bool gl = 4 * lane < rows_cta;
       int rr[4];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
@@ -241,11 +292,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const uint32_t full_local = tc::smem_u32(&ctl.full[stage]);
         const uint32_t full_even = mapa(full_local, 0);
         if (lane == 0) {
-          if (even) tc::mbar_arrive_expect_tx(full_local, 2 * STAGE_BYTES);
-          tma_load_2d_pair(tc::smem_u32(sB + stage * B_BYTES), &tmB, kb * BK, b_row, full_even);
+          if (even) tc::mbar_arrive_expect_tx(full_local, stage_tx(half));
+          load_b(tc::smem_u32(sB + stage * B_BYTES), &tmB, &tmB64, kb * BK, b_row, p.N, half,
+                 full_even);
         }
-        tma_gather4_pair(tc::smem_u32(sA + stage * A_BYTES) + lane * 512, &tmA, kb * BK, rows,
-                         full_even);
+        if (gl)
+          tma_gather4_pair(tc::smem_u32(sA + stage * A_BYTES) + lane * 512, &tmA, kb * BK, rows,
+                           full_even);
         issued |= 1u << stage;
         issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
         if (++stage == STAGES) { stage = 0; phase ^= 1; }
@@ -264,17 +317,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int tile = cid; tile < total && ok; tile += ncl) {
         int e, mb, nb;
-        decode_tile(ctl, E, nblk, tile, e, mb, nb);
-        const int a_row = ctl.off[e] + mb * BMC + (int)rank * BM;
-        const int b_row = MODE == kSwiGLU ? e * p.Nb + (int)rank * p.N + nb * BNL
-                                          : e * p.Nb + nb * BN + (int)rank * BNL;
+        bool half;
+        decode_tile(ctl, E, nblk, tile, e, mb, nb, half);
+        const int a_row = ctl.off[e] + mb * BMC + (int)rank * (half ? BM / 2 : BM);
+        const int b_row = b_first_row(p, e, nb, rank, half);
         for (int kb = 0; kb < KB; ++kb) {
           if (!tc::mbar_wait(tc::smem_u32(&ctl.empty[stage]), phase ^ 1, wc)) { ok = false; break; }
           const uint32_t full_local = tc::smem_u32(&ctl.full[stage]);
-          if (even) tc::mbar_arrive_expect_tx(full_local, 2 * STAGE_BYTES);
+          if (even) tc::mbar_arrive_expect_tx(full_local, stage_tx(half));
           const uint32_t full_even = mapa(full_local, 0);
-          tma_load_2d_pair(tc::smem_u32(sA + stage * A_BYTES), &tmA, kb * BK, a_row, full_even);
-          tma_load_2d_pair(tc::smem_u32(sB + stage * B_BYTES), &tmB, kb * BK, b_row, full_even);
+          tma_load_2d_pair(tc::smem_u32(sA + stage * A_BYTES), half ? &tmA64 : &tmA, kb * BK, a_row,
+                           full_even);
+          load_b(tc::smem_u32(sB + stage * B_BYTES), &tmB, &tmB64, kb * BK, b_row, p.N, half,
+                 full_even);
           issued |= 1u << stage;
           issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
           if (++stage == STAGES) { stage = 0; phase ^= 1; }
@@ -291,11 +346,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ================= MMA issuer (even CTA) =================
     if (even && lane == 0) {
-      constexpr uint32_t idesc = tc::idesc_bf16_f32(BMC, BN);
+      constexpr uint32_t idesc_full = tc::idesc_bf16_f32(BMC, BN);
+      constexpr uint32_t idesc_half = tc::idesc_bf16_f32(BM, BN);
       int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool ok = true;
       for (int tile = cid; tile < total && ok; tile += ncl) {
+        int e, mb, nb;
+        bool half;
+        decode_tile(ctl, E, nblk, tile, e, mb, nb, half);
+        const uint32_t idesc = half ? idesc_half : idesc_full;
         if (!tc::mbar_wait(tc::smem_u32(&ctl.tmem_empty[acc]), acc_phase ^ 1, wc)) break;
         tc::fence_after_sync();
         const uint32_t d = tmem_base + (uint32_t)(acc * BN);
@@ -328,22 +388,31 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const uint32_t tmem_empty_even1 = mapa(tc::smem_u32(&ctl.tmem_empty[1]), 0);
     for (int tile = cid; tile < total; tile += ncl) {
       int e, mb, nb;
-      decode_tile(ctl, E, nblk, tile, e, mb, nb);
+      bool half;
+      decode_tile(ctl, E, nblk, tile, e, mb, nb, half);
       if (!tc::mbar_wait(tc::smem_u32(&ctl.tmem_full[acc]), acc_phase, wc)) break;
       tc::fence_after_sync();
       const int m_e = ctl.off[e + 1] - ctl.off[e];
-      const int local_row = mb * BMC + (int)rank * BM + q * 32 + lane;
+      // Full tile: warp q holds rows 32q.. of the CTA's 128, every column.
+      // Half tile: warps 0-1 and 2-3 hold the same 64 rows (lanes 0-63 and
+      // 64-127), warps 2-3 the second half of the output columns.
+      const int local_row = half ? mb * BMC + (int)rank * (BM / 2) + (q & 1) * 32 + lane
+                                 : mb * BMC + (int)rank * BM + q * 32 + lane;
+      const int col_half = half ? (q >> 1) : 0;
       const bool valid = local_row < m_e;
       const int64_t row = (int64_t)ctl.off[e] + local_row;
       const float pr = (p.prob && p.prob_here && valid) ? __ldg(p.prob + row) : 1.f;
       const uint32_t tbase = tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(q * 32) << 16);
       if (MODE == kSwiGLU) {
+        // gate at accumulator column c, up at c + ncol (ncol = 128 or 64)
+        const int ncol = half ? BNL / 2 : BNL;
+        const int n0 = nb * BNL + col_half * (BNL / 2);
 #pragma unroll 1
-        for (int c = 0; c < BNL / 32; ++c) {
+        for (int c = 0; c < ncol / 32; ++c) {
           uint32_t g[32], u[32];
           tc::tmem_ld_32x32b_x32(tbase + c * 32, g);
-          tc::tmem_ld_32x32b_x32(tbase + BNL + c * 32, u);
-          const int n = nb * BNL + c * 32;
+          tc::tmem_ld_32x32b_x32(tbase + ncol + c * 32, u);
+          const int n = n0 + c * 32;
           if (valid) {
 #pragma unroll
             for (int gq = 0; gq < 4; ++gq) {
@@ -364,11 +433,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
         }
       } else {
+        const int ncol = half ? BN / 2 : BN;
+        const int n0 = nb * BN + col_half * (BN / 2);
 #pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
+        for (int c = 0; c < ncol / 32; ++c) {
           uint32_t r[32];
           tc::tmem_ld_32x32b_x32(tbase + c * 32, r);
-          const int n = nb * BN + c * 32;
+          const int n = n0 + c * 32;
           if (valid) {
 #pragma unroll
             for (int gq = 0; gq < 4; ++gq) {
@@ -425,8 +496,9 @@ bool encode(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint
 }
 
 template <int MODE, bool GATHER>
-cudaError_t launch_mode2(const CUtensorMap& a, const CUtensorMap& b, const Tc2Params& p,
-                         int64_t tiles, int sms, cudaStream_t s) {
+cudaError_t launch_mode2(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& a64,
+                         const CUtensorMap& b64, const Tc2Params& p, int64_t tiles, int sms,
+                         cudaStream_t s) {
   auto kern = grouped_gemm_tc2_kernel<MODE, GATHER>;
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
@@ -443,7 +515,7 @@ cudaError_t launch_mode2(const CUtensorMap& a, const CUtensorMap& b, const Tc2Pa
       max_clusters < 1)
     max_clusters = sms / 2;
   const int64_t pairs = tiles < max_clusters ? tiles : max_clusters;
-  kern<<<(unsigned)(2 * pairs), kThreads, kSmemBytes, s>>>(a, b, p);
+  kern<<<(unsigned)(2 * pairs), kThreads, kSmemBytes, s>>>(a, b, a64, b64, p);
   return cudaGetLastError();
 }
 
@@ -460,11 +532,16 @@ cudaError_t launch_grouped_gemm_tc2(int mode, int P, const void* A, int Kd, cons
   if (P == 0) return cudaSuccess;
   const bool gather = src_token != nullptr;
   if (gather && mode == kFc2) return cudaErrorInvalidValue;
-  CUtensorMap ma, mb;
+  CUtensorMap ma, mb, ma64, mb64;
   if (!encode(&mb, B, (uint64_t)E * Nb, (uint64_t)Kd, BNL)) return cudaErrorInvalidValue;
   // gather: the token rows x [T, Kd], fetched four rows at a time (box one row high)
   if (!encode(&ma, A, (uint64_t)(gather ? T : P), (uint64_t)Kd, gather ? 1 : BM))
     return cudaErrorInvalidValue;
+  // half tiles: 64 A rows per CTA, and for SwiGLU 64 gate + 64 up weight rows
+  if (gather) ma64 = ma;
+  else if (!encode(&ma64, A, (uint64_t)P, (uint64_t)Kd, BM / 2)) return cudaErrorInvalidValue;
+  if (mode != kSwiGLU) mb64 = mb;
+  else if (!encode(&mb64, B, (uint64_t)E * Nb, (uint64_t)Kd, BNL / 2)) return cudaErrorInvalidValue;
   Tc2Params p;
   p.offsets = offsets; p.prob = prob;
   p.xg = static_cast<const __nv_bfloat16*>(A);
@@ -479,12 +556,12 @@ cudaError_t launch_grouped_gemm_tc2(int mode, int P, const void* A, int Kd, cons
   const int64_t tiles = (ceil_div(P, BMC) + E) * (int64_t)nblk;
   switch (mode) {
     case kSwiGLU:
-      return gather ? launch_mode2<kSwiGLU, true>(ma, mb, p, tiles, sms, s)
-                    : launch_mode2<kSwiGLU, false>(ma, mb, p, tiles, sms, s);
+      return gather ? launch_mode2<kSwiGLU, true>(ma, mb, ma64, mb64, p, tiles, sms, s)
+                    : launch_mode2<kSwiGLU, false>(ma, mb, ma64, mb64, p, tiles, sms, s);
     case kGelu:
-      return gather ? launch_mode2<kGelu, true>(ma, mb, p, tiles, sms, s)
-                    : launch_mode2<kGelu, false>(ma, mb, p, tiles, sms, s);
-    default: return launch_mode2<kFc2, false>(ma, mb, p, tiles, sms, s);
+      return gather ? launch_mode2<kGelu, true>(ma, mb, ma64, mb64, p, tiles, sms, s)
+                    : launch_mode2<kGelu, false>(ma, mb, ma64, mb64, p, tiles, sms, s);
+    default: return launch_mode2<kFc2, false>(ma, mb, ma64, mb64, p, tiles, sms, s);
   }
 }
 

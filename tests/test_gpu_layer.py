@@ -86,6 +86,73 @@ def test_grouped_mlp_matches_oracle(T, h, E, K, F, act, bias, dtype, skew, path)
     assert ok, ("act_save", err, bound)
 
 
+
+# Per-expert row counts around the pair kernel's 256-row tiles and its
+# 128-row tail tiles: tails of 1, 64, 65, 127, 128 rows (half tiles), of 129,
+# 255 rows (full tiles), whole blocks, an empty expert and a 5-block expert.
+PAIR_TAIL_COUNTS = [1, 64, 65, 127, 128, 129, 192, 255, 256, 257, 300, 384, 385, 0, 640]
+
+
+@pytest.mark.parametrize("act,bias,F", [(O.ACT_SWIGLU, False, 384), (O.ACT_SWIGLU, False, 200),
+                                        (O.ACT_GELU, True, 264)])
+def test_pair_tiles_with_tail_tiles_match_oracle(act, bias, F):
+    """Every tail kind of the CTA-pair GEMMs (half and full tail tiles, ragged
+    hidden sizes) within the bf16 tolerance of the oracle; the gathering FC1
+    equals FC1 on the permuted rows bit for bit."""
+    M = lib()
+    counts = np.array(PAIR_TAIL_COUNTS, dtype=np.int64)
+    E, h, seed = len(counts), 256, 71 + F
+    offsets = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    P = int(offsets[-1])
+    R1 = 2 * F if act == O.ACT_SWIGLU else F
+    T = 4000  # token rows the permuted rows are gathered from (T >= P)
+    rng = np.random.default_rng(seed)
+    src_token = rng.integers(0, T, size=P).astype(np.int32)
+    x = inputs.normal((T, h), 1.0, seed, 1, "bf16")
+    x_perm = x[src_token]
+    w1 = inputs.normal((E, R1, h), h ** -0.5, seed, 2, "bf16")
+    w2 = inputs.normal((E, h, F), F ** -0.5, seed, 3, "bf16")
+    b1 = inputs.normal((E, F), h ** -0.5, seed, 4, "bf16") if bias else None
+    b2 = inputs.normal((E, h), F ** -0.5, seed, 5, "bf16") if bias else None
+    prob = rng.uniform(0.05, 1.0, size=P).astype(np.float32)
+    # K = 1 and T = P: the permuted-row entry points see exactly P rows (the
+    # routing is not used; the offsets are given)
+    cfg = M.make_config(P, h, E, 1, F, M.MOE_BF16, M.MOE_SCORE_SOFTMAX, act, int(bias), 0,
+                        M.MOE_FLAG_RENORM | M.MOE_FLAG_GEMM_2CTA)
+    dv = lambda a: None if a is None else to_dev(a, "bf16")
+    offs = torch.from_numpy(offsets).cuda()
+    probd = to_dev(prob, "f32")
+    a = torch.full((P, F), float("nan"), dtype=torch.bfloat16, device="cuda")
+    save = torch.full((P, R1), float("nan"), dtype=torch.bfloat16, device="cuda")
+    y_perm = torch.full((P, h), float("nan"), dtype=torch.bfloat16, device="cuda")
+    M.moe_expert_fc1(cfg, dv(x_perm), offs, probd, dv(w1), dv(b1), save, a)
+    M.moe_expert_fc2(cfg, a, offs, probd, dv(w2), dv(b2), y_perm)
+    a_g = torch.full((P, F), float("nan"), dtype=torch.bfloat16, device="cuda")
+    save_g = torch.full((P, R1), float("nan"), dtype=torch.bfloat16, device="cuda")
+    cfg_g = M.make_config(T, h, E, 1, F, M.MOE_BF16, M.MOE_SCORE_SOFTMAX, act, int(bias), 0,
+                          M.MOE_FLAG_RENORM | M.MOE_FLAG_GEMM_2CTA)
+    assert P <= T
+    M.moe_expert_fc1_gather(cfg_g, dv(x), torch.from_numpy(src_token).cuda(), offs, probd,
+                            dv(w1), dv(b1), save_g, a_g)
+    torch.cuda.synchronize()
+    assert M.moe_get_error() == M.MOE_OK
+    assert torch.equal(a, a_g) and torch.equal(save, save_g)
+    ref = np.zeros((P, h))
+    ref_h = np.zeros((P, R1))
+    for e in range(E):
+        r = slice(offsets[e], offsets[e + 1])
+        if counts[e] == 0:
+            continue
+        b1e = None if b1 is None else b1[e]
+        b2e = None if b2 is None else b2[e]
+        ref[r] = prob[r, None] * O.expert_ffn(x_perm[r], w1[e], w2[e], act, b1e, b2e)
+        ref_h[r] = O.expert_hidden(x_perm[r], w1[e], b1e, act)[0]
+    ok, err, bound = tol_ok(to_np(y_perm), ref, "bf16")
+    assert ok, (err, bound)
+    ok, err, bound = tol_ok(to_np(save), ref_h, "bf16")
+    assert ok, ("act_save", err, bound)
+
+
 def small_workloads():
     return [
         W.TINY,
