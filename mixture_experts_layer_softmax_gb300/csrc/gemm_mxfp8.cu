@@ -498,22 +498,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (MODE == kMxSwiGLU) {
         // columns: gate hf*64 .. +63 and the matching up columns (two 32-wide chunks)
         const float pr = (p.prob && valid) ? __ldg(p.prob + row) : 1.f;
-        float a[2][32];
+        // all of this warp's TMEM reads first (gate and up, two 32-column
+        // chunks each), then the release, then the math: the next tile's MMAs
+        // need not wait for the SiLU evaluations
+        uint32_t g[2][32], u[2][32];
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
-          uint32_t g[32], u[32];
           const int col = hf * 64 + c * 32;
-          tc::tmem_ld_32x32b_x32(tbase + col, g);
-          tc::tmem_ld_32x32b_x32(tbase + 128 + col, u);
-          if (c == 1) {  // this warp's TMEM reads of the tile are done
-            tc::fence_before_sync();
-            __syncwarp();
-            if (lane == 0) tc::mbar_arrive(tc::smem_u32(&ctl.tmem_empty));
-          }
+          tc::tmem_ld_32x32b_x32(tbase + col, g[c]);
+          tc::tmem_ld_32x32b_x32(tbase + 128 + col, u[c]);
+        }
+        tc::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(tc::smem_u32(&ctl.tmem_empty));
+        float a[2][32];
+#pragma unroll
+        for (int c = 0; c < 2; ++c)
 #pragma unroll
           for (int j = 0; j < 32; ++j)
-            a[c][j] = pr * (silu_f(__uint_as_float(g[j])) * __uint_as_float(u[j]));
-        }
+            a[c][j] = pr * (silu_f(__uint_as_float(g[c][j])) * __uint_as_float(u[c][j]));
         uint32_t codes = 0;  // this warp's 2 of the row's 4 block scales
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
