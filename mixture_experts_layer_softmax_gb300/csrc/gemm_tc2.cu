@@ -9,7 +9,14 @@
 // CTA issues one M256 N256 K16 MMA over both CTAs' shared memory, and each
 // CTA's TMEM receives its own 128 rows x 256 fp32 columns.  Against the 1-CTA
 // kernel this halves the B bytes each SM pulls from L2 and its shared-memory
-// stage (32 KB, so 6 stages fit).
+// stage.
+//
+// A ring stage is 128 deep in K (two 64-column TMA boxes per operand, 64 KB
+// per CTA, 3 stages): 8 MMAs per stage wait, fence and commit once.  The MMA
+// thread spends some 60-75 cycles issuing each tcgen05 instruction; with
+// 64-deep stages its 4 MMAs, commit, barrier wait and bookkeeping took about
+// as long as the 512 cycles the 4 MMAs run, and the tensor pipe idled between
+// stages.
 //
 // Half tiles: an expert's last row block with at most 128 rows is computed
 // as a 128 x 256 tile (M128 N256 K16 pair MMAs, which take half the cycles
@@ -39,11 +46,14 @@ constexpr int BM = 128;  // rows per CTA; the cluster tile is 256 rows
 constexpr int BMC = 256;
 constexpr int BN = 256;  // accumulator columns
 constexpr int BNL = 128; // B rows each CTA loads
-constexpr int BK = 64;
-constexpr int A_BYTES = BM * BK * 2;   // 16 KB
-constexpr int B_BYTES = BNL * BK * 2;  // 16 KB
+constexpr int BK = 64;                  // K columns per TMA box (one 128-byte swizzle row)
+constexpr int KSUB = 2;                 // boxes per operand per stage: stages are 128 deep in K
+constexpr int SUB_A = BM * BK * 2;      // 16 KB
+constexpr int SUB_B = BNL * BK * 2;     // 16 KB
+constexpr int A_BYTES = KSUB * SUB_A;   // 32 KB
+constexpr int B_BYTES = KSUB * SUB_B;   // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int STAGES = 6;
+constexpr int STAGES = 3;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int kThreads = 192;
 
@@ -129,9 +139,10 @@ MOE_D void tma_gather4_pair(uint32_t dst, const CUtensorMap* map, int32_t c0, in
       : "memory");
 }
 
-// Bytes both CTAs' loads of one stage deliver (the even CTA's expect_tx).
+// Bytes both CTAs' loads of one stage deliver (the even CTA's expect_tx); a
+// half tile loads 64 A rows per CTA.
 MOE_D uint32_t stage_tx(bool half) {
-  return half ? 2u * (A_BYTES / 2 + B_BYTES) : 2u * STAGE_BYTES;
+  return 2u * KSUB * ((half ? SUB_A / 2 : SUB_A) + SUB_B);
 }
 
 // First weight row this CTA loads for N block nb of expert e.  SwiGLU (B =
@@ -166,7 +177,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int cid = blockIdx.x >> 1, ncl = gridDim.x >> 1;
   const int E = p.E;
   const int nblk = MODE == kSwiGLU ? (p.N + BNL - 1) / BNL : (p.N + BN - 1) / BN;
-  const int KB = (p.Kd + BK - 1) / BK;
+  const int KB = (p.Kd + KSUB * BK - 1) / (KSUB * BK);  // 128-deep stages (a box past Kd reads zeros)
   auto b_first_row = [](const Tc2Params& pp, int e, int nb, uint32_t r, bool half) {
     return b_first_row_t<MODE>(pp, e, nb, r, half);
   };
@@ -176,7 +187,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                    int n_rows, bool half, uint32_t bar) {
     if (MODE == kSwiGLU && half) {
       tma_load_2d_pair(dst, m64, k, row, bar);
-      tma_load_2d_pair(dst + B_BYTES / 2, m64, k, row + n_rows, bar);
+      tma_load_2d_pair(dst + SUB_B / 2, m64, k, row + n_rows, bar);
     } else {
       tma_load_2d_pair(dst, m128, k, row, bar);
     }
@@ -260,12 +271,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const uint32_t full_even = mapa(full_local, 0);
         if (lane == 0) {
           if (even) tc::mbar_arrive_expect_tx(full_local, stage_tx(half));
-          load_b(tc::smem_u32(sB + stage * B_BYTES), &tmB, &tmB64, kb * BK, b_row, p.N, half,
-                 full_even);
+#pragma unroll
+          for (int j = 0; j < KSUB; ++j)
+            load_b(tc::smem_u32(sB + stage * B_BYTES + j * SUB_B), &tmB, &tmB64, (kb * KSUB + j) * BK,
+                   b_row, p.N, half, full_even);
         }
-        if (gl)
-          tma_gather4_pair(tc::smem_u32(sA + stage * A_BYTES) + lane * 512, &tmA, kb * BK, rows,
-                           full_even);
+        if (gl) {
+#pragma unroll
+          for (int j = 0; j < KSUB; ++j)
+            tma_gather4_pair(tc::smem_u32(sA + stage * A_BYTES + j * SUB_A) + lane * 512, &tmA,
+                             (kb * KSUB + j) * BK, rows, full_even);
+        }
         issued |= 1u << stage;
         issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
         if (++stage == STAGES) { stage = 0; phase ^= 1; }
@@ -293,10 +309,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const uint32_t full_local = tc::smem_u32(&ctl.full[stage]);
           if (even) tc::mbar_arrive_expect_tx(full_local, stage_tx(half));
           const uint32_t full_even = mapa(full_local, 0);
-          tma_load_2d_pair(tc::smem_u32(sA + stage * A_BYTES), half ? &tmA64 : &tmA, kb * BK, a_row,
-                           full_even);
-          load_b(tc::smem_u32(sB + stage * B_BYTES), &tmB, &tmB64, kb * BK, b_row, p.N, half,
-                 full_even);
+#pragma unroll
+          for (int j = 0; j < KSUB; ++j) {
+            tma_load_2d_pair(tc::smem_u32(sA + stage * A_BYTES + j * SUB_A), half ? &tmA64 : &tmA,
+                             (kb * KSUB + j) * BK, a_row, full_even);
+            load_b(tc::smem_u32(sB + stage * B_BYTES + j * SUB_B), &tmB, &tmB64, (kb * KSUB + j) * BK,
+                   b_row, p.N, half, full_even);
+          }
           issued |= 1u << stage;
           issued_par = (issued_par & ~(1u << stage)) | (phase << stage);
           if (++stage == STAGES) { stage = 0; phase ^= 1; }
@@ -332,9 +351,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const uint32_t a0 = tc::smem_u32(sA + stage * A_BYTES);
           const uint32_t b0 = tc::smem_u32(sB + stage * B_BYTES);
 #pragma unroll
-          for (int k = 0; k < BK / 16; ++k)
-            mma_pair(d, tc::desc_kmajor_sw128(a0 + k * 32), tc::desc_kmajor_sw128(b0 + k * 32), idesc,
-                     (kb | k) != 0);
+          for (int j = 0; j < KSUB; ++j)
+#pragma unroll
+            for (int k = 0; k < BK / 16; ++k)
+              mma_pair(d, tc::desc_kmajor_sw128(a0 + j * SUB_A + k * 32),
+                       tc::desc_kmajor_sw128(b0 + j * SUB_B + k * 32), idesc, (kb | j | k) != 0);
           commit_pair_multicast(tc::smem_u32(&ctl.empty[stage]), 0x3);
           if (++stage == STAGES) { stage = 0; phase ^= 1; }
         }
