@@ -13,9 +13,10 @@
 //
 // A ring stage is 128 deep in K (two 64-column TMA boxes per operand, 64 KB
 // per CTA, 3 stages): 8 MMAs per stage wait, fence and commit once.  The MMA
-// thread spends some 60-75 cycles issuing each tcgen05 instruction; with
-// 64-deep stages its 4 MMAs, commit, barrier wait and bookkeeping took about
-// as long as the 512 cycles the 4 MMAs run, and the tensor pipe idled between
+// thread spends about 190 cycles observing a stage barrier (even one whose
+// phase completed long before) and 45-75 issuing each tcgen05 instruction;
+// with 64-deep stages its wait, 4 MMAs, commit and bookkeeping took about as
+// long as the 512 cycles the 4 MMAs run, and the tensor pipe idled between
 // stages.
 //
 // Half tiles: an expert's last row block with at most 128 rows is computed
