@@ -34,7 +34,10 @@
 //                 bytes; both CTAs' TMA loads complete on it (.cta_group::2).
 //   empty[s]      both CTAs: the even CTA's MMA commit arrives on both (multicast).
 //   tmem_full[a]  both CTAs: multicast commit after a tile's last MMA.
-//   tmem_empty[a] even CTA, count 8: the 4 epilogue warps of each CTA.
+//   tmem_empty[a] even CTA: one arrival per epilogue warp of each CTA.  FC1
+//                 has 8 epilogue warps (two per TMEM lane quarter, each storing
+//                 half of the quarter's columns; its SwiGLU/GELU epilogue writes
+//                 more per tile than FC2's), FC2 has 4.
 //   drain         both CTAs: a final multicast commit, so no MMA completion can
 //                 still be in flight towards a CTA that is leaving.
 // TMEM is allocated and freed with cta_group::2 by one warp of each CTA.
@@ -56,9 +59,11 @@ constexpr int B_BYTES = KSUB * SUB_B;   // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int STAGES = 3;
 constexpr uint32_t TMEM_COLS = 512;
-constexpr int kThreads = 192;
-
 enum Tc2Mode { kSwiGLU = 0, kGelu = 1, kFc2 = 2 };
+
+// epilogue warps per CTA, and the CTA size: producer, MMA issuer, epilogue
+MOE_HD constexpr int epi_warps(int mode) { return mode == kFc2 ? 4 : 8; }
+MOE_HD constexpr int cta_threads(int mode) { return 32 * (2 + epi_warps(mode)); }
 
 struct Tc2Params {
   const int32_t* offsets;
@@ -160,7 +165,7 @@ MOE_D int b_first_row_t(const Tc2Params& p, int e, int nb, uint32_t rank, bool h
 }
 
 template <int MODE, bool GATHER>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(cta_threads(MODE), 1)
     grouped_gemm_tc2_kernel(const __grid_constant__ CUtensorMap tmA,
                             const __grid_constant__ CUtensorMap tmB,
                             const __grid_constant__ CUtensorMap tmA64,
@@ -201,7 +206,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       tc::mbar_init(tc::smem_u32(&ctl.tmem_full[a]), 1);
-      tc::mbar_init(tc::smem_u32(&ctl.tmem_empty[a]), 8);
+      tc::mbar_init(tc::smem_u32(&ctl.tmem_empty[a]), 2 * epi_warps(MODE));
     }
     tc::mbar_init(tc::smem_u32(&ctl.drain), 1);
     ctl.abort = 0;
@@ -215,7 +220,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tmem_alloc_pair(tc::smem_u32(&ctl.tmem_base), TMEM_COLS);
     tmem_relinquish_pair();
   }
-  for (int e = threadIdx.x; e <= E; e += kThreads) ctl.off[e] = __ldg(p.offsets + e);
+  for (int e = threadIdx.x; e <= E; e += cta_threads(MODE)) ctl.off[e] = __ldg(p.offsets + e);
   __syncthreads();
   if (warp == 2) {
     int running = 0;
@@ -369,8 +374,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
   } else {
-    // ================= epilogue (warps 2..5, both CTAs) =================
+    // ================= epilogue (warps 2..9, both CTAs) =================
+    // epi_warps / 4 warps per TMEM lane quarter q; warp hf of them takes that
+    // share of the quarter's accumulator columns
+    constexpr int NW = epi_warps(MODE) / 4;
     const int q = warp & 3;
+    const int hf = (warp - 2) >> 2;
     int acc = 0;
     uint32_t acc_phase = 0;
     const uint32_t tmem_empty_even0 = mapa(tc::smem_u32(&ctl.tmem_empty[0]), 0);
@@ -382,9 +391,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (!tc::mbar_wait(tc::smem_u32(&ctl.tmem_full[acc]), acc_phase, wc)) break;
       tc::fence_after_sync();
       const int m_e = ctl.off[e + 1] - ctl.off[e];
-      // Full tile: warp q holds rows 32q.. of the CTA's 128, every column.
-      // Half tile: warps 0-1 and 2-3 hold the same 64 rows (lanes 0-63 and
-      // 64-127), warps 2-3 the second half of the output columns.
+      // Full tile: lane quarter q holds rows 32q.. of the CTA's 128, every
+      // column.  Half tile: quarters 0-1 and 2-3 hold the same 64 rows (lanes
+      // 0-63 and 64-127), quarters 2-3 the second half of the output columns.
       const int local_row = half ? mb * BMC + (int)rank * (BM / 2) + (q & 1) * 32 + lane
                                  : mb * BMC + (int)rank * BM + q * 32 + lane;
       const int col_half = half ? (q >> 1) : 0;
@@ -397,7 +406,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int ncol = half ? BNL / 2 : BNL;
         const int n0 = nb * BNL + col_half * (BNL / 2);
 #pragma unroll 1
-        for (int c = 0; c < ncol / 32; ++c) {
+        for (int c = hf * (ncol / 32 / NW); c < (hf + 1) * (ncol / 32 / NW); ++c) {
           uint32_t g[32], u[32];
           tc::tmem_ld_32x32b_x32(tbase + c * 32, g);
           tc::tmem_ld_32x32b_x32(tbase + ncol + c * 32, u);
@@ -425,7 +434,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int ncol = half ? BN / 2 : BN;
         const int n0 = nb * BN + col_half * (BN / 2);
 #pragma unroll 1
-        for (int c = 0; c < ncol / 32; ++c) {
+        for (int c = hf * (ncol / 32 / NW); c < (hf + 1) * (ncol / 32 / NW); ++c) {
           uint32_t r[32];
           tc::tmem_ld_32x32b_x32(tbase + c * 32, r);
           const int n = n0 + c * 32;
@@ -497,14 +506,14 @@ cudaError_t launch_mode2(const CUtensorMap& a, const CUtensorMap& b, const CUten
   int max_clusters = 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * (unsigned)((sms + 1) / 2));
-  cfg.blockDim = dim3(kThreads);
+  cfg.blockDim = dim3(cta_threads(MODE));
   cfg.dynamicSmemBytes = kSmemBytes;
   cfg.stream = s;
   if (cudaOccupancyMaxActiveClusters(&max_clusters, kern, &cfg) != cudaSuccess ||
       max_clusters < 1)
     max_clusters = sms / 2;
   const int64_t pairs = tiles < max_clusters ? tiles : max_clusters;
-  kern<<<(unsigned)(2 * pairs), kThreads, kSmemBytes, s>>>(a, b, a64, b64, p);
+  kern<<<(unsigned)(2 * pairs), cta_threads(MODE), kSmemBytes, s>>>(a, b, a64, b64, p);
   return cudaGetLastError();
 }
 
