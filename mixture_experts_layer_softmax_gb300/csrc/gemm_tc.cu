@@ -37,7 +37,6 @@ namespace {
 
 constexpr int BM = 128, BK = 64;
 constexpr int A_BYTES = BM * BK * 2;  // 16 KB
-constexpr int kThreads = 192;
 
 // Tile width BN (accumulator columns; 256 for the expert GEMMs, narrower for
 // the router's few output columns) fixes the B stage size, the ring depth
@@ -57,6 +56,13 @@ struct Tile {
 };
 
 enum TcMode { kTcSwiGLU = 0, kTcGelu = 1, kTcFc2 = 2, kTcF32 = 3 };
+
+// Epilogue warps per CTA: FC1's SwiGLU/GELU epilogue writes more per tile
+// than the others and gets two warps per TMEM lane quarter (each storing half
+// of the quarter's columns), so that it keeps up with tiles of short K; the
+// CTA is the producer, the MMA issuer and the epilogue warps.
+MOE_HD constexpr int epi_warps(int mode) { return mode == kTcSwiGLU || mode == kTcGelu ? 8 : 4; }
+MOE_HD constexpr int cta_threads(int mode) { return 32 * (2 + epi_warps(mode)); }
 
 struct TcParams {
   const int32_t* offsets;        // [E+1]
@@ -138,7 +144,7 @@ MOE_D void store8(__nv_bfloat16* dst, const float* v) {
 // on the stage barrier like the tiled loads.  Rows past the expert's end load
 // token row 0 (their outputs are never stored).
 template <int MODE, int BNT, bool GATHER = false>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(cta_threads(MODE), 1)
     grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                            const __grid_constant__ CUtensorMap tmB, const TcParams p) {
   constexpr int BN = Tile<BNT>::BN;
@@ -169,7 +175,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       tc::mbar_init(tc::smem_u32(&ctl.tmem_full[a]), 1);
-      tc::mbar_init(tc::smem_u32(&ctl.tmem_empty[a]), 4);
+      tc::mbar_init(tc::smem_u32(&ctl.tmem_empty[a]), epi_warps(MODE));
     }
     tc::mbar_init(tc::smem_u32(&ctl.drain), 1);
     ctl.abort = 0;
@@ -182,7 +188,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::tmem_alloc(tc::smem_u32(&ctl.tmem_base), TMEM_COLS);
     tc::tmem_relinquish();
   }
-  for (int e = threadIdx.x; e <= E; e += kThreads) ctl.off[e] = __ldg(p.offsets + e);
+  for (int e = threadIdx.x; e <= E; e += cta_threads(MODE)) ctl.off[e] = __ldg(p.offsets + e);
   __syncthreads();
   if (warp == 2) {  // tile_start = exclusive scan of m-blocks x n-blocks
     int running = 0;
@@ -341,8 +347,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
   } else {
-    // ================= epilogue (warps 2..5) =================
-    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    // ================= epilogue (warps 2 ..) =================
+    // epi_warps / 4 warps per TMEM lane quarter q (the quarter this warp may
+    // access); warp hf of them takes that share of the quarter's columns
+    constexpr int NW = epi_warps(MODE) / 4;
+    const int q = warp & 3;
+    const int hf = (warp - 2) >> 2;
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
@@ -358,7 +368,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t tbase = tmem_base + (uint32_t)(acc * ACC_STRIDE) + ((uint32_t)(q * 32) << 16);
       if (MODE == kTcSwiGLU) {
 #pragma unroll 1
-        for (int c = 0; c < BN / 2 / 32; ++c) {
+        for (int c = hf * (BN / 2 / 32 / NW); c < (hf + 1) * (BN / 2 / 32 / NW); ++c) {
           uint32_t g[32], u[32];
           tc::tmem_ld_32x32b_x32(tbase + c * 32, g);
           tc::tmem_ld_32x32b_x32(tbase + BN / 2 + c * 32, u);
@@ -405,7 +415,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       } else {
 #pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
+        for (int c = hf * (BN / 32 / NW); c < (hf + 1) * (BN / 32 / NW); ++c) {
           uint32_t r[32];
           tc::tmem_ld_32x32b_x32(tbase + c * 32, r);
           const int n = nb * BN + c * 32;
@@ -471,7 +481,7 @@ cudaError_t launch_mode(const CUtensorMap& a, const CUtensorMap& b, const TcPara
   cudaError_t e =
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
   if (e != cudaSuccess) return e;
-  kern<<<grid, kThreads, bytes, s>>>(a, b, p);
+  kern<<<grid, cta_threads(MODE), bytes, s>>>(a, b, p);
   return cudaGetLastError();
 }
 
