@@ -130,11 +130,11 @@ MOE_D void store8(__nv_bfloat16* dst, const float* v) {
 
 // GATHER: the A rows are not a permuted buffer's consecutive rows but the
 // token rows x[src_token[r]], fetched by the TMA engine with tile::gather4
-// loads (four token rows per load, the x map's box one row high): the
-// producer warp's 32 lanes each fetch 4 of the CTA's 128 rows per stage into
-// the same 128-byte-swizzled layout, completing on the same stage barrier as
-// the tiled loads.  Rows past the expert's end load token row 0 (their
-// outputs are never stored).
+// loads (four token rows per load, the x map's box one row high): per
+// 64-column box the producer warp's 32 lanes each fetch 4 of the CTA's 128
+// rows (a half tile's 64 rows: lanes 0-15) into the same 128-byte-swizzled
+// layout, completing on the same stage barrier as the tiled loads.  Rows past
+// the expert's end load token row 0 (their outputs are never stored).
 MOE_D void tma_gather4_pair(uint32_t dst, const CUtensorMap* map, int32_t c0, int4 rows,
                             uint32_t bar_cluster) {
   asm volatile(
@@ -187,8 +187,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(cta_threads(MODE), 1
   auto b_first_row = [](const Tc2Params& pp, int e, int nb, uint32_t r, bool half) {
     return b_first_row_t<MODE>(pp, e, nb, r, half);
   };
-  // The B rows of one stage: one 128-row box, or for a SwiGLU half tile a
-  // 64-row box of gate rows and one of the matching up rows (p.N rows further).
+  // The B rows of one 64-column box: one 128-row box, or for a SwiGLU half
+  // tile a 64-row box of gate rows and one of the matching up rows (p.N rows
+  // further).
   auto load_b = [](uint32_t dst, const CUtensorMap* m128, const CUtensorMap* m64, int k, int row,
                    int n_rows, bool half, uint32_t bar) {
     if (MODE == kSwiGLU && half) {
