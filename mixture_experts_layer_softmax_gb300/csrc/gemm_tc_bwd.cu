@@ -24,7 +24,12 @@
 // MMA warp, 4 epilogue warps, TMEM 2 x 256 columns, bounded waits.  The data
 // gradients use a 4-stage ring of 48 KB; the weight gradient 2 stages of
 // 96 KB (one 128-row block of the expert per stage) and streams its output
-// through 32 KB of staging with TMA stores.  MN-major tiles are {64 elements,
+// through 32 KB of staging with TMA stores.  The weight gradient of an expert
+// without rows is zero: its tiles never reach the producer or the MMA warp;
+// the epilogue warps write them with plain 16-byte stores, interleaved with
+// the computed tiles (each CTA spreads its share of zero tiles evenly between
+// its computed ones), so that those stores overlap the computed tiles' operand
+// loads instead of idling the loads and MMAs for rounds of empty experts.  MN-major tiles are {64 elements,
 // BK K-rows} TMA boxes with 128-byte swizzle: LBO = 64 x BK x 2 bytes between
 // 64-element atoms, SBO = 1 KB between 8-row groups.
 #include "tc_ptx.cuh"
@@ -68,6 +73,9 @@ struct BwdParams {
 
 template <int STAGES, int NTS>
 struct SmemCtl {
+  uint8_t with_rows[256];  // wgrad: experts with rows, in order (E <= 256)
+  uint8_t no_rows[256];    // wgrad: experts without rows
+  int n_with_rows, n_no_rows;
   uint64_t full[STAGES], empty[STAGES], tmem_full[2], tmem_empty[2], drain;
   uint32_t tmem_base;
   int abort;
@@ -200,16 +208,32 @@ MOE_D void wgrad_store_tile(uint32_t tbase, bool have_rows, int e, int mb, int n
   store(3);
 }
 
+// One epilogue warp's share of a zero weight-gradient tile (an expert without
+// rows): its 32 rows of the 128 x 256 tile, one row per instruction, 32 lanes
+// x 16 bytes = 256 bf16 columns, coalesced; rows past M and columns past N are
+// skipped (N is a multiple of 8).
+MOE_D void wgrad_zero_tile(__nv_bfloat16* out, int M, int N, int e, int mb, int nb, int q,
+                           int lane) {
+  const int col = nb * BN + lane * 8;
+  if (col >= N) return;
+  for (int r = 0; r < 32; ++r) {
+    const int row = mb * BM + q * 32 + r;
+    if (row >= M) break;
+    *reinterpret_cast<uint4*>(out + ((int64_t)e * M + row) * N + col) = make_uint4(0, 0, 0, 0);
+  }
+}
+
 template <int KIND>
 struct Tiles {
   // dgrad: row tiles of each expert x N tiles; wgrad: M tiles x N tiles per expert
   template <typename Ctl>
   MOE_D static void decode(const Ctl& c, int E, int mt, int nt, int tile, int& e, int& mb,
                            int& nb) {
-    if (KIND == kWgrad) {
+    if (KIND == kWgrad) {  // tile indexes the computed tiles: those of experts with rows
       const int tpe = mt * nt;
-      e = tile / tpe;
-      const int local = tile - e * tpe;
+      const int k = tile / tpe;
+      e = c.with_rows[k];
+      const int local = tile - k * tpe;
       nb = local / mt;
       mb = local - nb * mt;
       return;
@@ -277,7 +301,25 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   if (warp == 2) {
     if (KIND == kWgrad) {
-      if (lane == 0) ctl.total = E * mt * nt;
+      // the experts with rows and those without, each in expert order
+      int n_ne = 0, n_z = 0;
+      for (int e0 = 0; e0 < E; e0 += 32) {
+        const int e = e0 + lane;
+        const bool in = e < E;
+        const bool has = in && ctl.off[e + 1] > ctl.off[e];
+        const uint32_t m_has = __ballot_sync(0xffffffffu, has);
+        const uint32_t m_none = __ballot_sync(0xffffffffu, in && !has);
+        const uint32_t below = (1u << lane) - 1u;
+        if (has) ctl.with_rows[n_ne + __popc(m_has & below)] = (uint8_t)e;
+        if (in && !has) ctl.no_rows[n_z + __popc(m_none & below)] = (uint8_t)e;
+        n_ne += __popc(m_has);
+        n_z += __popc(m_none);
+      }
+      if (lane == 0) {
+        ctl.n_with_rows = n_ne;
+        ctl.n_no_rows = n_z;
+        ctl.total = n_ne * mt * nt;  // computed tiles
+      }
     } else {
       int running = 0;
       for (int e0 = 0; e0 < E; e0 += 32) {
@@ -419,16 +461,39 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp & 3;
     int acc = 0;
     uint32_t acc_phase = 0;
+    // wgrad: this CTA's zero tiles (index zi = blockIdx.x + j * gridDim.x over
+    // the tiles of experts without rows), spread evenly between its computed
+    // tiles: after its k-th computed tile the first k * nz / nc of them
+    const int tpe = mt * nt;
+    const int G = (int)gridDim.x, b = (int)blockIdx.x;
+    const int nzt = KIND == kWgrad ? ctl.n_no_rows * tpe : 0;
+    const int nc = total > b ? (total - b + G - 1) / G : 0;
+    const int nz = nzt > b ? (nzt - b + G - 1) / G : 0;
+    int zdone = 0, kc = 0;
+    bool aborted = false;
+    auto zero_upto = [&](int target) {
+      for (; zdone < target; ++zdone) {
+        const int zi = b + zdone * G;
+        const int k = zi / tpe, local = zi - k * tpe;
+        const int nbz = local / mt, mbz = local - nbz * mt;
+        wgrad_zero_tile(p.out, p.M, p.N, ctl.no_rows[k], mbz, nbz, q, lane);
+      }
+    };
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
       int e, mb, nb;
       Tiles<KIND>::decode(ctl, E, mt, nt, tile, e, mb, nb);
       const int m_e = ctl.off[e + 1] - ctl.off[e];
-      if (!tc::mbar_wait(tc::smem_u32(&ctl.tmem_full[acc]), acc_phase, wc)) break;
+      if (!tc::mbar_wait(tc::smem_u32(&ctl.tmem_full[acc]), acc_phase, wc)) {
+        aborted = true;
+        break;
+      }
       tc::fence_after_sync();
       const uint32_t tbase = tmem_base + (uint32_t)(acc * BN) + ((uint32_t)(q * 32) << 16);
       if (KIND == kWgrad) {
         wgrad_store_tile(tbase, m_e > 0, e, mb, nb, q, lane, sC, &tmC,
                          tc::smem_u32(&ctl.tmem_empty[acc]));
+        ++kc;
+        zero_upto((int)((int64_t)kc * nz / nc));
       } else {
         const int local_row = mb * BM + q * 32 + lane;
         const bool valid = local_row < m_e;
@@ -476,6 +541,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1;
     }
+    if (KIND == kWgrad && !aborted) zero_upto(nz);  // the rest (all of them when nc = 0)
     if (KIND == kWgrad && lane == 0) bulk_wait0();  // every TMA store has completed
   }
   tc::fence_before_sync();
